@@ -1,0 +1,206 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module draws random matrices and lays them out in memory; it holds none of
+the GEMM's arithmetic.  Both the parity tests (GPU library vs CPU oracle) and
+the benchmark draw their inputs here, so both sides read the same bytes.
+
+Recipe: one CPU ``torch.Generator`` seeded per problem; values are drawn in the
+order A, B, C, bias, each in logical row-major order (A is M x K, B is K x N,
+C is M x N); floating values are drawn in fp32 and rounded once (round to
+nearest even) to the storage type; the logical matrix is then written into its
+storage layout (N = column-major, T = row-major) with an optional padded leading
+dimension whose padding holds a poison value (NaN for floats, 127 for int8) so
+that a kernel reading outside the logical matrix is caught.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import torch
+
+TORCH_DTYPES = {
+    "f32": torch.float32,
+    "f16": torch.float16,
+    "bf16": torch.bfloat16,
+    "s8": torch.int8,
+    "s32": torch.int32,
+}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "s8": 1, "s32": 4}
+
+BASE_SEED = 20261202
+
+
+@dataclass(frozen=True)
+class Dist:
+    """A value distribution: 'uniform' on [lo, hi], 'normal' with std `std`,
+    'int' uniform on the integers lo..hi inclusive, or 'small' uniform on the
+    integers lo..hi (exactly representable in every input type)."""
+    kind: str
+    lo: float = -1.0
+    hi: float = 1.0
+    std: float = 1.0
+
+
+U11 = Dist("uniform", -1.0, 1.0)
+I8 = Dist("int", -128, 127)
+
+
+@dataclass(frozen=True)
+class Problem:
+    name: str
+    ab: str               # 'f16' | 'bf16' | 's8' | 'f32'
+    layout_a: str         # 'N' | 'T'
+    layout_b: str
+    M: int
+    N: int
+    K: int
+    alpha: float = 1.0
+    beta: float = 0.0
+    c: Optional[str] = None      # dtype of C (None: beta == 0, C not allocated)
+    d: str = "f32"               # dtype of D
+    bias: Optional[str] = None   # dtype of the bias vector
+    bias_mode: str = "none"      # 'none' | 'col' | 'row'
+    act: str = "none"            # 'none' | 'relu'
+    dist_a: Dist = U11
+    dist_b: Dist = U11
+    dist_c: Dist = Dist("normal", std=1.0)
+    dist_bias: Dist = Dist("normal", std=0.1)
+    pad_a: int = 0               # extra leading-dimension elements (poisoned)
+    pad_b: int = 0
+    pad_c: int = 0
+    pad_d: int = 0
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def lda(self) -> int:
+        return (self.M if self.layout_a == "N" else self.K) + self.pad_a
+
+    @property
+    def ldb(self) -> int:
+        return (self.K if self.layout_b == "N" else self.N) + self.pad_b
+
+    @property
+    def ldc(self) -> int:
+        return self.N + self.pad_c
+
+    @property
+    def ldd(self) -> int:
+        return self.N + self.pad_d
+
+    def with_(self, **kw) -> "Problem":
+        return replace(self, **kw)
+
+
+@dataclass
+class Inputs:
+    A: torch.Tensor                # storage (2-D, contiguous), host
+    B: torch.Tensor
+    C: Optional[torch.Tensor]
+    bias: Optional[torch.Tensor]
+    problem: Problem
+    logical: dict = field(default_factory=dict)   # logical row-major copies (host)
+
+
+def _draw(gen: torch.Generator, rows: int, cols: int, dist: Dist, dtype: str) -> torch.Tensor:
+    shape = (rows, cols)
+    if dist.kind == "uniform":
+        x = torch.rand(shape, generator=gen, dtype=torch.float32) * (dist.hi - dist.lo) + dist.lo
+    elif dist.kind == "normal":
+        x = torch.randn(shape, generator=gen, dtype=torch.float32) * dist.std
+    elif dist.kind in ("int", "small"):
+        x = torch.randint(int(dist.lo), int(dist.hi) + 1, shape, generator=gen, dtype=torch.int64)
+    elif dist.kind == "zeros":
+        x = torch.zeros(shape, dtype=torch.float32)
+    elif dist.kind == "ones":
+        x = torch.ones(shape, dtype=torch.float32)
+    else:
+        raise ValueError(f"unknown distribution {dist.kind}")
+    return x.to(TORCH_DTYPES[dtype])
+
+
+def _poison(dtype: str):
+    return 127 if dtype == "s8" else (2147483647 if dtype == "s32" else float("nan"))
+
+
+def _store(logical: torch.Tensor, layout: str, ld: int, dtype: str) -> torch.Tensor:
+    """Write a logical (rows x cols) matrix into column- ('N') or row-major ('T')
+    storage with leading dimension ld.  Returns the 2-D storage tensor."""
+    rows, cols = logical.shape
+    if layout == "T":
+        st = torch.full((rows, ld), _poison(dtype), dtype=TORCH_DTYPES[dtype]) if ld > cols \
+            else torch.empty((rows, cols), dtype=TORCH_DTYPES[dtype])
+        st[:, :cols] = logical
+    else:
+        st = torch.full((cols, ld), _poison(dtype), dtype=TORCH_DTYPES[dtype]) if ld > rows \
+            else torch.empty((cols, rows), dtype=TORCH_DTYPES[dtype])
+        st[:, :rows] = logical.t()
+    return st.contiguous()
+
+
+def generate(p: Problem, seed: int, keep_logical: bool = False) -> Inputs:
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    a = _draw(gen, p.M, p.K, p.dist_a, p.ab)
+    b = _draw(gen, p.K, p.N, p.dist_b, p.ab)
+    c = _draw(gen, p.M, p.N, p.dist_c, p.c) if p.c is not None else None
+    nb = p.N if p.bias_mode == "col" else p.M
+    bias = _draw(gen, 1, nb, p.dist_bias, p.bias).reshape(nb) if p.bias_mode != "none" else None
+    A = _store(a, p.layout_a, p.lda, p.ab)
+    B = _store(b, p.layout_b, p.ldb, p.ab)
+    C = _store(c, "T", p.ldc, p.c) if c is not None else None
+    logical = {"a": a, "b": b, "c": c} if keep_logical else {}
+    return Inputs(A=A, B=B, C=C, bias=bias, problem=p, logical=logical)
+
+
+def sha256_of(t: torch.Tensor) -> str:
+    import hashlib
+    return hashlib.sha256(t.contiguous().view(torch.uint8).numpy().tobytes()).hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# The workloads (names say what they are, with their sizes).
+# ---------------------------------------------------------------------------
+
+def square_fp16_256() -> Problem:
+    """M=N=K=256, A row-major / B column-major fp16 in U[-1,1], fp32 D = A*B."""
+    return Problem("gemm_f16_tn_256", "f16", "T", "N", 256, 256, 256)
+
+
+def square_fp16_8192(layout: str) -> Problem:
+    """M=N=K=8192 fp16, fp32 C and D, alpha=1.5, beta=0.5, C ~ N(0,1)."""
+    return Problem(f"gemm_f16_{layout.lower()}_8192_ab", "f16", layout[0], layout[1],
+                   8192, 8192, 8192, alpha=1.5, beta=0.5, c="f32", d="f32")
+
+
+def fc_bf16_8192x4096x11008() -> Problem:
+    """X[8192,4096] bf16 ~ N(0,1) times W[4096,11008] bf16 ~ N(0,0.02), both
+    row-major, + bias[11008] ~ N(0,0.1), ReLU, bf16 D."""
+    return Problem("fc_bf16_8192x4096x11008_bias_relu", "bf16", "T", "T", 8192, 11008, 4096,
+                   d="bf16", bias="f32", bias_mode="col", act="relu",
+                   dist_a=Dist("normal", std=1.0), dist_b=Dist("normal", std=0.02),
+                   dist_bias=Dist("normal", std=0.1))
+
+
+def int8_8192() -> Problem:
+    """M=N=K=8192 int8 (uniform integers in [-128,127]), A row-major / B
+    column-major, int32 accumulate and output."""
+    return Problem("gemm_s8_tn_8192", "s8", "T", "N", 8192, 8192, 8192, d="s32",
+                   dist_a=I8, dist_b=I8)
+
+
+def sgemm_4096_bias_relu() -> Problem:
+    """fp32 SGEMM M=N=K=4096 (FFMA, no TF32), U[-1,1] inputs, bias ~ N(0,0.1), ReLU."""
+    return Problem("sgemm_f32_tn_4096_bias_relu", "f32", "T", "N", 4096, 4096, 4096,
+                   d="f32", bias="f32", bias_mode="col", act="relu")
+
+
+def square_fp16(n: int) -> Problem:
+    return Problem(f"gemm_f16_tn_{n}", "f16", "T", "N", n, n, n)
+
+
+def skinny_fp16_16384x64x16384() -> Problem:
+    return Problem("gemm_f16_tn_skinny_16384x64x16384", "f16", "T", "N", 16384, 64, 16384)

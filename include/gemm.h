@@ -1,0 +1,237 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) generalized GEMM library, libgemm.so.
+ *
+ *     D = epilogue( alpha * op(A) * op(B) + beta * C )
+ *     epilogue(v)[i,j] = cast_out( act( v[i,j] + bias ) )
+ *
+ * The operation is the BLAS-style scaled product C := alpha*A*B + beta*C of
+ * "CUTLASS: Fast Linear Algebra in CUDA C++" (section "Efficient Matrix
+ * Multiplication on GPUs"), with the transposition of the inputs of the
+ * BLAS-like interface in "Flexible Performant GEMM Kernels on GPUs" (section
+ * 4.3, Listings 10-11), the N (column-major) / T (row-major) operand layouts of
+ * that paper's section 5.1, and the fused epilogue of both pages: the
+ * fused_bias_relu_epilogue functor of the CUTLASS page ("Fusing Element-wise
+ * Operations: An Example with SGEMM": alpha*acc + bias + beta*c, then a ReLU
+ * clamp) and the bias vector added to every row in section 5.3 of the paper
+ * (Table 2).
+ *
+ * Conventions shared by every entry point:
+ *   - A is logically M x K, B is K x N, C and D are M x N.
+ *   - Layout N: column-major storage; element (r, c) at ptr[r + c*ld].
+ *     Layout T: row-major storage;    element (r, c) at ptr[r*ld + c].
+ *     (The paper's linearisation n*M + m of a column-major tile, section 3.2,
+ *     Figure 4, with the leading dimension in place of M.)
+ *   - C and D are always row-major: element (i, j) at ptr[i*ld + j], ld >= N.
+ *     A column-major D is obtained from the identity D^T = op(B)^T op(A)^T:
+ *     swap the operands, flip both layout letters and use GEMM_BIAS_ROW.
+ *   - All sizes and leading dimensions are in elements, not bytes.
+ *   - Device pointers (gemm_run) and the stream are owned by the caller; the
+ *     library never frees them.  A plan owns only its own device scratch
+ *     (an error word, and the int8 operand staging described at gemm_run).
+ *   - gemm_run is asynchronous on `stream`: its return value reports argument
+ *     and launch errors only.  Device-side failures surface at the caller's
+ *     stream synchronisation or through gemm_plan_device_status.
+ *   - No entry point falls back to the CPU.  Unsupported requests return
+ *     GEMM_ERR_UNSUPPORTED.
+ */
+#ifndef DENSE_GEMM_EPILOGUES_GB300_GEMM_H
+#define DENSE_GEMM_EPILOGUES_GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t is a pointer to this opaque driver type; 0 is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,  /* a size, leading dimension, pointer or enum is invalid */
+    GEMM_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement */
+    GEMM_ERR_ALIGNMENT = 3,    /* a forced kernel needs alignment the buffers lack */
+    GEMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (no device, launch error) */
+    GEMM_ERR_TIMEOUT = 5       /* a bounded in-kernel wait expired (read via gemm_plan_device_status) */
+} gemm_status_t;
+
+typedef enum { GEMM_OP_N = 0 /* column-major */, GEMM_OP_T = 1 /* row-major */ } gemm_layout_t;
+
+typedef enum {
+    GEMM_F32 = 0,
+    GEMM_F16 = 1,
+    GEMM_BF16 = 2,
+    GEMM_S8 = 3,
+    GEMM_S32 = 4
+} gemm_dtype_t;
+
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1 } gemm_act_t;
+
+typedef enum {
+    GEMM_BIAS_NONE = 0,
+    GEMM_BIAS_COL = 1, /* bias has N entries; bias[j] is added to column j of every row */
+    GEMM_BIAS_ROW = 2  /* bias has M entries; bias[i] is added to row i (transposed use) */
+} gemm_bias_mode_t;
+
+/* Fused epilogue.  Order: v = alpha*acc + beta*C[i,j] + bias; v = act(v);
+ * D[i,j] = cast to out_dtype (round to nearest even).  NULL epilogue pointer
+ * means: no bias, no activation, out_dtype equal to the plan's c_dtype. */
+typedef struct {
+    const void* bias;             /* device pointer, or NULL when bias_mode == GEMM_BIAS_NONE */
+    gemm_dtype_t bias_dtype;      /* F32/F16/BF16 for floating plans, S32 for int8 plans */
+    gemm_bias_mode_t bias_mode;
+    gemm_act_t act;
+    gemm_dtype_t out_dtype;       /* dtype of D */
+} gemm_epilogue_t;
+
+typedef struct gemm_plan* gemm_plan_t;
+
+/* Kernels the selector chooses between (gemm_config_t.kernel). */
+typedef enum {
+    GEMM_KERNEL_AUTO = 0,   /* let the selector decide (default) */
+    GEMM_KERNEL_NONE = 1,   /* nothing to launch (M == 0 or N == 0) */
+    GEMM_KERNEL_TC = 2,     /* tcgen05 + TMA persistent warp-specialised kernel, fp16/bf16 */
+    GEMM_KERNEL_TC_INT8 = 3,/* int8 exact: int8->fp16 staging, tcgen05 in K-chunks, int32 accumulation */
+    GEMM_KERNEL_FFMA = 4,   /* fp32 SGEMM on CUDA cores, register-blocked FFMA */
+    GEMM_KERNEL_SIMT = 5    /* generic CUDA-core kernel: any alignment, K == 0, every dtype */
+} gemm_kernel_t;
+
+/* A launch configuration (what the selector returns; what a run used). */
+typedef struct {
+    int32_t kernel;       /* gemm_kernel_t */
+    int32_t bm, bn, bk;   /* CTA tile (rows of D, columns of D, K per pipeline stage) */
+    int32_t stages;       /* shared-memory pipeline depth */
+    int32_t cta_group;    /* CTAs cooperating on one MMA tile (1 or 2) */
+    int32_t split_k;      /* K splits (1 = none) */
+    int32_t raster;       /* tile rows per raster group (L2 reuse) */
+    int32_t grid;         /* CTAs launched */
+    int32_t k_chunk;      /* int8 path: K elements per exact fp32 chunk; 0 otherwise */
+    int32_t tiles;        /* output tiles */
+    int32_t reserved;
+} gemm_config_t;
+
+/* ---------------------------------------------------------------------------
+ * gemm_plan_create -- make a plan for one device and one operand type.
+ *   plan      out: the new plan (owned by the caller, release with gemm_plan_destroy).
+ *   ab_dtype  type of A and B: GEMM_F16, GEMM_BF16 (tensor cores, fp32 accumulate),
+ *             GEMM_S8 (exact int32 accumulate), GEMM_F32 (CUDA-core FFMA, no TF32).
+ *   c_dtype   type of C: F32/F16/BF16 for 16-bit inputs, F32 for F32, S32 for S8.
+ *   device    CUDA device ordinal.
+ * Allocates a 4-byte device error word on `device`.  Returns GEMM_ERR_INVALID_ARG
+ * for a bad type pair, GEMM_ERR_CUDA when the device cannot be used.
+ * Paper counterpart: the get_config step of "Flexible Performant GEMM Kernels on
+ * GPUs" (section 4.3, Listing 9) and the plan-then-launch split of cuBLASLt
+ * discussed in its section 6.
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype,
+                               int device);
+
+/* Release a plan and its device scratch.  Synchronises the plan's device.  NULL is a no-op. */
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* ---------------------------------------------------------------------------
+ * gemm_run -- D = epilogue(alpha * op(A) * op(B) + beta * C) on `stream`.
+ *   layoutA/B   GEMM_OP_N (column-major) or GEMM_OP_T (row-major).
+ *   M, N, K     sizes (>= 0).  M == 0 or N == 0 returns GEMM_OK and launches
+ *               nothing; K == 0 gives D = epilogue(beta*C).
+ *   alpha,beta  scalars.  Floating plans apply them in fp32.  S8 plans require
+ *               integral values within int32 and apply them in int32.
+ *               beta == 0: C is not read (may be NULL; NaNs in C are ignored).
+ *   A, lda      device pointer, leading dimension: lda >= M for N, >= K for T.
+ *   B, ldb      device pointer, leading dimension: ldb >= K for N, >= N for T.
+ *   C, ldc      device pointer (row-major), ldc >= N when beta != 0.
+ *   D, ldd      device pointer (row-major), ldd >= N.  D may equal C only when
+ *               ldc == ldd and the types match (in-place C := ...).
+ *   epi         fused epilogue (NULL: none, out_dtype = c_dtype).
+ *   stream      CUDA stream (cudaStream_t) the kernels are enqueued on.
+ * Kernel choice: 16-byte aligned A/B with 16-byte multiple strides use the
+ * tcgen05 tensor-core kernel (S8: an int8->fp16 staging pass into plan-owned
+ * device scratch, grown on demand with stream-ordered allocation, then the
+ * tensor-core kernel in exact K-chunks); F32 uses the FFMA kernel; anything
+ * else uses the generic CUDA-core kernel.  All paths run on the GPU.
+ * Errors: GEMM_ERR_INVALID_ARG / GEMM_ERR_UNSUPPORTED before any launch;
+ * GEMM_ERR_CUDA when a launch or scratch allocation fails.
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                       int64_t M, int64_t N, int64_t K, double alpha,
+                       const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                       const void* C, int64_t ldc, void* D, int64_t ldd,
+                       const gemm_epilogue_t* epi, gemm_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gemm_run_host -- the same operation on HOST buffers (pinned or pageable).
+ * Copies A, B, C (when beta != 0) and the bias into plan-owned device staging
+ * (grown on demand), runs gemm_run on `stream`, copies D back to the host and
+ * synchronises `stream` before returning.  Arguments mean what they mean for
+ * gemm_run, with host pointers; the bias pointer in `epi` is a host pointer too.
+ * Host buffers stay owned by the caller.
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                            int64_t M, int64_t N, int64_t K, double alpha,
+                            const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                            const void* C, int64_t ldc, void* D, int64_t ldd,
+                            const gemm_epilogue_t* epi, gemm_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gemm_validate -- the argument checks gemm_run performs, on the host only
+ * (no device access; pointers are checked for NULL-ness, never dereferenced).
+ * Returns GEMM_OK when gemm_run would accept the arguments for a plan of
+ * (ab_dtype, c_dtype).
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_validate(gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype,
+                            gemm_layout_t layoutA, gemm_layout_t layoutB,
+                            int64_t M, int64_t N, int64_t K, double alpha,
+                            const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                            const void* C, int64_t ldc, const void* D, int64_t ldd,
+                            const gemm_epilogue_t* epi);
+
+/* ---------------------------------------------------------------------------
+ * gemm_select -- the tile-shape selector, on the host only.
+ *   Inputs are those of gemm_run (pointers are used for their alignment only,
+ *   never dereferenced) plus the SM count of the target device.
+ *   out   the kernel, tile, pipeline depth, raster group and grid gemm_run
+ *         would launch.
+ * Paper counterpart: the defaulting heuristics of the params abstraction in
+ * "Flexible Performant GEMM Kernels on GPUs" (section 4.2: the largest square
+ * or nearly-square tile that fits in shared memory) and the shape-keyed
+ * policies (a tall/skinny policy) of the CUTLASS page.
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_select(gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype,
+                          gemm_layout_t layoutA, gemm_layout_t layoutB,
+                          int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda, const void* B, int64_t ldb,
+                          const void* C, int64_t ldc, const void* D, int64_t ldd,
+                          double beta, const gemm_epilogue_t* epi, int sm_count,
+                          gemm_config_t* out);
+
+/* Force a kernel for subsequent runs of `plan` (GEMM_KERNEL_AUTO restores the
+ * selector).  A forced kernel that cannot serve a request makes gemm_run return
+ * GEMM_ERR_ALIGNMENT or GEMM_ERR_UNSUPPORTED instead of running another one. */
+gemm_status_t gemm_plan_set_kernel(gemm_plan_t plan, gemm_kernel_t kernel);
+
+/* The configuration the most recent successful gemm_run of `plan` launched. */
+gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_t* out);
+
+/* Synchronise `stream`, then read and clear the plan's device error word.
+ * *code is 0 when no kernel reported a failure; otherwise the status
+ * (GEMM_ERR_TIMEOUT) of the first failure since the last read. */
+gemm_status_t gemm_plan_device_status(gemm_plan_t plan, gemm_stream_t stream, int32_t* code);
+
+/* Set the bound of every in-kernel wait, in nanoseconds (default 4e9).  A wait
+ * that runs past it records GEMM_ERR_TIMEOUT in the error word and its CTA
+ * winds down (waiting, again bounded, for its own copies in flight and
+ * releasing its tensor memory) instead of spinning for ever. */
+gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* gemm_status_string(gemm_status_t status);
+
+/* ABI version of this header (major * 100 + minor). */
+int gemm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_EPILOGUES_GB300_GEMM_H */

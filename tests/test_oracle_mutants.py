@@ -1,0 +1,75 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case compiles a copy of oracle.c with one planted mistake (a dropped term,
+a wrong sign, a transposed index, a row/column mix-up, a wrong rounding rule)
+into a temporary library, points the oracle wrapper at it, and checks that at
+least one pin test fails.  Everything runs on the CPU.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle as O
+
+import test_oracle as T
+
+SRC = os.path.join(os.path.dirname(O.__file__), "oracle.c")
+
+MUTANTS = {
+    "drop_beta_term": ("v += p->beta * load_float", "v += 0.0 * load_float"),
+    "negated_alpha": ("double v = p->alpha * acc;", "double v = -p->alpha * acc;"),
+    "transposed_A_index": ("? i + k * lda : i * lda + k", "? k + i * lda : i * lda + k"),
+    "transposed_B_index": ("? k + j * ldb : k * ldb + j", "? k + j * ldb : j * ldb + k"),
+    "bias_indexed_by_row": ("if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, j);",
+                            "if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, i);"),
+    "relu_dropped": ("if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;", ""),
+    "ties_round_up": ("(fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0", "fl + 1.0"),
+    "int_beta_sign": ("if (beta != 0) v += beta *", "if (beta != 0) v -= beta *"),
+    "k_loop_short": ("for (int64_t k = 0; k < p->K; ++k)\n        acc += load_float",
+                     "for (int64_t k = 1; k < p->K; ++k)\n        acc += load_float"),
+}
+
+PINS = [
+    lambda: [T.test_hand_worked_examples(c, lay) for c in T._golden_cases() for lay in T.LAYOUTS],
+    lambda: [T.test_small_integers_match_numpy_int_matmul(lay, ab, epi)
+             for lay in T.LAYOUTS for ab in ["f16", "s8"]
+             for epi in ["plain", "alpha_beta", "bias_col_relu", "bias_row_relu"]],
+    lambda: [T.test_identity_A_gives_op_B(lay, "f32") for lay in T.LAYOUTS],
+    lambda: [T.test_f16_rounding_cases(x, b) for x, b in T.F16_CASES],
+    lambda: [T.test_bf16_rounding_cases(x, b) for x, b in T.BF16_CASES],
+    lambda: T.test_random_float_within_fp64_rounding_of_exact_sum(),
+]
+
+
+def _pins_fail() -> bool:
+    for pin in PINS:
+        try:
+            pin()
+        except AssertionError:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "oracle_mut.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", str(mutated),
+                    "-o", str(lib), "-lm"], check=True)
+    saved = O._lib
+    try:
+        O._lib = None
+        O._load_from(str(lib))
+        assert _pins_fail(), f"no pin caught the planted mistake '{name}'"
+    finally:
+        O._lib = saved
+
+
+def test_unmutated_oracle_passes_the_same_pins():
+    assert not _pins_fail()
