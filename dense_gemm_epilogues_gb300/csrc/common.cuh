@@ -1,0 +1,381 @@
+// common.cuh -- types and device helpers shared by the library's kernels.
+//
+// Everything here is the GPU side of libgemm.so; it shares nothing with the
+// CPU oracle.  The PTX wrappers cover the Blackwell (sm_100-family) features the
+// tensor-core kernel is built on: mbarrier phase waits (bounded), TMA tiled
+// loads (cp.async.bulk.tensor), tcgen05 MMA/commit/ld into and out of tensor
+// memory, and the 64-bit shared-memory matrix descriptor.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gemm.h"
+
+namespace gemmlib {
+
+// ---------------------------------------------------------------------------
+// Fused epilogue parameters: v = alpha*acc + beta*C[i,j] + bias; v = act(v);
+// D[i,j] = cast(v).  (The fused_bias_relu_epilogue functor of the CUTLASS page,
+// "Fusing Element-wise Operations: An Example with SGEMM", with the bias
+// indexed per column as in section 5.3 of "Flexible Performant GEMM Kernels on
+// GPUs"; threshold 0.)
+// ---------------------------------------------------------------------------
+struct EpiParams {
+  float alpha, beta;          // floating paths (fp32 arithmetic)
+  int32_t alpha_i, beta_i;    // integer path (int32 arithmetic)
+  const void* C;              // row-major, ldc elements per row (unused when beta == 0)
+  int64_t ldc;
+  int32_t c_dtype;            // gemm_dtype_t
+  int32_t d_dtype;
+  void* D;                    // row-major, ldd elements per row
+  int64_t ldd;
+  const void* bias;
+  int32_t bias_dtype;
+  int32_t bias_mode;          // gemm_bias_mode_t
+  int32_t relu;
+  int32_t vec_c;              // C rows may be read with 16-byte vectors
+  int32_t vec_d;              // D rows may be written with 16-byte vectors
+  int32_t read_c;             // beta != 0
+};
+
+__host__ __device__ inline int dtype_bytes(int dt) {
+  return dt == GEMM_F32 || dt == GEMM_S32 ? 4 : (dt == GEMM_S8 ? 1 : 2);
+}
+
+#if defined(__CUDACC__)
+
+// --------------------------- scalar element access -------------------------
+
+__device__ __forceinline__ float load_as_float(const void* p, int dt, int64_t idx) {
+  switch (dt) {
+    case GEMM_F32: return static_cast<const float*>(p)[idx];
+    case GEMM_F16: return __half2float(static_cast<const __half*>(p)[idx]);
+    case GEMM_BF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[idx]);
+    case GEMM_S8: return (float)static_cast<const int8_t*>(p)[idx];
+    default: return (float)static_cast<const int32_t*>(p)[idx];
+  }
+}
+
+__device__ __forceinline__ int32_t load_as_int(const void* p, int dt, int64_t idx) {
+  return dt == GEMM_S8 ? (int32_t) static_cast<const int8_t*>(p)[idx]
+                       : static_cast<const int32_t*>(p)[idx];
+}
+
+__device__ __forceinline__ void store_float_as(void* p, int dt, int64_t idx, float v) {
+  switch (dt) {
+    case GEMM_F32: static_cast<float*>(p)[idx] = v; break;
+    case GEMM_F16: static_cast<__half*>(p)[idx] = __float2half_rn(v); break;
+    default: static_cast<__nv_bfloat16*>(p)[idx] = __float2bfloat16_rn(v); break;
+  }
+}
+
+// Integer epilogue arithmetic wraps modulo 2^32 (done in unsigned to keep it defined).
+__device__ __forceinline__ int32_t wrap_madd(int32_t a, int32_t b, int32_t c) {
+  return (int32_t)((uint32_t)a * (uint32_t)b + (uint32_t)c);
+}
+
+// ------------------ a row of 32 consecutive outputs (one thread) -------------
+// The tensor-core epilogue gives each thread one row of the tile and 32
+// consecutive columns per TMEM load; these helpers finish such a chunk.
+
+// x[j] holds alpha*acc for columns n_base..n_base+31 of row m (m < M checked by caller).
+__device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64_t m, int64_t M_rows,
+                                                       int64_t n_base, int64_t N, float (&x)[32]) {
+  (void)M_rows;
+  const bool full = n_base + 32 <= N;
+  if (e.read_c) {
+    const int64_t off = m * e.ldc + n_base;
+    if (full && e.vec_c) {
+      if (e.c_dtype == GEMM_F32) {
+        const float4* c4 = reinterpret_cast<const float4*>(static_cast<const float*>(e.C) + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 c = c4[q];
+          x[4 * q + 0] = fmaf(e.beta, c.x, x[4 * q + 0]);
+          x[4 * q + 1] = fmaf(e.beta, c.y, x[4 * q + 1]);
+          x[4 * q + 2] = fmaf(e.beta, c.z, x[4 * q + 2]);
+          x[4 * q + 3] = fmaf(e.beta, c.w, x[4 * q + 3]);
+        }
+      } else {
+        const uint4* c4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(e.C) + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 c = c4[q];
+          uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float lo, hi;
+            if (e.c_dtype == GEMM_F16) {
+              __half2 v = *reinterpret_cast<__half2*>(&w[h]);
+              lo = __low2float(v); hi = __high2float(v);
+            } else {
+              __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[h]);
+              lo = __low2float(v); hi = __high2float(v);
+            }
+            x[8 * q + 2 * h + 0] = fmaf(e.beta, lo, x[8 * q + 2 * h + 0]);
+            x[8 * q + 2 * h + 1] = fmaf(e.beta, hi, x[8 * q + 2 * h + 1]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n_base + j < N) x[j] = fmaf(e.beta, load_as_float(e.C, e.c_dtype, off + j), x[j]);
+    }
+  }
+  if (e.bias_mode == GEMM_BIAS_COL) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n_base + j < N) x[j] += load_as_float(e.bias, e.bias_dtype, n_base + j);
+  } else if (e.bias_mode == GEMM_BIAS_ROW) {
+    const float b = load_as_float(e.bias, e.bias_dtype, m);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] += b;
+  }
+  if (e.relu) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = fmaxf(x[j], 0.0f);
+  }
+  const int64_t doff = m * e.ldd + n_base;
+  if (full && e.vec_d) {
+    if (e.d_dtype == GEMM_F32) {
+      float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(e.D) + doff);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) d4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else {
+      uint4* d4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.D) + doff);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          if (e.d_dtype == GEMM_F16) {
+            __half2 v = __floats2half2_rn(x[8 * q + 2 * h], x[8 * q + 2 * h + 1]);
+            w[h] = *reinterpret_cast<uint32_t*>(&v);
+          } else {
+            __nv_bfloat162 v = __floats2bfloat162_rn(x[8 * q + 2 * h], x[8 * q + 2 * h + 1]);
+            w[h] = *reinterpret_cast<uint32_t*>(&v);
+          }
+        }
+        d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n_base + j < N) store_float_as(e.D, e.d_dtype, doff + j, x[j]);
+  }
+}
+
+// x[j] holds the exact int32 product sums of columns n_base..n_base+31 of row m;
+// it is finished in place (alpha, beta*C, bias, ReLU) and stored.
+__device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t m, int64_t n_base,
+                                                     int64_t N, int32_t* x) {
+  const bool full = n_base + 32 <= N;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = wrap_madd(e.alpha_i, x[j], 0);
+  if (e.read_c) {
+    const int64_t off = m * e.ldc + n_base;
+    if (full && e.vec_c) {
+      const int4* c4 = reinterpret_cast<const int4*>(static_cast<const int32_t*>(e.C) + off);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        int4 c = c4[q];
+        x[4 * q + 0] = wrap_madd(e.beta_i, c.x, x[4 * q + 0]);
+        x[4 * q + 1] = wrap_madd(e.beta_i, c.y, x[4 * q + 1]);
+        x[4 * q + 2] = wrap_madd(e.beta_i, c.z, x[4 * q + 2]);
+        x[4 * q + 3] = wrap_madd(e.beta_i, c.w, x[4 * q + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n_base + j < N) x[j] = wrap_madd(e.beta_i, load_as_int(e.C, GEMM_S32, off + j), x[j]);
+    }
+  }
+  if (e.bias_mode == GEMM_BIAS_COL) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n_base + j < N) x[j] = wrap_madd(1, load_as_int(e.bias, GEMM_S32, n_base + j), x[j]);
+  } else if (e.bias_mode == GEMM_BIAS_ROW) {
+    const int32_t b = load_as_int(e.bias, GEMM_S32, m);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = wrap_madd(1, b, x[j]);
+  }
+  if (e.relu) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = x[j] > 0 ? x[j] : 0;
+  }
+  int32_t* d = static_cast<int32_t*>(e.D) + m * e.ldd + n_base;
+  if (full && e.vec_d) {
+    int4* d4 = reinterpret_cast<int4*>(d);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_int4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n_base + j < N) d[j] = x[j];
+  }
+}
+
+// ------------------------------- PTX wrappers -------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Shared state of a CTA's bounded waits.
+struct WaitCtx {
+  volatile int32_t* abort;   // shared: set once any role of the CTA gave up
+  int32_t* err;              // global error word (first failure wins)
+  uint64_t timeout_ns;
+};
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up after
+// ctx.timeout_ns (recording GEMM_ERR_TIMEOUT) or as soon as another role of the
+// CTA has given up.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& ctx) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*ctx.abort) return false;
+    if (globaltimer_ns() - t0 > ctx.timeout_ns) {
+      atomicCAS(ctx.err, 0, (int32_t)GEMM_ERR_TIMEOUT);
+      *ctx.abort = 1;
+      __threadfence_block();
+      return false;
+    }
+  }
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (fp16/bf16 in, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets TMEM lane (base lane + t).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) for a 128-byte-swizzled
+// operand tile whose swizzle atoms (8 rows of 128 bytes) start on 1024-byte
+// boundaries:
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-47  descriptor version (1)
+//   bits 49-51  base offset (0: atoms are 1024-byte aligned)
+//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace gemmlib

@@ -1,0 +1,586 @@
+// gemm_api.cu -- the C ABI of libgemm.so (declared in include/gemm.h):
+// argument validation, the tile-shape selector, TMA tensor-map encoding, plan
+// state and kernel launches.  Host code only; the kernels live in
+// tc_kernel.cu and simt_kernels.cu.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "kernels.h"
+
+using namespace gemmlib;
+
+struct gemm_plan {
+  int device = 0;
+  gemm_dtype_t ab = GEMM_F16;
+  gemm_dtype_t c = GEMM_F32;
+  int sm_count = 0;
+  int32_t* d_err = nullptr;          // device error word
+  void* ws = nullptr;                // int8 staging: fp16 copies of A and B
+  size_t ws_bytes = 0;
+  void* stage = nullptr;             // gemm_run_host device buffers
+  size_t stage_bytes = 0;
+  gemm_kernel_t forced = GEMM_KERNEL_AUTO;
+  gemm_config_t last{};
+  uint64_t timeout_ns = 4000000000ull;
+};
+
+namespace {
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;   // tile indices and TMA coordinates are 32-bit
+
+bool is_f16ish(int t) { return t == GEMM_F16 || t == GEMM_BF16; }
+bool is_float_out(int t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
+
+gemm_status_t check_types(gemm_dtype_t ab, gemm_dtype_t c) {
+  switch (ab) {
+    case GEMM_F16:
+    case GEMM_BF16: return is_float_out(c) ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+    case GEMM_S8: return c == GEMM_S32 ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+    case GEMM_F32: return c == GEMM_F32 ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+    default: return GEMM_ERR_INVALID_ARG;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Can TMA describe this operand (16-byte aligned base, 16-byte multiple row pitch)?
+bool tma_ok(const void* p, int64_t ld, int esize) {
+  return aligned16(p) && ((ld * esize) % 16) == 0 && ld * esize < (int64_t(1) << 40);
+}
+
+// Storage extent (elements) of a rows x cols logical matrix in a layout.
+int64_t storage_elems(gemm_layout_t layout, int64_t rows, int64_t cols, int64_t ld) {
+  if (rows == 0 || cols == 0) return 0;
+  return layout == GEMM_OP_T ? (rows - 1) * ld + cols : (cols - 1) * ld + rows;
+}
+
+bool integral_int32(double v) {
+  return std::isfinite(v) && v == std::floor(v) && v >= -2147483648.0 && v <= 2147483647.0;
+}
+
+gemm_dtype_t out_dtype_of(gemm_dtype_t c, const gemm_epilogue_t* epi) {
+  return epi ? epi->out_dtype : c;
+}
+
+gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
+                       int64_t N, int64_t K, double alpha, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, double beta, const void* C, int64_t ldc, const void* D, int64_t ldd,
+                       const gemm_epilogue_t* epi) {
+  gemm_status_t s = check_types(ab, c);
+  if (s != GEMM_OK) return s;
+  if ((la != GEMM_OP_N && la != GEMM_OP_T) || (lb != GEMM_OP_N && lb != GEMM_OP_T)) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+  const gemm_dtype_t out = out_dtype_of(c, epi);
+  if (ab == GEMM_S8 ? out != GEMM_S32 : !is_float_out(out)) return GEMM_ERR_INVALID_ARG;
+  if (epi) {
+    if (epi->act != GEMM_ACT_NONE && epi->act != GEMM_ACT_RELU) return GEMM_ERR_INVALID_ARG;
+    if (epi->bias_mode != GEMM_BIAS_NONE && epi->bias_mode != GEMM_BIAS_COL &&
+        epi->bias_mode != GEMM_BIAS_ROW)
+      return GEMM_ERR_INVALID_ARG;
+    if (epi->bias_mode != GEMM_BIAS_NONE) {
+      if (!epi->bias) return GEMM_ERR_INVALID_ARG;
+      if (ab == GEMM_S8 ? epi->bias_dtype != GEMM_S32 : !is_float_out(epi->bias_dtype))
+        return GEMM_ERR_INVALID_ARG;
+    }
+  }
+  if (ab == GEMM_S8 && (!integral_int32(alpha) || !integral_int32(beta))) return GEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!D || ldd < N) return GEMM_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (!A || !B) return GEMM_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(1, la == GEMM_OP_N ? M : K)) return GEMM_ERR_INVALID_ARG;
+    if (ldb < std::max<int64_t>(1, lb == GEMM_OP_N ? K : N)) return GEMM_ERR_INVALID_ARG;
+  }
+  if (beta != 0.0) {
+    if (!C || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (C == D && (ldc != ldd || c != out)) return GEMM_ERR_INVALID_ARG;
+  }
+  return GEMM_OK;
+}
+
+// Relative cost of one 128 x BN tile of the tensor-core kernel (a 128x128 tile
+// does half the MMA work of a 128x256 tile but keeps the fixed per-tile costs).
+double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.56; }
+
+gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
+                            int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                            int sm_count, gemm_kernel_t forced, gemm_config_t* out) {
+  (void)c;
+  gemm_config_t cfg{};
+  cfg.split_k = 1;
+  cfg.cta_group = 1;
+  if (sm_count <= 0) sm_count = 1;
+  if (M == 0 || N == 0) {
+    cfg.kernel = GEMM_KERNEL_NONE;
+    *out = cfg;
+    return GEMM_OK;
+  }
+  // Which kernels could serve this request?
+  const bool tc_ok = K > 0 && is_f16ish(ab) && tma_ok(A, lda, 2) && tma_ok(B, ldb, 2);
+  const bool int8_ok = K > 0 && ab == GEMM_S8 && (lda % 8) == 0 && (ldb % 8) == 0;
+  const bool ffma_ok = K > 0 && ab == GEMM_F32 && aligned16(A) && aligned16(B) && (lda % 4) == 0 &&
+                       (ldb % 4) == 0;
+  gemm_kernel_t k;
+  if (forced != GEMM_KERNEL_AUTO) {
+    k = forced;
+    bool type_ok = true, feasible = true;
+    switch (forced) {
+      case GEMM_KERNEL_TC: type_ok = is_f16ish(ab); feasible = tc_ok; break;
+      case GEMM_KERNEL_TC_INT8: type_ok = ab == GEMM_S8; feasible = int8_ok; break;
+      case GEMM_KERNEL_FFMA: type_ok = ab == GEMM_F32; feasible = ffma_ok; break;
+      case GEMM_KERNEL_SIMT: break;
+      default: return GEMM_ERR_INVALID_ARG;
+    }
+    if (!type_ok) return GEMM_ERR_UNSUPPORTED;
+    if (!feasible) return K == 0 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_ALIGNMENT;
+  } else {
+    k = tc_ok ? GEMM_KERNEL_TC
+              : int8_ok ? GEMM_KERNEL_TC_INT8 : ffma_ok ? GEMM_KERNEL_FFMA : GEMM_KERNEL_SIMT;
+  }
+  (void)la;
+  (void)lb;
+  cfg.kernel = k;
+  switch (k) {
+    case GEMM_KERNEL_TC:
+    case GEMM_KERNEL_TC_INT8: {
+      int bn = 128;
+      if (k == GEMM_KERNEL_TC) {
+        // Pick the tile width with the smaller estimated makespan over the SMs
+        // (the largest tile that fits, unless it leaves SMs idle).
+        double best = 1e300;
+        for (int cand : {256, 128}) {
+          const int64_t tiles = ((M + 127) / 128) * ((N + cand - 1) / cand);
+          const int64_t waves = (tiles + sm_count - 1) / sm_count;
+          const double cost = (double)waves * tc_tile_cost(cand);
+          if (cost < best - 1e-9) { best = cost; bn = cand; }
+        }
+      }
+      cfg.bm = TC_BM;
+      cfg.bn = bn;
+      cfg.bk = TC_BK;
+      cfg.stages = tc_stages(bn);
+      const int64_t tiles_m = (M + 127) / 128, tiles_n = (N + bn - 1) / bn;
+      cfg.tiles = (int32_t)std::min<int64_t>(tiles_m * tiles_n, kMaxDim);
+      cfg.raster = (int32_t)std::min<int64_t>(16, tiles_m);
+      cfg.grid = (int32_t)std::min<int64_t>(cfg.tiles, sm_count);
+      cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? 512 : 0;
+      break;
+    }
+    case GEMM_KERNEL_FFMA: {
+      cfg.bm = FFMA_BM;
+      cfg.bn = FFMA_BN;
+      cfg.bk = FFMA_BK;
+      cfg.stages = 2;
+      const int64_t tiles = ((M + FFMA_BM - 1) / FFMA_BM) * ((N + FFMA_BN - 1) / FFMA_BN);
+      cfg.tiles = (int32_t)std::min<int64_t>(tiles, kMaxDim);
+      cfg.grid = cfg.tiles;
+      cfg.raster = 1;
+      break;
+    }
+    default: {  // SIMT
+      cfg.bm = 16;
+      cfg.bn = 16;
+      cfg.bk = 16;
+      cfg.stages = 1;
+      const int64_t tiles = ((M + 15) / 16) * ((N + 15) / 16);
+      cfg.tiles = (int32_t)std::min<int64_t>(tiles, kMaxDim);
+      cfg.grid = cfg.tiles;
+      cfg.raster = 1;
+      break;
+    }
+  }
+  *out = cfg;
+  return GEMM_OK;
+}
+
+// --------------------------- TMA tensor maps -------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Row-pitched 2-D tensor (inner elements contiguous, `ld` elements between rows
+// of the outer dimension), 16-bit elements, 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  if (!encode_fn()) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// tcgen05 instruction descriptor, kind::f16 with fp32 accumulation:
+//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16, 1 = bf16),
+//   15 / 16 A / B MN-major, 17-22 N >> 3, 24-28 M >> 4.
+uint32_t make_idesc(bool bf16, int bn, bool a_mn_major, bool b_mn_major) {
+  const uint32_t f = bf16 ? 1u : 0u;
+  return (1u << 4) | (f << 7) | (f << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+EpiParams make_epi(const gemm_plan* plan, double alpha, double beta, const void* C, int64_t ldc, void* D,
+                   int64_t ldd, const gemm_epilogue_t* epi) {
+  EpiParams e{};
+  const gemm_dtype_t out = out_dtype_of(plan->c, epi);
+  e.alpha = (float)alpha;
+  e.beta = (float)beta;
+  if (plan->ab == GEMM_S8) {
+    e.alpha_i = (int32_t)alpha;
+    e.beta_i = (int32_t)beta;
+  }
+  e.read_c = beta != 0.0 ? 1 : 0;
+  e.C = e.read_c ? C : nullptr;
+  e.ldc = ldc;
+  e.c_dtype = plan->c;
+  e.D = D;
+  e.ldd = ldd;
+  e.d_dtype = out;
+  e.bias = (epi && epi->bias_mode != GEMM_BIAS_NONE) ? epi->bias : nullptr;
+  e.bias_dtype = epi ? epi->bias_dtype : GEMM_F32;
+  e.bias_mode = epi ? epi->bias_mode : GEMM_BIAS_NONE;
+  e.relu = (epi && epi->act == GEMM_ACT_RELU) ? 1 : 0;
+  e.vec_c = (e.read_c && aligned16(C) && (ldc * dtype_bytes(plan->c)) % 16 == 0) ? 1 : 0;
+  e.vec_d = (aligned16(D) && (ldd * dtype_bytes(out)) % 16 == 0) ? 1 : 0;
+  return e;
+}
+
+gemm_status_t ensure_ws(gemm_plan* plan, size_t bytes, cudaStream_t stream) {
+  if (plan->ws_bytes >= bytes) return GEMM_OK;
+  if (plan->ws) {
+    cudaFreeAsync(plan->ws, stream);
+    plan->ws = nullptr;
+    plan->ws_bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  plan->ws = p;
+  plan->ws_bytes = bytes;
+  return GEMM_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
+                                int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                                int64_t ldb, CUtensorMapDataType dt, bool bf16, const EpiParams& epi,
+                                int chunk_kb, cudaStream_t stream) {
+  TcParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  const int bn = cfg.bn;
+  const bool a_mn = la == GEMM_OP_N, b_mn = lb == GEMM_OP_T;
+  bool ok;
+  // A: K-major (row-major A) boxes 64(K) x 128(M); M-major boxes 64(M) x 64(K).
+  if (!a_mn) ok = encode_2d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, TC_BK, TC_BM);
+  else ok = encode_2d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, 64, TC_BK);
+  if (!ok) return GEMM_ERR_CUDA;
+  // B: K-major (column-major B) boxes 64(K) x BN(N); N-major boxes 64(N) x 64(K).
+  if (!b_mn) ok = encode_2d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, TC_BK, (uint32_t)bn);
+  else ok = encode_2d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, TC_BK);
+  if (!ok) return GEMM_ERR_CUDA;
+  tp.M = (int32_t)M;
+  tp.N = (int32_t)N;
+  tp.K = (int32_t)K;
+  tp.num_kb = (int32_t)((K + TC_BK - 1) / TC_BK);
+  tp.tiles_m = (int32_t)((M + TC_BM - 1) / TC_BM);
+  tp.tiles_n = (int32_t)((N + bn - 1) / bn);
+  tp.num_tiles = tp.tiles_m * tp.tiles_n;
+  tp.raster = cfg.raster > 0 ? cfg.raster : 1;
+  tp.a_mn_major = a_mn ? 1 : 0;
+  tp.b_mn_major = b_mn ? 1 : 0;
+  tp.idesc = make_idesc(bf16, bn, a_mn, b_mn);
+  tp.chunk_kb = chunk_kb;
+  tp.epi = epi;
+  tp.err = plan->d_err;
+  tp.timeout_ns = plan->timeout_ns;
+  return launch_tc(tp, bn, cfg.grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_abi_version(void) { return 100; }
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid size, leading dimension, pointer or enum";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: request not implemented by this library";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT: forced kernel needs 16-byte aligned operands";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA call failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a bounded in-kernel wait expired";
+    default: return "unknown gemm_status_t";
+  }
+}
+
+gemm_status_t gemm_validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
+                            int64_t N, int64_t K, double alpha, const void* A, int64_t lda, const void* B,
+                            int64_t ldb, double beta, const void* C, int64_t ldc, const void* D, int64_t ldd,
+                            const gemm_epilogue_t* epi) {
+  return validate(ab, c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+}
+
+gemm_status_t gemm_select(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
+                          int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                          const void* C, int64_t ldc, const void* D, int64_t ldd, double beta,
+                          const gemm_epilogue_t* epi, int sm_count, gemm_config_t* out) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  const double alpha_probe = ab == GEMM_S8 ? 1.0 : 1.0;
+  gemm_status_t s = validate(ab, c, la, lb, M, N, K, alpha_probe, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out);
+}
+
+gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab, gemm_dtype_t c, int device) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  *plan = nullptr;
+  gemm_status_t s = check_types(ab, c);
+  if (s != GEMM_OK) return s;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  DeviceGuard g(device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  gemm_plan* p = new (std::nothrow) gemm_plan();
+  if (!p) return GEMM_ERR_CUDA;
+  p->device = device;
+  p->ab = ab;
+  p->c = c;
+  if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaMalloc(&p->d_err, sizeof(int32_t)) != cudaSuccess ||
+      cudaMemset(p->d_err, 0, sizeof(int32_t)) != cudaSuccess) {
+    if (p->d_err) cudaFree(p->d_err);
+    delete p;
+    return GEMM_ERR_CUDA;
+  }
+  *plan = p;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
+  if (!plan) return GEMM_OK;
+  DeviceGuard g(plan->device);
+  cudaDeviceSynchronize();
+  if (plan->ws) cudaFree(plan->ws);
+  if (plan->stage) cudaFree(plan->stage);
+  if (plan->d_err) cudaFree(plan->d_err);
+  delete plan;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_kernel(gemm_plan_t plan, gemm_kernel_t kernel) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  if (kernel != GEMM_KERNEL_AUTO && kernel != GEMM_KERNEL_TC && kernel != GEMM_KERNEL_TC_INT8 &&
+      kernel != GEMM_KERNEL_FFMA && kernel != GEMM_KERNEL_SIMT)
+    return GEMM_ERR_INVALID_ARG;
+  plan->forced = kernel;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_t* out) {
+  if (!plan || !out) return GEMM_ERR_INVALID_ARG;
+  *out = plan->last;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns) {
+  if (!plan || timeout_ns == 0) return GEMM_ERR_INVALID_ARG;
+  plan->timeout_ns = timeout_ns;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_device_status(gemm_plan_t plan, gemm_stream_t stream, int32_t* code) {
+  if (!plan || !code) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemcpy(&v, plan->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemset(plan->d_err, 0, sizeof(int32_t)) != cudaSuccess) return GEMM_ERR_CUDA;
+  *code = v;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N, int64_t K,
+                       double alpha, const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                       const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
+                       gemm_stream_t stream_) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  gemm_config_t cfg{};
+  s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count, plan->forced, &cfg);
+  if (s != GEMM_OK) return s;
+  if (cfg.kernel == GEMM_KERNEL_NONE) {
+    plan->last = cfg;
+    return GEMM_OK;
+  }
+  DeviceGuard g(plan->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const EpiParams e = make_epi(plan, alpha, beta, C, ldc, D, ldd, epi);
+
+  switch (cfg.kernel) {
+    case GEMM_KERNEL_TC: {
+      const bool bf16 = plan->ab == GEMM_BF16;
+      s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb,
+                            bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bf16,
+                            e, 0, stream);
+      break;
+    }
+    case GEMM_KERNEL_TC_INT8: {
+      // Stage exact fp16 copies of A and B (same layouts and leading dimensions).
+      const int64_t a_el = storage_elems(la, M, K, lda);
+      const int64_t b_el = storage_elems(lb, K, N, ldb);
+      const size_t a_bytes = align_up((size_t)a_el * 2, 256);
+      s = ensure_ws(plan, a_bytes + (size_t)b_el * 2, stream);
+      if (s != GEMM_OK) break;
+      __half* A16 = static_cast<__half*>(plan->ws);
+      __half* B16 = reinterpret_cast<__half*>(static_cast<char*>(plan->ws) + a_bytes);
+      const int8_t* A8 = static_cast<const int8_t*>(A);
+      const int8_t* B8 = static_cast<const int8_t*>(B);
+      cudaError_t ce = la == GEMM_OP_T ? launch_s8_to_f16(A8, A16, M, K, lda, stream)
+                                       : launch_s8_to_f16(A8, A16, K, M, lda, stream);
+      if (ce == cudaSuccess)
+        ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8, B16, N, K, ldb, stream)
+                             : launch_s8_to_f16(B8, B16, K, N, ldb, stream);
+      if (ce != cudaSuccess) { s = GEMM_ERR_CUDA; break; }
+      s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                            false, e, cfg.k_chunk / TC_BK, stream);
+      break;
+    }
+    case GEMM_KERNEL_FFMA: {
+      FfmaParams fp{};
+      fp.A = static_cast<const float*>(A);
+      fp.B = static_cast<const float*>(B);
+      fp.lda = lda;
+      fp.ldb = ldb;
+      fp.M = (int32_t)M;
+      fp.N = (int32_t)N;
+      fp.K = (int32_t)K;
+      fp.epi = e;
+      s = launch_ffma(fp, la == GEMM_OP_T, lb == GEMM_OP_T, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+      break;
+    }
+    default: {
+      SimtParams sp{};
+      sp.A = A;
+      sp.B = B;
+      sp.lda = lda;
+      sp.ldb = ldb;
+      sp.ab_dtype = plan->ab;
+      sp.a_row_major = la == GEMM_OP_T;
+      sp.b_row_major = lb == GEMM_OP_T;
+      sp.M = M;
+      sp.N = N;
+      sp.K = K;
+      sp.epi = e;
+      s = launch_simt(sp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+      break;
+    }
+  }
+  if (s == GEMM_OK) plan->last = cfg;
+  return s;
+}
+
+gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N,
+                            int64_t K, double alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                            double beta, const void* C, int64_t ldc, void* D, int64_t ldd,
+                            const gemm_epilogue_t* epi, gemm_stream_t stream_) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) return GEMM_OK;
+  DeviceGuard g(plan->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const gemm_dtype_t out = out_dtype_of(plan->c, epi);
+  const int ab_b = dtype_bytes(plan->ab);
+  const size_t a_bytes = K > 0 ? (size_t)storage_elems(la, M, K, lda) * ab_b : 0;
+  const size_t b_bytes = K > 0 ? (size_t)storage_elems(lb, K, N, ldb) * ab_b : 0;
+  const bool in_place = beta != 0.0 && C == D;
+  const size_t c_bytes = (beta != 0.0 && !in_place) ? (size_t)((M - 1) * ldc + N) * dtype_bytes(plan->c) : 0;
+  const bool has_bias = epi && epi->bias_mode != GEMM_BIAS_NONE;
+  const size_t bias_bytes =
+      has_bias ? (size_t)(epi->bias_mode == GEMM_BIAS_COL ? N : M) * dtype_bytes(epi->bias_dtype) : 0;
+  const size_t d_bytes = (size_t)((M - 1) * ldd + N) * dtype_bytes(out);
+  size_t off_a = 0, off_b = align_up(off_a + a_bytes, 256), off_c = align_up(off_b + b_bytes, 256);
+  size_t off_bias = align_up(off_c + c_bytes, 256), off_d = align_up(off_bias + bias_bytes, 256);
+  const size_t total = align_up(off_d + d_bytes, 256);
+  if (plan->stage_bytes < total) {
+    if (plan->stage) {
+      cudaStreamSynchronize(stream);
+      cudaFree(plan->stage);
+      plan->stage = nullptr;
+      plan->stage_bytes = 0;
+    }
+    if (cudaMalloc(&plan->stage, total) != cudaSuccess) return GEMM_ERR_CUDA;
+    plan->stage_bytes = total;
+  }
+  char* base = static_cast<char*>(plan->stage);
+  void* dA = base + off_a;
+  void* dB = base + off_b;
+  void* dD = base + off_d;
+  void* dC = in_place ? dD : (beta != 0.0 ? base + off_c : nullptr);
+  void* dbias = has_bias ? base + off_bias : nullptr;
+  if (a_bytes && cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (b_bytes && cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (beta != 0.0) {
+    const size_t cb = (size_t)((M - 1) * ldc + N) * dtype_bytes(plan->c);
+    if (cudaMemcpyAsync(dC, C, cb, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  }
+  if (has_bias && cudaMemcpyAsync(dbias, epi->bias, bias_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  gemm_epilogue_t e2{};
+  if (epi) {
+    e2 = *epi;
+    e2.bias = dbias;
+  }
+  s = gemm_run(plan, la, lb, M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, dD, ldd, epi ? &e2 : nullptr,
+               stream_);
+  if (s != GEMM_OK) return s;
+  if (cudaMemcpyAsync(D, dD, d_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// kernels.h -- host-side launch interface of the library's kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gemmlib {
+
+// Tensor-core kernel (tcgen05 + TMA), one CTA per SM, persistent over tiles.
+struct TcParams {
+  CUtensorMap tmA;        // A tiles (see tc_kernel.cu for the box shapes)
+  CUtensorMap tmB;        // B tiles
+  int32_t M, N, K;
+  int32_t num_kb;         // K blocks of 64 elements
+  int32_t tiles_m, tiles_n, num_tiles;
+  int32_t raster;         // tile rows per raster group
+  int32_t a_mn_major;     // A stored M-contiguous (layout N) rather than K-contiguous
+  int32_t b_mn_major;     // B stored N-contiguous (layout T) rather than K-contiguous
+  uint32_t idesc;         // tcgen05 instruction descriptor
+  int32_t chunk_kb;       // > 0: exact integer mode, K blocks per fp32 chunk
+  EpiParams epi;
+  int32_t* err;
+  uint64_t timeout_ns;
+};
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;   // 16-bit elements: one 128-byte swizzle row
+
+int tc_stages(int bn);
+size_t tc_smem_bytes(int bn);
+cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream);
+
+// FFMA SGEMM (fp32, CUDA cores).
+struct FfmaParams {
+  const float* A;
+  const float* B;
+  int64_t lda, ldb;
+  int32_t M, N, K;
+  EpiParams epi;
+};
+constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = 8;
+cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, cudaStream_t stream);
+
+// Generic CUDA-core kernel: any dtype, layout, alignment; K may be 0.
+struct SimtParams {
+  const void* A;
+  const void* B;
+  int64_t lda, ldb;
+  int32_t ab_dtype;
+  int32_t a_row_major, b_row_major;
+  int64_t M, N, K;
+  EpiParams epi;
+};
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream);
+
+// int8 -> fp16 staging copy of a strided matrix: dst[r*ld + c] = src[r*ld + c]
+// for r < outer, c < inner.
+cudaError_t launch_s8_to_f16(const int8_t* src, __half* dst, int64_t outer, int64_t inner, int64_t ld,
+                             cudaStream_t stream);
+
+}  // namespace gemmlib

@@ -1,0 +1,321 @@
+// simt_kernels.cu -- CUDA-core kernels of the library (sm_103a):
+//   * ffma_sgemm_kernel: fp32 SGEMM, register-blocked FFMA, double-buffered
+//     shared memory, fused epilogue;
+//   * simt_gemm_kernel: the generic path for every type, layout and alignment
+//     (and K == 0), used where TMA cannot describe the operands;
+//   * s8_to_f16_kernel: the int8 -> fp16 staging copy of the exact int8 path.
+//
+// The SGEMM follows the hierarchy of the CUTLASS page ("Thread Block Tile",
+// "Warp Tile", "Thread Tile", "Software Pipelining"): a 128x128 block tile
+// over 256 threads, each thread accumulating an 8x8 register tile from 8x1 and
+// 1x8 fragments of A and B in shared memory (outer products, K innermost per
+// tile), with global loads for the next K slice in flight while the current
+// slice is multiplied, and two shared-memory buffers so that one
+// __syncthreads() per K slice suffices.
+#include "kernels.h"
+
+namespace gemmlib {
+namespace {
+
+// ================================ FFMA SGEMM =================================
+
+constexpr int SG_THREADS = 256;
+constexpr int SG_PAD = 4;                       // row padding: conflict-free transposed stores
+constexpr int SG_LDS = FFMA_BM + SG_PAD;        // 132 floats per K row (BM == BN)
+
+// Loads one BK x 128 slice of op(A) (as A^T: [k][m]) or of op(B) ([k][n]) into
+// four registers per thread.  `kmajor`: the operand is K-contiguous in global
+// memory (A row-major / B column-major), so a thread loads 4 consecutive K
+// values of one row/column; otherwise 4 consecutive M/N values of one K row.
+template <bool KMAJOR>
+struct SliceLoader {
+  const float* ptr;
+  int64_t ld;
+  int64_t extent_mn;   // M (for A) or N (for B)
+  int64_t K;
+  static constexpr bool kmajor = KMAJOR;
+
+  __device__ __forceinline__ void load(int64_t mn0, int64_t k0, int tid, float (&v)[4]) const {
+    if constexpr (KMAJOR) {
+      const int64_t r = mn0 + (tid >> 1);
+      const int64_t k = k0 + (tid & 1) * 4;
+      const float* src = ptr + r * ld + k;
+      if (r < extent_mn && k + 4 <= K) {
+        const float4 f = *reinterpret_cast<const float4*>(src);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = (r < extent_mn && k + j < K) ? src[j] : 0.0f;
+      }
+    } else {
+      const int64_t k = k0 + (tid >> 5);
+      const int64_t c = mn0 + (tid & 31) * 4;
+      const float* src = ptr + k * ld + c;
+      if (k < K && c + 4 <= extent_mn) {
+        const float4 f = *reinterpret_cast<const float4*>(src);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = (k < K && c + j < extent_mn) ? src[j] : 0.0f;
+      }
+    }
+  }
+
+  // Store the four values into the [BK][SG_LDS] shared buffer.
+  __device__ __forceinline__ void store(float* s, int tid, const float (&v)[4]) const {
+    if constexpr (KMAJOR) {
+      const int r = tid >> 1, k = (tid & 1) * 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[(k + j) * SG_LDS + r] = v[j];
+    } else {
+      const int k = tid >> 5, c = (tid & 31) * 4;
+      *reinterpret_cast<float4*>(&s[k * SG_LDS + c]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+};
+
+template <bool A_KMAJOR, bool B_KMAJOR>
+__global__ void __launch_bounds__(SG_THREADS, 2) ffma_sgemm_kernel(const FfmaParams p) {
+  __shared__ __align__(16) float As[2][FFMA_BK * SG_LDS];
+  __shared__ __align__(16) float Bs[2][FFMA_BK * SG_LDS];
+
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int64_t tiles_n = (p.N + FFMA_BN - 1) / FFMA_BN;
+  const int64_t m0 = (int64_t)(blockIdx.x / tiles_n) * FFMA_BM;
+  const int64_t n0 = (int64_t)(blockIdx.x % tiles_n) * FFMA_BN;
+
+  const SliceLoader<A_KMAJOR> la{p.A, p.lda, p.M, p.K};
+  const SliceLoader<B_KMAJOR> lb{p.B, p.ldb, p.N, p.K};
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+  const int nkt = (p.K + FFMA_BK - 1) / FFMA_BK;
+  float ra[4], rb[4];
+  if (nkt > 0) {
+    la.load(m0, 0, tid, ra);
+    lb.load(n0, 0, tid, rb);
+    la.store(As[0], tid, ra);
+    lb.store(Bs[0], tid, rb);
+  }
+  __syncthreads();
+
+  int buf = 0;
+  for (int kt = 0; kt < nkt; ++kt) {
+    const bool more = kt + 1 < nkt;
+    if (more) {
+      la.load(m0, (int64_t)(kt + 1) * FFMA_BK, tid, ra);
+      lb.load(n0, (int64_t)(kt + 1) * FFMA_BK, tid, rb);
+    }
+    const float* as = As[buf];
+    const float* bs = Bs[buf];
+#pragma unroll
+    for (int kk = 0; kk < FFMA_BK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&as[kk * SG_LDS + ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&as[kk * SG_LDS + 64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + 64 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (more) {
+      la.store(As[buf ^ 1], tid, ra);
+      lb.store(Bs[buf ^ 1], tid, rb);
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+
+  // Fused epilogue.  Thread rows: ty*4+i and 64+ty*4+i; columns tx*4+j and 64+tx*4+j.
+  const EpiParams& e = p.epi;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    if (m >= p.M) continue;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t nb = n0 + h * 64 + tx * 4;
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = acc[i][h * 4 + j] * e.alpha;
+      const bool full = nb + 4 <= p.N;
+      if (e.read_c) {
+        const int64_t off = m * e.ldc + nb;
+        if (full && e.vec_c && e.c_dtype == GEMM_F32) {
+          const float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(e.C) + off);
+          x[0] = fmaf(e.beta, c.x, x[0]); x[1] = fmaf(e.beta, c.y, x[1]);
+          x[2] = fmaf(e.beta, c.z, x[2]); x[3] = fmaf(e.beta, c.w, x[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (nb + j < p.N) x[j] = fmaf(e.beta, load_as_float(e.C, e.c_dtype, off + j), x[j]);
+        }
+      }
+      if (e.bias_mode == GEMM_BIAS_COL) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (nb + j < p.N) x[j] += load_as_float(e.bias, e.bias_dtype, nb + j);
+      } else if (e.bias_mode == GEMM_BIAS_ROW) {
+        const float b = load_as_float(e.bias, e.bias_dtype, m);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] += b;
+      }
+      if (e.relu) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = fmaxf(x[j], 0.0f);
+      }
+      const int64_t doff = m * e.ldd + nb;
+      if (full && e.vec_d && e.d_dtype == GEMM_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(e.D) + doff) = make_float4(x[0], x[1], x[2], x[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (nb + j < p.N) store_float_as(e.D, e.d_dtype, doff + j, x[j]);
+      }
+    }
+  }
+}
+
+// ============================ generic SIMT kernel ============================
+
+constexpr int GT = 16;   // 16 x 16 outputs per block, one per thread, K slices of 16
+
+__device__ __forceinline__ int64_t a_index(const SimtParams& p, int64_t i, int64_t k) {
+  return p.a_row_major ? i * p.lda + k : i + k * p.lda;
+}
+__device__ __forceinline__ int64_t b_index(const SimtParams& p, int64_t k, int64_t j) {
+  return p.b_row_major ? k * p.ldb + j : k + j * p.ldb;
+}
+
+template <bool IS_INT>
+__global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
+  using Acc = typename std::conditional<IS_INT, int32_t, float>::type;
+  __shared__ Acc As[GT][GT + 1];
+  __shared__ Acc Bs[GT][GT + 1];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int64_t tiles_n = (p.N + GT - 1) / GT;
+  const int64_t bm = (int64_t)blockIdx.x / tiles_n, bn = (int64_t)blockIdx.x % tiles_n;
+  const int64_t i = bm * GT + ty;
+  const int64_t j = bn * GT + tx;
+  Acc acc = 0;
+  for (int64_t k0 = 0; k0 < p.K; k0 += GT) {
+    {
+      const int64_t ai = bm * GT + ty, ak = k0 + tx;
+      Acc v = 0;
+      if (ai < p.M && ak < p.K) {
+        if constexpr (IS_INT) v = load_as_int(p.A, p.ab_dtype, a_index(p, ai, ak));
+        else v = load_as_float(p.A, p.ab_dtype, a_index(p, ai, ak));
+      }
+      As[ty][tx] = v;
+      const int64_t bk = k0 + ty, bj = bn * GT + tx;
+      Acc w = 0;
+      if (bk < p.K && bj < p.N) {
+        if constexpr (IS_INT) w = load_as_int(p.B, p.ab_dtype, b_index(p, bk, bj));
+        else w = load_as_float(p.B, p.ab_dtype, b_index(p, bk, bj));
+      }
+      Bs[ty][tx] = w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < GT; ++kk) {
+      if constexpr (IS_INT) acc += As[ty][kk] * Bs[kk][tx];
+      else acc = fmaf(As[ty][kk], Bs[kk][tx], acc);
+    }
+    __syncthreads();
+  }
+  if (i >= p.M || j >= p.N) return;
+  const EpiParams& e = p.epi;
+  if constexpr (IS_INT) {
+    int32_t v = wrap_madd(e.alpha_i, acc, 0);
+    if (e.read_c) v = wrap_madd(e.beta_i, load_as_int(e.C, GEMM_S32, i * e.ldc + j), v);
+    if (e.bias_mode == GEMM_BIAS_COL) v = wrap_madd(1, load_as_int(e.bias, GEMM_S32, j), v);
+    else if (e.bias_mode == GEMM_BIAS_ROW) v = wrap_madd(1, load_as_int(e.bias, GEMM_S32, i), v);
+    if (e.relu) v = v > 0 ? v : 0;
+    static_cast<int32_t*>(e.D)[i * e.ldd + j] = v;
+  } else {
+    float v = acc * e.alpha;
+    if (e.read_c) v = fmaf(e.beta, load_as_float(e.C, e.c_dtype, i * e.ldc + j), v);
+    if (e.bias_mode == GEMM_BIAS_COL) v += load_as_float(e.bias, e.bias_dtype, j);
+    else if (e.bias_mode == GEMM_BIAS_ROW) v += load_as_float(e.bias, e.bias_dtype, i);
+    if (e.relu) v = fmaxf(v, 0.0f);
+    store_float_as(e.D, e.d_dtype, i * e.ldd + j, v);
+  }
+}
+
+// ============================ int8 -> fp16 staging ===========================
+
+// One thread converts 16 consecutive elements of a row (vector path when the
+// row start and leading dimension keep 16-byte alignment), grid-stride.
+__global__ void s8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restrict__ dst, int64_t outer,
+                                 int64_t inner, int64_t ld, int vec) {
+  const int64_t groups_per_row = (inner + 15) / 16;
+  const int64_t total = outer * groups_per_row;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = g / groups_per_row;
+    const int64_t c = (g - r * groups_per_row) * 16;
+    const int8_t* s = src + r * ld + c;
+    __half* d = dst + r * ld + c;
+    if (vec && c + 16 <= inner) {
+      const int4 w = *reinterpret_cast<const int4*>(s);
+      const int8_t* b = reinterpret_cast<const int8_t*>(&w);
+      uint32_t out[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        __half2 v = __halves2half2(__int2half_rn(b[2 * h]), __int2half_rn(b[2 * h + 1]));
+        out[h] = *reinterpret_cast<uint32_t*>(&v);
+      }
+      reinterpret_cast<uint4*>(d)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      reinterpret_cast<uint4*>(d)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    } else {
+      for (int j = 0; j < 16 && c + j < inner; ++j) d[j] = __int2half_rn(s[j]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, cudaStream_t stream) {
+  const int64_t tiles = ((p.N + FFMA_BN - 1) / FFMA_BN) * ((p.M + FFMA_BM - 1) / FFMA_BM);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)tiles);
+  // A row-major (T) is K-contiguous; B column-major (N) is K-contiguous.
+  const bool ak = a_row_major != 0, bk = b_row_major == 0;
+  if (ak && bk) ffma_sgemm_kernel<true, true><<<grid, SG_THREADS, 0, stream>>>(p);
+  else if (ak) ffma_sgemm_kernel<true, false><<<grid, SG_THREADS, 0, stream>>>(p);
+  else if (bk) ffma_sgemm_kernel<false, true><<<grid, SG_THREADS, 0, stream>>>(p);
+  else ffma_sgemm_kernel<false, false><<<grid, SG_THREADS, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) {
+  const dim3 block(GT, GT);
+  const int64_t tiles = ((p.N + GT - 1) / GT) * ((p.M + GT - 1) / GT);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)tiles);
+  if (p.ab_dtype == GEMM_S8) simt_gemm_kernel<true><<<grid, block, 0, stream>>>(p);
+  else simt_gemm_kernel<false><<<grid, block, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_s8_to_f16(const int8_t* src, __half* dst, int64_t outer, int64_t inner, int64_t ld,
+                             cudaStream_t stream) {
+  if (outer <= 0 || inner <= 0) return cudaSuccess;
+  const int vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0 &&
+                   (ld % 16) == 0) ? 1 : 0;
+  const int64_t total = outer * ((inner + 15) / 16);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  s8_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, dst, outer, inner, ld, vec);
+  return cudaGetLastError();
+}
+
+}  // namespace gemmlib

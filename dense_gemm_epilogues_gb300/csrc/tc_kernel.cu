@@ -1,0 +1,321 @@
+// tc_kernel.cu -- tcgen05 tensor-core GEMM with a fused epilogue (sm_103a).
+//
+// D = epilogue(alpha * op(A) * op(B) + beta * C) for fp16/bf16 operands with
+// fp32 accumulation in tensor memory, and (exact integer mode) for int8
+// operands staged as fp16.
+//
+// The structure follows the recursive blocking of "Flexible Performant GEMM
+// Kernels on GPUs" (section 3: global -> shared -> MMA -> epilogue) and the
+// software pipelining of the CUTLASS page ("Software Pipelining": loads, shared
+// memory and math in flight at once), mapped onto Blackwell hardware:
+//   - one persistent CTA per SM walks a list of 128 x BN output tiles;
+//   - warp 0 (one thread) streams 128x64 A and BNx64 B tiles with TMA into an
+//     S-stage ring of 128-byte-swizzled shared-memory buffers (full/empty
+//     mbarriers) -- the swizzle removes the bank conflicts that section 5.1 of
+//     the paper names as its main gap;
+//   - warp 1 (one thread) issues tcgen05.mma (M=128, N=BN, K=16) into a
+//     tensor-memory accumulator and commits stage releases to the empty
+//     barriers; it owns the tensor-memory allocation (all 512 columns: two
+//     128x256 or four 128x128 fp32 accumulators);
+//   - warps 2-5 drain a finished accumulator with tcgen05.ld (one row per
+//     thread), apply alpha, beta*C, bias, ReLU and the output cast in registers
+//     and store with 16-byte vector writes, while warp 1 already accumulates the
+//     next tile into the other accumulator buffer.
+// Exact integer mode (int8 inputs): every product of two int8 values is exact
+// in fp32 and so is any sum of up to 1024 of them (|sum| <= 2^24), so the MMA
+// accumulates K in chunks of chunk_kb*64 <= 512 into a fresh fp32 accumulator;
+// the epilogue warps convert each finished chunk to int32 and add it into
+// registers, giving the exact int32 result for any K.
+//
+// Every wait is bounded (see mbar_wait): on expiry the CTA records
+// GEMM_ERR_TIMEOUT, drains its own copies and MMAs in flight (again bounded)
+// and releases tensor memory before it exits.
+#include "kernels.h"
+
+namespace gemmlib {
+namespace {
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;   // 16 KiB
+  static constexpr int B_BYTES = BN * TC_BK * 2;      // 32 KiB (BN=256) / 16 KiB (BN=128)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_BUFS = 512 / BN;           // accumulators in the 512 TMEM columns
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+};
+
+constexpr int NUM_THREADS = 192;      // producer warp, MMA warp, 4 epilogue warps
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int MN_BOX = 64;            // MN extent of one TMA box for MN-major operands
+constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;   // 8 KiB
+
+// Tile t -> (tile row, tile column), in groups of `raster` tile rows so that
+// CTAs running at the same time share A row panels and B column panels in L2
+// (the block rasterisation of the CUTLASS page's policy).
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+  const int group_tiles = p.raster * p.tiles_n;
+  const int g = t / group_tiles;
+  const int first_m = g * p.raster;
+  const int gsize = min(p.tiles_m - first_m, p.raster);
+  const int r = t - g * group_tiles;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+// Bounded wait that ignores the abort flag: used while winding down, so that no
+// copy or MMA of this CTA is still in flight when it releases tensor memory and
+// exits.  Its bound is at least one second whatever the user's wait bound is.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t user_timeout_ns) {
+  const uint64_t timeout_ns = user_timeout_ns > 1000000000ull ? user_timeout_ns : 1000000000ull;
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// All lanes of a warp wait; the warp gives up together if any lane gave up.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+template <int BN, bool INT_MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  static_assert(!INT_MODE || BN == 128, "exact integer mode keeps 128 int32 accumulators per thread");
+  using Cfg = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;       // swizzle atoms need 1024-byte alignment
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar0 = base + (uint32_t)(Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES +
+                                                    Cfg::NUM_BARS * 8);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(Cfg::STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * Cfg::STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * Cfg::STAGES + Cfg::ACC_BUFS + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (uint32_t)(2 * Cfg::STAGES + 2 * Cfg::ACC_BUFS);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);    // producer's expect_tx arrival + TMA bytes
+      mbar_init(empty_bar(s), 1);   // tcgen05.commit after the stage's MMAs
+    }
+    for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
+      mbar_init(tfull_bar(b), 1);   // tcgen05.commit after a unit's last MMA
+      mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(teardown_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  const int units_per_tile = p.chunk_kb > 0 ? (p.num_kb + p.chunk_kb - 1) / p.chunk_kb : 1;
+  const int kb_per_unit = p.chunk_kb > 0 ? p.chunk_kb : p.num_kb;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tmA);
+      tma_prefetch_desc(&p.tmB);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p, tm, tn);
+        const int m0 = tm * TC_BM, n0 = tn * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb = full_bar(stage);
+          mbar_expect_tx(fb, (uint32_t)Cfg::STAGE_BYTES);
+          const uint32_t sa = base + (uint32_t)(stage * Cfg::STAGE_BYTES);
+          const uint32_t sb = sa + (uint32_t)Cfg::A_BYTES;
+          const int k0 = kb * TC_BK;
+          if (p.a_mn_major) {
+#pragma unroll
+            for (int h = 0; h < TC_BM / MN_BOX; ++h)
+              tma_load_2d(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, fb);
+          } else {
+            tma_load_2d(sa, &p.tmA, k0, m0, fb);
+          }
+          if (p.b_mn_major) {
+#pragma unroll
+            for (int h = 0; h < BN / MN_BOX; ++h)
+              tma_load_2d(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, fb);
+          } else {
+            tma_load_2d(sb, &p.tmB, k0, n0, fb);
+          }
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Every copy this thread started must have landed before the CTA exits.
+      for (int s = 0; s < Cfg::STAGES; ++s)
+        if (issued & (1u << s)) drain_wait(full_bar(s), (last_parity >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        for (int u = 0; ok && u < units_per_tile; ++u) {
+          const int buf = (int)(acc_it % Cfg::ACC_BUFS);
+          const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
+          if (!mbar_wait(tempty_bar(buf), apar ^ 1u, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+          const int kb_begin = u * kb_per_unit;
+          const int kb_end = min(p.num_kb, kb_begin + kb_per_unit);
+          for (int kb = kb_begin; kb < kb_end; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = base + (uint32_t)(stage * Cfg::STAGE_BYTES);
+            const uint32_t sb = sa + (uint32_t)Cfg::A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < TC_BK / 16; ++kk) {
+              // K-major: the 16-element K step is 32 bytes inside each 128-byte row.
+              // MN-major: it is 16 rows of 128 bytes; LBO steps between 64-wide MN boxes.
+              const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
+                                               : smem_desc_sw128(sa + kk * 32u, 16, 1024);
+              const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
+                                               : smem_desc_sw128(sb + kk * 32u, 16, 1024);
+              tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));
+            if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit(tfull_bar(buf));
+          ++acc_it;
+        }
+      }
+      // Every MMA this thread issued must be complete before tensor memory is freed.
+      tc_commit(teardown_bar);
+      drain_wait(teardown_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // -------------------------------- epilogue --------------------------------
+    const int q = warp & 3;                          // TMEM lane quarter this warp may access
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const int64_t m = (int64_t)tm * TC_BM + q * 32 + lane;
+      const int64_t n0 = (int64_t)tn * BN;
+      const bool row_ok = m < p.M;
+      if constexpr (INT_MODE) {
+        int32_t acc[BN];
+#pragma unroll
+        for (int j = 0; j < BN; ++j) acc[j] = 0;
+        for (int u = 0; u < units_per_tile; ++u) {
+          const int buf = (int)(acc_it % Cfg::ACC_BUFS);
+          const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
+          if (!warp_wait(tfull_bar(buf), apar, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[c * 32 + j] += __float2int_rn(__uint_as_float(r[j]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+          ++acc_it;
+        }
+        if (!ok) break;
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) epi_finish_row32_int(p.epi, m, n0 + c * 32, p.N, &acc[c * 32]);
+        }
+      } else {
+        const int buf = (int)(acc_it % Cfg::ACC_BUFS);
+        const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
+        if (!warp_wait(tfull_bar(buf), apar, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+          tmem_wait_ld();
+          if (row_ok) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
+            epi_finish_row32_float(p.epi, m, p.M, n0 + c * 32, p.N, x);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+        ++acc_it;
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int BN, bool INT_MODE>
+cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
+  using Cfg = TcCfg<BN>;
+  static_assert(Cfg::SMEM <= 232448, "shared memory budget");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  tc_gemm_kernel<BN, INT_MODE><<<grid, NUM_THREADS, Cfg::SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_stages(int bn) { return bn == 256 ? TcCfg<256>::STAGES : TcCfg<128>::STAGES; }
+size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>::SMEM; }
+
+cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream) {
+  if (p.chunk_kb > 0) {
+    // exact integer mode keeps 128 int32 accumulators per thread: BN = 128 only
+    return bn == 128 ? launch_bn<128, true>(p, grid, stream) : cudaErrorInvalidValue;
+  }
+  if (bn == 256) return launch_bn<256, false>(p, grid, stream);
+  if (bn == 128) return launch_bn<128, false>(p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gemmlib

@@ -1,0 +1,173 @@
+"""Shared helpers of the parity tests: run a problem through the GPU library
+(C ABI, device buffers with guard bands) and through the CPU oracle, and compare.
+
+The tolerance for floating outputs, computed in fp64 from both outputs widened
+to fp64:  max |D - D_ref| <= 1e-2 * (|D_ref| + 1) elementwise, and
+||D - D_ref||_F / ||D_ref||_F <= 2e-3.  Integer outputs must be bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import dense_gemm_epilogues_gb300 as G
+import oracle as O
+from dense_gemm_epilogues_gb300 import inputs as I
+
+OR_DT = {"f32": O.F32, "f16": O.F16, "bf16": O.BF16, "s8": O.S8, "s32": O.S32}
+OR_LAY = {"N": O.LAYOUT_N, "T": O.LAYOUT_T}
+OR_BIAS = {"none": O.BIAS_NONE, "col": O.BIAS_COL, "row": O.BIAS_ROW}
+OR_ACT = {"none": O.ACT_NONE, "relu": O.ACT_RELU}
+G_BIAS = {"none": G.GEMM_BIAS_NONE, "col": G.GEMM_BIAS_COL, "row": G.GEMM_BIAS_ROW}
+
+ABS_TOL = 1e-2
+FRO_TOL = 2e-3
+GUARD_ROWS = 3
+SENTINEL = {"f32": float.fromhex("0x1.5p+100"), "f16": 12345.0, "bf16": 1.5e30, "s32": 0x5A5A5A5A}
+
+
+def _oracle_kwargs(p: I.Problem, inp: I.Inputs) -> dict:
+    return dict(beta=p.beta, c_dtype=OR_DT[p.c] if p.c else O.F32, C=inp.C,
+                ldc=p.ldc if p.c else 0, bias_dtype=OR_DT[p.bias] if p.bias else O.F32,
+                bias=inp.bias, bias_mode=OR_BIAS[p.bias_mode], act=OR_ACT[p.act],
+                d_dtype=OR_DT[p.d])
+
+
+def oracle_full(inp: I.Inputs) -> np.ndarray:
+    p = inp.problem
+    D, ovf = O.gemm(OR_DT[p.ab], OR_LAY[p.layout_a], OR_LAY[p.layout_b], p.M, p.N, p.K, p.alpha,
+                    inp.A, p.lda, inp.B, p.ldb, ldd=p.N, **_oracle_kwargs(p, inp))
+    assert ovf == 0, "inputs overflow int32; the library contract leaves that undefined"
+    return D
+
+
+def oracle_entries(inp: I.Inputs, rows, cols) -> np.ndarray:
+    p = inp.problem
+    out, ovf = O.gemm_entries(OR_DT[p.ab], OR_LAY[p.layout_a], OR_LAY[p.layout_b], p.M, p.N, p.K,
+                              p.alpha, inp.A, p.lda, inp.B, p.ldb, rows, cols,
+                              **_oracle_kwargs(p, inp))
+    assert ovf == 0
+    return out
+
+
+def to_f64(x, dtype: str) -> np.ndarray:
+    """Widen raw output (numpy bits for 16-bit types, or a torch tensor) to fp64."""
+    if isinstance(x, torch.Tensor):
+        return x.to(torch.float64).cpu().numpy()
+    if dtype in ("f16", "bf16"):
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16))
+        return t.view(I.TORCH_DTYPES[dtype]).to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def check_close(D_gpu: torch.Tensor, D_ref_raw: np.ndarray, d_dtype: str, what: str = ""):
+    if d_dtype == "s32":
+        got = D_gpu.cpu().numpy().astype(np.int64)
+        ref = np.asarray(D_ref_raw).astype(np.int64)
+        bad = np.argwhere(got != ref)
+        assert bad.size == 0, f"{what}: {len(bad)} int32 mismatches, first at {bad[:3].tolist()}"
+        return
+    got = to_f64(D_gpu, d_dtype)
+    ref = to_f64(D_ref_raw, d_dtype)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite outputs"
+    err = np.abs(got - ref)
+    lim = ABS_TOL * (np.abs(ref) + 1.0)
+    worst = np.unravel_index(np.argmax(err - lim), err.shape) if err.size else None
+    assert np.all(err <= lim), (f"{what}: elementwise bound violated at {worst}: "
+                                f"got {got[worst]} ref {ref[worst]}")
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        fro = np.linalg.norm(got - ref) / nref
+        assert fro <= FRO_TOL, f"{what}: relative Frobenius error {fro:.3e} > {FRO_TOL}"
+
+
+class DeviceProblem:
+    """Device copies of a problem's inputs, plus a guarded output buffer."""
+
+    def __init__(self, inp: I.Inputs, device="cuda"):
+        p = inp.problem
+        self.inp, self.p = inp, p
+        self.A = inp.A.to(device)
+        self.B = inp.B.to(device)
+        self.C = inp.C.to(device) if inp.C is not None else None
+        self.bias = inp.bias.to(device) if inp.bias is not None else None
+        rows = p.M + 2 * GUARD_ROWS
+        self.Dbuf = torch.full((rows, p.ldd), SENTINEL[p.d], dtype=I.TORCH_DTYPES[p.d], device=device)
+        self.D = self.Dbuf[GUARD_ROWS:GUARD_ROWS + p.M]
+
+    def epilogue(self) -> G.gemm_epilogue_t:
+        p = self.p
+        return G.make_epilogue(G.DTYPE_CODES[p.d],
+                               self.bias.data_ptr() if self.bias is not None else 0,
+                               G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
+                               G_BIAS[p.bias_mode],
+                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE)
+
+    def run(self, plan: G.Plan, stream=None):
+        p = self.p
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M, p.N,
+                   p.K, p.alpha, self.A.data_ptr(), p.lda, self.B.data_ptr(), p.ldb, p.beta,
+                   self.C.data_ptr() if self.C is not None else None, p.ldc if p.c else 0,
+                   self.D.data_ptr(), p.ldd, self.epilogue(), stream)
+
+    def check_guards(self):
+        p = self.p
+        s = torch.tensor(SENTINEL[p.d], dtype=I.TORCH_DTYPES[p.d])
+        top = self.Dbuf[:GUARD_ROWS].cpu()
+        bot = self.Dbuf[GUARD_ROWS + p.M:].cpu()
+        pad = self.D[:, p.N:].cpu()
+        for name, t in (("rows before D", top), ("rows after D", bot), ("padding of D", pad)):
+            assert torch.all(t == s), f"kernel wrote into the {name}"
+
+    def result(self) -> torch.Tensor:
+        return self.D[:, :self.p.N]
+
+
+def make_plan(p: I.Problem, kernel=None) -> G.Plan:
+    c = p.c if p.c else ("s32" if p.ab == "s8" else "f32")
+    plan = G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[c], torch.cuda.current_device())
+    if kernel is not None:
+        plan.set_kernel(kernel)
+    return plan
+
+
+def run_and_check_full(p: I.Problem, seed: int, kernel=None, expect_kernel=None) -> dict:
+    inp = I.generate(p, seed)
+    dp = DeviceProblem(inp)
+    plan = make_plan(p, kernel)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    cfg = plan.last_config()
+    if expect_kernel is not None:
+        assert cfg["kernel"] == expect_kernel, f"ran {cfg['kernel_name']}"
+    dp.check_guards()
+    check_close(dp.result(), oracle_full(inp), p.d, p.name)
+    plan.close()
+    return cfg
+
+
+def sample_entries(M: int, N: int, n: int, seed: int, tile_m=128, tile_n=256):
+    """Random entries plus corners and tile-boundary rows/columns."""
+    rng = np.random.default_rng(seed)
+    rows = list(rng.integers(0, M, n))
+    cols = list(rng.integers(0, N, n))
+    edge_r = sorted({0, M - 1, min(M - 1, tile_m - 1), min(M - 1, tile_m), M // 2, max(0, M - tile_m)})
+    edge_c = sorted({0, N - 1, min(N - 1, tile_n - 1), min(N - 1, tile_n), N // 2, max(0, N - tile_n)})
+    for r in edge_r:
+        for c in edge_c:
+            rows.append(r)
+            cols.append(c)
+    return np.array(rows, dtype=np.int64), np.array(cols, dtype=np.int64)
+
+
+def tma_aligned(p: I.Problem, mult: int = 8) -> I.Problem:
+    """Pad the leading dimensions of A and B up to a multiple of `mult` elements
+    (16 bytes for 16-bit types), as the tensor-core kernels' TMA loads require.
+    The logical sizes (and their ragged tails) are unchanged; the padding is
+    poisoned by the input generator."""
+    ra = (p.M if p.layout_a == "N" else p.K)
+    rb = (p.K if p.layout_b == "N" else p.N)
+    return p.with_(pad_a=p.pad_a + (-(ra + p.pad_a)) % mult, pad_b=p.pad_b + (-(rb + p.pad_b)) % mult)

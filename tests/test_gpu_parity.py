@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Small and ragged problems are compared element by element on the full output;
+every kernel (tensor-core fp16/bf16, exact int8, FFMA SGEMM, generic CUDA-core)
+and every layout, epilogue and output type is covered, plus guard bands around
+D, in-place C == D, empty and K == 0 problems, host-buffer entry and the
+bounded-wait status.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_epilogues_gb300 as G
+from dense_gemm_epilogues_gb300 import inputs as I
+
+import parity_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = ["NN", "NT", "TN", "TT"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    G.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+# ------------------------------- tensor cores --------------------------------
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("ab", ["f16", "bf16"])
+def test_tc_ragged_alpha_beta(layout, ab):
+    """Several 128x256 tiles with ragged M, N, K tails; alpha/beta with fp32 C."""
+    p = H.tma_aligned(I.Problem("tc_ab", ab, layout[0], layout[1], 300, 520, 200, alpha=1.5,
+                                  beta=0.5, c="f32"))
+    H.run_and_check_full(p, 101, expect_kernel=G.GEMM_KERNEL_TC)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_tc_bias_relu_bf16_out(layout):
+    p = H.tma_aligned(I.Problem("tc_fc", "bf16", layout[0], layout[1], 257, 384, 320, d="bf16",
+                                bias="f32", bias_mode="col", act="relu",
+                                dist_a=I.Dist("normal", std=1.0), dist_b=I.Dist("normal", std=0.05)))
+    H.run_and_check_full(p, 102, expect_kernel=G.GEMM_KERNEL_TC)
+
+
+@pytest.mark.parametrize("n", [64, 96, 128, 129, 200])
+def test_tc_narrow_n_tiles(n):
+    """N <= 128 selects 128-wide tiles; N just above selects by the wave model."""
+    p = H.tma_aligned(I.Problem("tc_n", "f16", "T", "N", 256, n, 192))
+    H.run_and_check_full(p, 103, expect_kernel=G.GEMM_KERNEL_TC)
+
+
+@pytest.mark.parametrize("c,d", [("f16", "f16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f16")])
+def test_tc_c_and_d_types(c, d):
+    ab = "bf16" if "bf16" in (c, d) else "f16"
+    p = H.tma_aligned(I.Problem("tc_cd", ab, "N", "T", 200, 300, 136, alpha=-0.75, beta=1.25, c=c,
+                                d=d, bias="bf16" if ab == "bf16" else "f16", bias_mode="row",
+                                act="relu"))
+    H.run_and_check_full(p, 104, expect_kernel=G.GEMM_KERNEL_TC)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_tc_padded_leading_dims(layout):
+    """Leading dimensions larger than the logical extent (poisoned padding, 16-byte
+    multiples) and a padded, unaligned-width D."""
+    p = H.tma_aligned(I.Problem("tc_pad", "f16", layout[0], layout[1], 190, 270, 150, beta=1.0,
+                                c="f32", pad_a=8, pad_b=16, pad_c=3, pad_d=5))
+    H.run_and_check_full(p, 105, expect_kernel=G.GEMM_KERNEL_TC)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_tc_small_integers_bit_exact(layout):
+    """Small-integer data is exact in every step, so the tensor-core result must
+    equal the oracle bit for bit (fp32 out)."""
+    p = H.tma_aligned(I.Problem("tc_exact", "f16", layout[0], layout[1], 260, 300, 520, alpha=2.0,
+                                beta=-1.0, c="f32", dist_a=I.Dist("small", -3, 3),
+                                dist_b=I.Dist("small", -3, 3), dist_c=I.Dist("small", -100, 100),
+                                bias="f32", bias_mode="col", dist_bias=I.Dist("small", -50, 50),
+                                act="relu"))
+    inp = I.generate(p, 106)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.last_config()["kernel"] == G.GEMM_KERNEL_TC
+    np.testing.assert_array_equal(dp.result().cpu().numpy(), H.oracle_full(inp))
+    dp.check_guards()
+
+
+def test_tc_in_place_c_equals_d():
+    p = I.Problem("inplace", "f16", "T", "N", 150, 260, 96, alpha=1.0, beta=2.0, c="f32")
+    inp = I.generate(p, 107)
+    ref = H.oracle_full(inp)
+    plan = H.make_plan(p)
+    A, B = inp.A.cuda(), inp.B.cuda()
+    CD = inp.C.cuda()
+    G.gemm_run(plan.handle, G.GEMM_OP_T, G.GEMM_OP_N, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda,
+               B.data_ptr(), p.ldb, p.beta, CD.data_ptr(), p.ldc, CD.data_ptr(), p.ldc,
+               G.make_epilogue(G.GEMM_F32), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    H.check_close(CD, ref, "f32", "in-place")
+
+
+def test_tc_many_tiles_persistent_loop():
+    """More tiles than SMs: every CTA walks several tiles (both accumulator buffers)."""
+    p = I.Problem("tc_many", "f16", "T", "N", 2048, 2304, 128, beta=0.5, c="f32")
+    cfg = H.run_and_check_full(p, 108, expect_kernel=G.GEMM_KERNEL_TC)
+    assert cfg["tiles"] > cfg["grid"]
+
+
+# ---------------------------------- int8 -------------------------------------
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_int8_exact_ragged(layout):
+    """K = 1100 spans two exact 512-chunks and a tail; bit-exact int32."""
+    p = H.tma_aligned(I.Problem("i8", "s8", layout[0], layout[1], 260, 390, 1100, d="s32",
+                                dist_a=I.I8, dist_b=I.I8))
+    H.run_and_check_full(p, 109, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+
+
+def test_int8_adversarial_extremes_exact():
+    """All -128: every partial sum is 16384*k, far beyond fp32's exact range at
+    K = 4096 (2^26), so a single fp32 accumulator would be wrong."""
+    p = I.Problem("i8max", "s8", "T", "N", 130, 140, 4096, d="s32",
+                  dist_a=I.Dist("int", -128, -128), dist_b=I.Dist("int", -128, -128))
+    H.run_and_check_full(p, 110, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+
+
+def test_int8_alpha_beta_bias_relu():
+    p = H.tma_aligned(I.Problem("i8epi", "s8", "N", "T", 200, 136, 700, alpha=3.0, beta=-2.0,
+                                c="s32", d="s32", bias="s32", bias_mode="col", act="relu",
+                                dist_a=I.I8, dist_b=I.I8, dist_c=I.Dist("int", -100000, 100000),
+                                dist_bias=I.Dist("int", -5000, 5000)))
+    H.run_and_check_full(p, 111, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+
+
+# ---------------------------------- FFMA -------------------------------------
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_ffma_sgemm_bias_relu(layout):
+    p = I.Problem("sg", "f32", layout[0], layout[1], 300, 260, 100, alpha=1.0, beta=0.5, c="f32",
+                  bias="f32", bias_mode="col", act="relu")
+    H.run_and_check_full(p, 112, expect_kernel=G.GEMM_KERNEL_FFMA)
+
+
+def test_ffma_ragged_k_and_padding():
+    p = I.Problem("sg2", "f32", "T", "N", 129, 131, 37, pad_a=3, pad_b=1, d="bf16")
+    # lda = 40, ldb = 38: ldb is not a multiple of 4 -> generic path; force FFMA fails
+    inp = I.generate(p, 113)
+    plan = H.make_plan(p, G.GEMM_KERNEL_FFMA)
+    dp = H.DeviceProblem(inp)
+    with pytest.raises(G.GemmError) as e:
+        dp.run(plan)
+    assert e.value.status == G.GEMM_ERR_ALIGNMENT
+    p2 = p.with_(pad_b=3)   # ldb = 40
+    H.run_and_check_full(p2, 113, expect_kernel=G.GEMM_KERNEL_FFMA)
+
+
+# ------------------------------ generic kernel -------------------------------
+
+@pytest.mark.parametrize("ab", ["f16", "bf16", "s8", "f32"])
+def test_generic_kernel_unaligned(ab):
+    """Odd leading dimensions that TMA cannot describe run on the generic kernel."""
+    d = "s32" if ab == "s8" else "f32"
+    kw = dict(dist_a=I.I8, dist_b=I.I8) if ab == "s8" else {}
+    p = I.Problem("gen", ab, "T", "N", 45, 37, 29, d=d, pad_a=1, pad_b=2, **kw)
+    H.run_and_check_full(p, 114, expect_kernel=G.GEMM_KERNEL_SIMT)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_forced_generic_matches(layout):
+    p = I.Problem("gen2", "bf16", layout[0], layout[1], 70, 90, 33, alpha=0.5, beta=-1.0,
+                  c="bf16", d="f16", bias="f32", bias_mode="row", act="relu")
+    H.run_and_check_full(p, 115, kernel=G.GEMM_KERNEL_SIMT, expect_kernel=G.GEMM_KERNEL_SIMT)
+
+
+def test_k_zero_is_epilogue_of_beta_c():
+    p = I.Problem("k0", "f16", "T", "N", 33, 47, 0, alpha=3.0, beta=0.5, c="f32", bias="f32",
+                  bias_mode="col", act="relu")
+    H.run_and_check_full(p, 116, expect_kernel=G.GEMM_KERNEL_SIMT)
+
+
+def test_empty_problems_are_noops():
+    for M, N in ((0, 16), (16, 0)):
+        p = I.Problem("empty", "f16", "T", "N", M, N, 8)
+        inp = I.generate(p, 117)
+        dp = H.DeviceProblem(inp)
+        plan = H.make_plan(p)
+        dp.run(plan)
+        torch.cuda.synchronize()
+        assert plan.last_config()["kernel"] == G.GEMM_KERNEL_NONE
+        dp.check_guards()
+
+
+# ------------------------------ host entry point -----------------------------
+
+def test_run_host_buffers():
+    p = I.Problem("host", "bf16", "T", "T", 300, 280, 96, beta=0.25, c="f32", d="bf16",
+                  bias="f32", bias_mode="col", act="relu")
+    inp = I.generate(p, 118)
+    ref = H.oracle_full(inp)
+    plan = H.make_plan(p)
+    A = inp.A.pin_memory()
+    B = inp.B.pin_memory()
+    C = inp.C.pin_memory()
+    bias = inp.bias.pin_memory()
+    D = torch.zeros((p.M, p.ldd), dtype=torch.bfloat16).pin_memory()
+    epi = G.make_epilogue(G.GEMM_BF16, bias.data_ptr(), G.GEMM_F32, G.GEMM_BIAS_COL, G.GEMM_ACT_RELU)
+    G.gemm_run_host(plan.handle, G.GEMM_OP_T, G.GEMM_OP_T, p.M, p.N, p.K, p.alpha, A.data_ptr(),
+                    p.lda, B.data_ptr(), p.ldb, p.beta, C.data_ptr(), p.ldc, D.data_ptr(), p.ldd,
+                    epi, torch.cuda.current_stream().cuda_stream)
+    H.check_close(D[:, :p.N], ref, "bf16", "host entry")
+
+
+# ------------------------------- bounded waits -------------------------------
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait bound far below a tile's run time makes the tensor-core kernel's
+    waits expire: the kernel records GEMM_ERR_TIMEOUT, winds down and returns;
+    the same context then runs the problem correctly."""
+    p = I.Problem("tmo", "f16", "T", "N", 512, 512, 4096)
+    inp = I.generate(p, 119)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p)
+    G.gemm_plan_set_timeout(plan.handle, 200)       # 200 ns
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == G.GEMM_ERR_TIMEOUT
+    G.gemm_plan_set_timeout(plan.handle, 4_000_000_000)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    H.check_close(dp.result(), H.oracle_full(inp), "f32", "after timeout")
