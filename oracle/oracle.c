@@ -249,8 +249,10 @@ static int64_t element_ijk(const problem_t* p, int64_t i, int64_t j, void* D, in
 static int valid_problem(const problem_t* p) {
     if (p->M < 0 || p->N < 0 || p->K < 0) return 0;
     if (p->ab_dtype < OR_F32 || p->ab_dtype > OR_S8) return 0;
-    if (p->layout_a == OR_LAYOUT_N ? p->lda < (p->M > 1 ? p->M : 1) : p->lda < (p->K > 1 ? p->K : 1)) return 0;
-    if (p->layout_b == OR_LAYOUT_N ? p->ldb < (p->K > 1 ? p->K : 1) : p->ldb < (p->N > 1 ? p->N : 1)) return 0;
+    if (p->K > 0) {   /* K == 0 is an empty sum: A and B are not read */
+        if (p->layout_a == OR_LAYOUT_N ? p->lda < (p->M > 1 ? p->M : 1) : p->lda < (p->K > 1 ? p->K : 1)) return 0;
+        if (p->layout_b == OR_LAYOUT_N ? p->ldb < (p->K > 1 ? p->K : 1) : p->ldb < (p->N > 1 ? p->N : 1)) return 0;
+    }
     if (p->ldd < p->N) return 0;
     if (p->beta != 0.0 && (p->C == NULL || p->ldc < p->N)) return 0;
     if (p->bias_mode != OR_BIAS_NONE && p->bias == NULL) return 0;

@@ -108,7 +108,7 @@ def test_tc_in_place_c_equals_d():
 
 def test_tc_many_tiles_persistent_loop():
     """More tiles than SMs: every CTA walks several tiles (both accumulator buffers)."""
-    p = I.Problem("tc_many", "f16", "T", "N", 2048, 2304, 128, beta=0.5, c="f32")
+    p = I.Problem("tc_many", "f16", "T", "N", 2560, 2560, 64, beta=0.5, c="f32")   # 200 tiles
     cfg = H.run_and_check_full(p, 108, expect_kernel=G.GEMM_KERNEL_TC)
     assert cfg["tiles"] > cfg["grid"]
 

@@ -374,3 +374,14 @@ def test_invalid_arguments_rejected():
         O.gemm(O.F32, O.LAYOUT_T, O.LAYOUT_N, 2, 2, 2, 1.0, A, 2, A, 2, beta=1.0)
     with pytest.raises(ValueError):   # non-integral alpha on the int path
         O.gemm(O.S8, O.LAYOUT_T, O.LAYOUT_N, 2, 2, 2, 0.5, A, 2, A, 2, d_dtype=O.S32)
+
+
+def test_k_zero_is_epilogue_of_beta_c():
+    """K == 0: the product is an empty sum, so D = act(beta*C + bias) and A, B
+    (and their leading dimensions) are not read."""
+    p = I.Problem("k0", "f16", "T", "N", 5, 6, 0, alpha=3.0, beta=0.5, c="f32", bias="f32",
+                  bias_mode="col", act="relu")
+    inp = I.generate(p, 13)
+    D, _ = run_oracle(inp)
+    v = np.maximum(np.float64(0.5) * inp.C.double().numpy() + inp.bias.double().numpy()[None, :], 0)
+    np.testing.assert_array_equal(D, v.astype(np.float32))
