@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 generalized GEMM with fused epilogues.
+
+Default run (the contract line): one step is the whole hot path over one batch
+of synthetic input -- the M = N = K = 8192 fp16 GEMM with fp32 C and D,
+alpha = 1.5, beta = 0.5, in all four operand layouts (NN, NT, TN, TT), each a
+separate library call.  `value` is TFLOP/s over the timed steps with inputs
+resident in HBM (inputs are larger than L2, no flush needed); `e2e` is the same
+metric through gemm_run_host (host buffers, copies inside the timed region).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--suite]
+
+--impl reference times the CPU oracle (fp64, all host cores) on bounded samples
+of the same workload.  --suite prints one extra JSON line per workload of the
+parity suite (256^3, FC layer, int8, SGEMM, square sweep, skinny).
+Multi-GPU: replicas only (each rank runs the full workload on its own GPU; no
+data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (TOP/s int8) at 1 GB300 and % of dense tensor-core peak"
+LAYOUTS = ["NN", "NT", "TN", "TT"]
+MAIN_N = 8192
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DOMINANT_KERNEL_SOURCES = ["dense_gemm_epilogues_gb300/csrc/tc_kernel.cu",
+                           "dense_gemm_epilogues_gb300/csrc/common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tc_gemm_f16_8192_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--suite", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def workload_config(world: int) -> dict:
+    return {"workload": "gemm_f16_8192x8192x8192_alpha1.5_beta0.5_fp32_C_D_layouts_NN_NT_TN_TT",
+            "M": MAIN_N, "N": MAIN_N, "K": MAIN_N, "layouts": LAYOUTS, "ab": "f16",
+            "accumulate": "f32", "c": "f32", "d": "f32", "alpha": 1.5, "beta": 0.5,
+            "gemms_per_step": len(LAYOUTS),
+            "l2": "inputs larger than L2 (A, B 134 MB per layout, C and D 268 MB); no flush",
+            "parallelism": f"replicas{world}"}
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while work runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# --------------------------------------------------------------- traffic ----
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in DOMINANT_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since it was captured."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if "=" in line and not line.lstrip().startswith("#"):
+                    k, v = line.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ our kernels ---
+
+def make_main_problems():
+    from dense_gemm_epilogues_gb300 import inputs as I
+    return [I.square_fp16_8192(l) for l in LAYOUTS]
+
+
+def device_inputs(problems, device):
+    """Generate each layout's inputs (same seed => same logical matrices) and
+    copy them to the device; C is shared, D is one output buffer."""
+    import torch
+    from dense_gemm_epilogues_gb300 import inputs as I
+    out = []
+    C = None
+    for p in problems:
+        inp = I.generate(p, I.BASE_SEED + 1)
+        if C is None:
+            C = inp.C.to(device)
+        out.append({"p": p, "A": inp.A.to(device), "B": inp.B.to(device), "host": inp})
+    D = torch.empty((MAIN_N, MAIN_N), dtype=torch.float32, device=device)
+    return out, C, D
+
+
+def run_gemm(G, plan, p, A, B, C, D, stream, epi):
+    G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M, p.N, p.K,
+               p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta, C.data_ptr(), p.ldc,
+               D.data_ptr(), p.ldd, epi, stream)
+
+
+def bench_ours(args, rank, world, local_rank):
+    import torch
+    import dense_gemm_epilogues_gb300 as G
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    G.load_library()
+    problems = make_main_problems()
+    ins, C, D = device_inputs(problems, device)
+    plan = G.Plan(G.GEMM_F16, G.GEMM_F32, local_rank)
+    epi = G.make_epilogue(G.GEMM_F32)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+
+    def step(ev=None):
+        for li, x in enumerate(ins):
+            if ev is not None:
+                ev[li][0].record(stream)
+            run_gemm(G, plan, x["p"], x["A"], x["B"], C, D, sh, epi)
+            if ev is not None:
+                ev[li][1].record(stream)
+
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    gpu_id = cvd.split(",")[local_rank] if cvd else str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cfg_used = plan.last_config()
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in ins] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [e[0].elapsed_time(e[1]) for st in evs for e in st]
+    status = plan.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops_per_gemm = 2.0 * MAIN_N ** 3
+    flops_step = flops_per_gemm * len(ins)
+    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+    peaks = load_peaks()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = flops_per_gemm / avg_launch_s / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": measured_traffic(),
+                "peak_source": f"{peaks['source']} bf16 dense burst (fp16 has the same dense rate)",
+                "kernel": "tc_gemm_kernel<256,false> (tcgen05 128x256 tiles)",
+                "algorithmic_flops_per_launch": flops_per_gemm,
+                "avg_launch_ms": round(avg_launch_s * 1e3, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(G, plan, ins, device, min(args.steps, 20), dist)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic", "config": workload_config(world), "roofline": roofline,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": len(ins) * args.steps,
+            "kernel_config": cfg_used,
+            "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(budget_s=15.0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if args.suite and rank == 0:
+        run_suite(G, device)
+    plan.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_e2e(G, plan, ins, device, steps, dist):
+    """Same metric through gemm_run_host: per step and layout, the H2D copy of A,
+    B and C from pinned host memory, the GEMM, and the D2H copy of D."""
+    import torch
+    hosts = []
+    for x in ins:
+        h = x["host"]
+        hosts.append((x["p"], h.A.pin_memory(), h.B.pin_memory()))
+    Ch = ins[0]["host"].C.pin_memory()
+    Dh = torch.empty((MAIN_N, MAIN_N), dtype=torch.float32).pin_memory()
+    epi = G.make_epilogue(G.GEMM_F32)
+    stream = torch.cuda.current_stream(device).cuda_stream
+
+    def step():
+        for p, A, B in hosts:
+            G.gemm_run_host(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b],
+                            p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
+                            p.beta, Ch.data_ptr(), p.ldc, Dh.data_ptr(), p.ldd, epi, stream)
+
+    step()   # sizes the plan's staging buffers
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t
+    if dist:
+        tt = torch.tensor([el], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    world = dist.get_world_size() if dist else 1
+    flops = 2.0 * MAIN_N ** 3 * len(hosts) * steps * world
+    h2d = sum(A.numel() * A.element_size() + B.numel() * B.element_size() for _, A, B in hosts)
+    h2d += len(hosts) * Ch.numel() * Ch.element_size()
+    d2h = len(hosts) * Dh.numel() * Dh.element_size()
+    return {"value": round(flops / el / 1e12, 1), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "api": "gemm_run_host (C ABI, host buffers)"}
+
+
+# ------------------------------------------------------------- CPU oracle ---
+
+def _oracle_rows(O, inp, rows, nthreads=None):
+    import numpy as np
+    p = inp.problem
+    rr = np.repeat(np.asarray(rows, dtype=np.int64), p.N)
+    cc = np.tile(np.arange(p.N, dtype=np.int64), len(rows))
+    t = time.perf_counter()
+    O.gemm_entries(O.F16, O.LAYOUT_N if p.layout_a == "N" else O.LAYOUT_T,
+                   O.LAYOUT_N if p.layout_b == "N" else O.LAYOUT_T, p.M, p.N, p.K, p.alpha,
+                   inp.A, p.lda, inp.B, p.ldb, rr, cc, beta=p.beta, c_dtype=O.F32, C=inp.C,
+                   ldc=p.ldc, d_dtype=O.F32, nthreads=nthreads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline_sample(budget_s: float = 15.0, problem=None, inp=None) -> dict:
+    """The oracle, as it stands, on whole rows of the TN 8192^3 GEMM."""
+    import oracle as O
+    from dense_gemm_epilogues_gb300 import inputs as I
+    O.build()
+    if inp is None:
+        problem = problem or I.square_fp16_8192("TN")
+        inp = I.generate(problem, I.BASE_SEED + 1)
+    p = inp.problem
+    t1 = _oracle_rows(O, inp, [0])
+    rows = max(1, int(budget_s / max(t1, 1e-6)))
+    rows = min(rows, p.M)
+    el = _oracle_rows(O, inp, list(range(rows)))
+    flops = 2.0 * rows * p.N * p.K
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": O.max_threads(),
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": f"{rows} full rows ({rows}x{p.N} outputs, K={p.K}) of the {p.layout_a}{p.layout_b} "
+                      f"8192^3 fp16 GEMM with alpha/beta epilogue, fp64 accumulation"}
+
+
+def bench_reference(args, rank, world):
+    """The reference arm: the CPU oracle timed on bounded samples of the same
+    workload (rows of each layout's GEMM in turn)."""
+    if rank != 0:
+        return
+    import oracle as O
+    from dense_gemm_epilogues_gb300 import inputs as I
+    O.build()
+    problems = make_main_problems()
+    inps = [I.generate(p, I.BASE_SEED + 1) for p in problems]
+    t_row = _oracle_rows(O, inps[2], [0])
+    total_steps = args.steps + args.warmup
+    per_step = min(6.0, 150.0 / max(total_steps, 1))
+    rows = max(1, int(per_step / max(t_row, 1e-6)))
+    for s in range(args.warmup):
+        _oracle_rows(O, inps[s % 4], list(range(rows)))
+    el = 0.0
+    for s in range(args.steps):
+        el += _oracle_rows(O, inps[s % 4], list(range(rows)))
+    flops = 2.0 * rows * MAIN_N * MAIN_N * args.steps
+    value = flops / el / 1e12
+    sample = (f"{rows} full rows per step ({rows}x{MAIN_N} outputs, K={MAIN_N}), layouts NN/NT/TN/TT "
+              f"in turn, fp64 oracle")
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(world), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": O.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ suite ---
+
+def run_suite(G, device, warmup=3, iters=10):
+    """One JSON line per workload of the parity suite (not the contract line)."""
+    import torch
+    from dense_gemm_epilogues_gb300 import inputs as I
+    peaks = load_peaks()
+    cases = [(I.square_fp16_256(), 0), (I.fc_bf16_8192x4096x11008(), 2), (I.int8_8192(), 3),
+             (I.sgemm_4096_bias_relu(), 4)]
+    cases += [(I.square_fp16(n), 5) for n in (512, 1024, 2048, 4096, 16384)]
+    cases += [(I.skinny_fp16_16384x64x16384(), 6)]
+    stream = torch.cuda.current_stream(device)
+    for p, k in cases:
+        inp = I.generate(p, I.BASE_SEED + k)
+        A, B = inp.A.to(device), inp.B.to(device)
+        C = inp.C.to(device) if inp.C is not None else None
+        bias = inp.bias.to(device) if inp.bias is not None else None
+        D = torch.empty((p.M, p.ldd), dtype=I.TORCH_DTYPES[p.d], device=device)
+        cc = p.c or ("s32" if p.ab == "s8" else "f32")
+        plan = G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[cc], device.index or 0)
+        bm = {"none": G.GEMM_BIAS_NONE, "col": G.GEMM_BIAS_COL, "row": G.GEMM_BIAS_ROW}[p.bias_mode]
+        epi = G.make_epilogue(G.DTYPE_CODES[p.d], bias.data_ptr() if bias is not None else 0,
+                              G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32, bm,
+                              G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE)
+
+        def call():
+            G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M,
+                       p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                       C.data_ptr() if C is not None else None, p.ldc if C is not None else 0,
+                       D.data_ptr(), p.ldd, epi, stream.cuda_stream)
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+        for _ in range(warmup):
+            call()
+        times = []
+        for _ in range(iters):
+            flush.zero_()      # L2 flush between timed iterations (small workloads fit in L2)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / 1e3)
+        t = statistics.median(times)
+        status = plan.device_status()
+        cfg = plan.last_config()
+        eb = I.ELEM_BYTES
+        algo_bytes = (inp.A.numel() * eb[p.ab] + inp.B.numel() * eb[p.ab] + p.M * p.N * eb[p.d]
+                      + (p.M * p.N * eb[p.c] if p.c else 0))
+        tflops = p.flops / t / 1e12
+        rec = {"suite": p.name, "M": p.M, "N": p.N, "K": p.K, "kernel": cfg["kernel_name"],
+               "tile": f"{cfg['bm']}x{cfg['bn']}x{cfg['bk']}", "grid": cfg["grid"],
+               "median_us": round(t * 1e6, 2), "tflops": round(tflops, 2),
+               "gbs": round(algo_bytes / t / 1e9, 1), "algo_bytes": algo_bytes,
+               "frac_tensor_peak": round(tflops / peaks["bf16_tflops"], 4),
+               "frac_hbm": round(algo_bytes / t / 1e9 / peaks["hbm_gbs"], 4), "status": status}
+        print(json.dumps(rec), flush=True)
+        plan.close()
+        del A, B, C, D, bias, flush
+        torch.cuda.empty_cache()
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_info()
+    if args.impl == "reference":
+        bench_reference(args, rank, world)
+        return
+    bench_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -274,9 +274,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;   // try_wait itself suspends for a while
     if (*ctx.abort) return false;
     if (globaltimer_ns() - t0 > ctx.timeout_ns) {
       atomicCAS(ctx.err, 0, (int32_t)GEMM_ERR_TIMEOUT);

@@ -229,20 +229,73 @@ static int store_int(void* D, int64_t idx, int64_t v) {
     return (v < INT32_MIN || v > INT32_MAX) ? 1 : 0;
 }
 
+/* Decoding tables for the 16-bit formats: entry b is the value of bit pattern
+ * b, filled once from the decoders above. */
+static double f16_table[65536], bf16_table[65536];
+static int tables_ready = 0;
+
+static void init_tables(void) {
+    if (tables_ready) return;
+#pragma omp critical(oracle_tables)
+    {
+        if (!tables_ready) {
+            for (int b = 0; b < 65536; ++b) {
+                f16_table[b] = oracle_f16_to_double((uint16_t)b);
+                bf16_table[b] = oracle_bf16_to_double((uint16_t)b);
+            }
+            tables_ready = 1;
+        }
+    }
+}
+
+/* sum_k a(i,k) * b(k,j), k ascending.  The storage position of a(i,k) moves by
+ * a constant step as k grows (a_offset is affine in k), so the loop walks the
+ * offsets from a_offset(i,0) and b_offset(0,j) by those steps. */
+static double dot_float(const problem_t* p, int64_t i, int64_t j) {
+    const int64_t a0 = a_offset(p->layout_a, i, 0, p->lda);
+    const int64_t da = p->K > 1 ? a_offset(p->layout_a, i, 1, p->lda) - a0 : 0;
+    const int64_t b0 = b_offset(p->layout_b, 0, j, p->ldb);
+    const int64_t db = p->K > 1 ? b_offset(p->layout_b, 1, j, p->ldb) - b0 : 0;
+    double acc = 0.0;
+    int64_t ia = a0, ib = b0;
+    switch (p->ab_dtype) {
+    case OR_F32: {
+        const float *A = (const float*)p->A, *B = (const float*)p->B;
+        for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += (double)A[ia] * (double)B[ib];
+        break;
+    }
+    case OR_F16: {
+        const uint16_t *A = (const uint16_t*)p->A, *B = (const uint16_t*)p->B;
+        for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += f16_table[A[ia]] * f16_table[B[ib]];
+        break;
+    }
+    case OR_BF16: {
+        const uint16_t *A = (const uint16_t*)p->A, *B = (const uint16_t*)p->B;
+        for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += bf16_table[A[ia]] * bf16_table[B[ib]];
+        break;
+    }
+    default:
+        for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db)
+            acc += load_float(p->ab_dtype, p->A, ia) * load_float(p->ab_dtype, p->B, ib);
+    }
+    return acc;
+}
+
+static int64_t dot_int(const problem_t* p, int64_t i, int64_t j) {
+    const int64_t a0 = a_offset(p->layout_a, i, 0, p->lda);
+    const int64_t da = p->K > 1 ? a_offset(p->layout_a, i, 1, p->lda) - a0 : 0;
+    const int64_t b0 = b_offset(p->layout_b, 0, j, p->ldb);
+    const int64_t db = p->K > 1 ? b_offset(p->layout_b, 1, j, p->ldb) - b0 : 0;
+    const int8_t *A = (const int8_t*)p->A, *B = (const int8_t*)p->B;
+    int64_t acc = 0, ia = a0, ib = b0;
+    for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += (int64_t)A[ia] * (int64_t)B[ib];
+    return acc;
+}
+
 /* One output element in the dot-product order: sum over k for fixed (i, j). */
 static int64_t element_ijk(const problem_t* p, int64_t i, int64_t j, void* D, int64_t out_idx) {
-    if (is_int_problem(p)) {
-        int64_t acc = 0;
-        for (int64_t k = 0; k < p->K; ++k)
-            acc += load_int(p->ab_dtype, p->A, a_offset(p->layout_a, i, k, p->lda)) *
-                   load_int(p->ab_dtype, p->B, b_offset(p->layout_b, k, j, p->ldb));
-        return store_int(D, out_idx, epilogue_int(p, i, j, acc));
-    }
-    double acc = 0.0;
-    for (int64_t k = 0; k < p->K; ++k)
-        acc += load_float(p->ab_dtype, p->A, a_offset(p->layout_a, i, k, p->lda)) *
-               load_float(p->ab_dtype, p->B, b_offset(p->layout_b, k, j, p->ldb));
-    store_float(p->d_dtype, D, out_idx, epilogue_float(p, i, j, acc));
+    if (is_int_problem(p)) return store_int(D, out_idx, epilogue_int(p, i, j, dot_int(p, i, j)));
+    store_float(p->d_dtype, D, out_idx, epilogue_float(p, i, j, dot_float(p, i, j)));
     return 0;
 }
 
@@ -284,6 +337,7 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
                    lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype};
     if (!valid_problem(&p)) return -1;
     if (M == 0 || N == 0) return 0;
+    init_tables();
     int64_t overflow = 0;
     if (loop_order == 0) {
         if (nthreads < 1) nthreads = 1;
@@ -339,6 +393,7 @@ int64_t oracle_gemm_entries(int ab_dtype, int layout_a, int layout_b,
     if (!valid_problem(&p)) return -1;
     for (int64_t e = 0; e < n_entries; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
+    init_tables();
     int64_t overflow = 0;
     if (nthreads < 1) nthreads = 1;
 #pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads) reduction(+ : overflow)

@@ -26,8 +26,14 @@ MUTANTS = {
     "relu_dropped": ("if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;", ""),
     "ties_round_up": ("(fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0", "fl + 1.0"),
     "int_beta_sign": ("if (beta != 0) v += beta *", "if (beta != 0) v -= beta *"),
-    "k_loop_short": ("for (int64_t k = 0; k < p->K; ++k)\n        acc += load_float",
-                     "for (int64_t k = 1; k < p->K; ++k)\n        acc += load_float"),
+    "k_loop_short_f16": ("for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += f16_table",
+                         "for (int64_t k = 1; k < p->K; ++k, ia += da, ib += db) acc += f16_table"),
+    "k_loop_short_int": ("for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += (int64_t)",
+                         "for (int64_t k = 1; k < p->K; ++k, ia += da, ib += db) acc += (int64_t)"),
+    "b_step_wrong": ("b_offset(p->layout_b, 1, j, p->ldb) - b0 : 0;\n    double acc",
+                     "b_offset(p->layout_b, 1, j, p->ldb) - b0 + 1 : 0;\n    double acc"),
+    "bf16_table_is_f16": ("acc += bf16_table[A[ia]] * bf16_table[B[ib]]",
+                          "acc += f16_table[A[ia]] * bf16_table[B[ib]]"),
 }
 
 PINS = [
