@@ -37,7 +37,8 @@ LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 # Every entry point declared in include/gemm.h.
 EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host", "gemm_validate",
             "gemm_select", "gemm_plan_set_kernel", "gemm_plan_last_config", "gemm_plan_device_status",
-            "gemm_plan_set_timeout", "gemm_status_string", "gemm_abi_version"]
+            "gemm_plan_set_timeout", "gemm_status_string", "gemm_abi_version",
+            "gemm_run_s8_noalloc"]
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -93,6 +94,8 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_status_string.argtypes = [ci]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_abi_version.argtypes = []
+    lib.gemm_run_s8_noalloc.argtypes = [ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64,
+                                        vp, i64, ctypes.POINTER(gemm_epilogue_t), vp, vp]
     for name in EXPORTED:
         if name not in ("gemm_status_string", "gemm_abi_version"):
             getattr(lib, name).restype = ci
@@ -145,6 +148,20 @@ def gemm_run_host(plan, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta
                   epi: Optional[gemm_epilogue_t] = None, stream: int = 0) -> None:
     _check(load_library().gemm_run_host(plan, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
                                         beta, C, ldc, D, ldd, _epi_ptr(epi), stream), "gemm_run_host")
+
+
+def gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd,
+                        epi: Optional[gemm_epilogue_t] = None, status: Optional[int] = None,
+                        stream: int = 0) -> None:
+    """int8 GEMM on the current device with no device allocation (library-held
+    fixed scratch; see include/gemm.h).  `status`: optional device address of a
+    caller-owned int32 error word."""
+    _check(load_library().gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
+                                              beta, C, ldc, D, ldd, _epi_ptr(epi), status, stream),
+           "gemm_run_s8_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def gemm_validate(ab_dtype, c_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C,

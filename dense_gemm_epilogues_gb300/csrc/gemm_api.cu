@@ -584,3 +584,115 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// gemm_run_s8_noalloc: the int8 path with its fp16 staging in a fixed device
+// array instead of plan-owned, allocated scratch (see include/gemm.h).
+// ===========================================================================
+
+// The staging array and the library's own error word.  In host code these
+// names are host-side stand-ins, not device addresses: the host only ever
+// passes the addresses cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
+static __device__ __align__(16) int32_t g_noalloc_status;
+
+namespace {
+
+struct NoallocDevice {
+  bool ready = false;
+  void* scratch = nullptr;     // device address of g_noalloc_scratch on this device
+  int32_t* status = nullptr;   // device address of g_noalloc_status on this device
+  int sm_count = 0;
+};
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
+
+// Once per device, with that device current: look up the arrays' device addresses.
+gemm_status_t noalloc_device(int dev, NoallocDevice** out) {
+  if (dev < 0 || dev >= kNoallocMaxDevices) return GEMM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* scratch = nullptr;
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaGetSymbolAddress(&status, g_noalloc_status) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    d.scratch = scratch;
+    d.status = static_cast<int32_t*>(status);
+    d.ready = true;
+  }
+  *out = &d;
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_s8_noalloc(gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N,
+                                             int64_t K, double alpha, const void* A, int64_t lda,
+                                             const void* B, int64_t ldb, double beta, const void* C,
+                                             int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
+                                             int32_t* status, gemm_stream_t stream_) {
+  gemm_status_t s = validate(GEMM_S8, GEMM_S32, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  if (M == 0 || N == 0) return GEMM_OK;
+  size_t a_bytes = 0, total = 0;
+  if (K > 0) {
+    if ((lda % 8) != 0 || (ldb % 8) != 0) return GEMM_ERR_ALIGNMENT;
+    a_bytes = align_up((size_t)storage_elems(la, M, K, lda) * 2, 256);
+    total = a_bytes + (size_t)storage_elems(lb, K, N, ldb) * 2;
+    if (total > (size_t)GEMM_NOALLOC_SCRATCH_BYTES) return GEMM_ERR_UNSUPPORTED;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  NoallocDevice* nd = nullptr;
+  s = noalloc_device(dev, &nd);
+  if (s != GEMM_OK) return s;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int32_t* err = status ? status : nd->status;
+  if (!status && cudaMemsetAsync(err, 0, sizeof(int32_t), stream) != cudaSuccess) return GEMM_ERR_CUDA;
+
+  // A plan-shaped record on the stack (no device memory behind it) so that the
+  // launch helpers of gemm_run serve this entry point unchanged.
+  gemm_plan local;
+  local.device = dev;
+  local.ab = GEMM_S8;
+  local.c = GEMM_S32;
+  local.sm_count = nd->sm_count;
+  local.d_err = err;
+  gemm_config_t cfg{};
+  s = select_config(GEMM_S8, GEMM_S32, la, lb, M, N, K, A, lda, B, ldb, local.sm_count, GEMM_KERNEL_AUTO, &cfg);
+  if (s != GEMM_OK) return s;
+  const EpiParams e = make_epi(&local, alpha, beta, C, ldc, D, ldd, epi);
+  if (cfg.kernel != GEMM_KERNEL_TC_INT8) {   // K == 0: epilogue of beta*C only, no staging
+    SimtParams sp{};
+    sp.A = A;
+    sp.B = B;
+    sp.lda = lda;
+    sp.ldb = ldb;
+    sp.ab_dtype = GEMM_S8;
+    sp.a_row_major = la == GEMM_OP_T;
+    sp.b_row_major = lb == GEMM_OP_T;
+    sp.M = M;
+    sp.N = N;
+    sp.K = K;
+    sp.epi = e;
+    return launch_simt(sp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
+  __half* A16 = static_cast<__half*>(nd->scratch);
+  __half* B16 = reinterpret_cast<__half*>(static_cast<char*>(nd->scratch) + a_bytes);
+  const int8_t* A8 = static_cast<const int8_t*>(A);
+  const int8_t* B8 = static_cast<const int8_t*>(B);
+  cudaError_t ce = la == GEMM_OP_T ? launch_s8_to_f16(A8, A16, M, K, lda, stream)
+                                   : launch_s8_to_f16(A8, A16, K, M, lda, stream);
+  if (ce == cudaSuccess)
+    ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8, B16, N, K, ldb, stream)
+                         : launch_s8_to_f16(B8, B16, K, N, ldb, stream);
+  if (ce != cudaSuccess) return GEMM_ERR_CUDA;
+  return launch_tc_problem(&local, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           false, e, cfg.k_chunk / TC_BK, stream);
+}
+

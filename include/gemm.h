@@ -230,6 +230,49 @@ const char* gemm_status_string(gemm_status_t status);
 /* ABI version of this header (major * 100 + minor). */
 int gemm_abi_version(void);
 
+/* ---------------------------------------------------------------------------
+ * gemm_run_s8_noalloc -- the exact int8 GEMM (int32 accumulation, the same
+ * kernels as gemm_run on an S8 plan) without allocating any device memory.
+ * The paper has no counterpart: this is a service of the library.
+ *
+ * Why: some callers cannot allocate device memory when they call the GEMM --
+ * a process whose device memory was reserved up front by a framework's memory
+ * pool (a cudaMalloc would fail or fragment the pool), a latency-bound loop
+ * that must not pay for cudaMalloc/cudaFree and the synchronisation they
+ * imply, or a program held to a memory budget fixed in advance.  gemm_run on
+ * an S8 plan allocates its fp16 staging of A and B on demand and the plan
+ * allocates an error word; this entry point needs neither a plan nor an
+ * allocation: the staging lives in a fixed array inside the library,
+ * GEMM_NOALLOC_SCRATCH_BYTES per device, which every GPU that loads the
+ * library holds until the process exits.
+ *
+ *   Arguments mean what they mean for gemm_run with an (S8, S32) plan, on the
+ *   current CUDA device; inputs and outputs are caller-owned device buffers.
+ *   status  optional caller-owned device word (4 bytes) that receives
+ *           GEMM_ERR_TIMEOUT if an in-kernel wait expires; NULL selects a word
+ *           inside the library, which each call first clears to zero.
+ * Limits: the staging needs 2 bytes per element of A's storage (rounded up to
+ * 256 bytes) plus 2 bytes per element of B's storage; a problem needing more
+ * than GEMM_NOALLOC_SCRATCH_BYTES returns GEMM_ERR_UNSUPPORTED before anything
+ * is launched.  With K > 0, lda and ldb must be multiples of 8, else
+ * GEMM_ERR_ALIGNMENT.
+ * The first call on a device looks up the device address of the array
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.
+ * Every call shares the array, which keeps the last call's contents; calls
+ * that overlap on the GPU (other streams, other host threads) race on it, so
+ * the caller must serialise them.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ * ------------------------------------------------------------------------- */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+gemm_status_t gemm_run_s8_noalloc(gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                  int64_t M, int64_t N, int64_t K, double alpha,
+                                  const void* A, int64_t lda, const void* B, int64_t ldb,
+                                  double beta, const void* C, int64_t ldc, void* D, int64_t ldd,
+                                  const gemm_epilogue_t* epi, int32_t* status,
+                                  gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

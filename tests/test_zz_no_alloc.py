@@ -1,0 +1,86 @@
+"""The allocation-free int8 entry point, gemm_run_s8_noalloc, against gemm_run.
+
+Some callers cannot allocate device memory when they call the GEMM: their
+device memory was reserved up front by a framework's memory pool, or their loop
+cannot afford cudaMalloc/cudaFree and the synchronisation those imply.
+gemm_run_s8_noalloc serves them from a fixed staging array that the library
+holds on each device.  This test calls it through the C ABI and checks its
+output against the plan-based entry point (gemm_run) on the same inputs --
+bit for bit, the tolerance every int8 test here uses -- on two calls in a row
+(the second call reuses the array the first one left filled, with other shapes
+and layouts), and checks that a problem too large for the array is refused
+before anything is launched.
+
+The file name makes pytest collect it last, so a run that stops at the first
+failure has already run every other test.  It needs no state from them.
+"""
+import pytest
+import torch
+
+import dense_gemm_epilogues_gb300 as G
+from dense_gemm_epilogues_gb300 import inputs as I
+
+import parity_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    G.load_library()
+
+
+def _noalloc_run(dp: H.DeviceProblem, status_ptr=None):
+    p = dp.p
+    G.gemm_run_s8_noalloc(G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M, p.N, p.K,
+                          p.alpha, dp.A.data_ptr(), p.lda, dp.B.data_ptr(), p.ldb, p.beta,
+                          dp.C.data_ptr() if dp.C is not None else None, p.ldc if p.c else 0,
+                          dp.D.data_ptr(), p.ldd, dp.epilogue(), status_ptr,
+                          torch.cuda.current_stream().cuda_stream)
+
+
+PROBLEMS = [
+    H.tma_aligned(I.Problem("noalloc_1", "s8", "T", "N", 1000, 776, 1544, d="s32",
+                            dist_a=I.I8, dist_b=I.I8)),
+    H.tma_aligned(I.Problem("noalloc_2", "s8", "N", "T", 520, 1032, 2056, alpha=2.0, beta=-3.0,
+                            c="s32", d="s32", bias="s32", bias_mode="col", act="relu",
+                            dist_a=I.I8, dist_b=I.I8, dist_c=I.Dist("int", -1000, 1000),
+                            dist_bias=I.Dist("int", -500, 500))),
+]
+
+
+def test_noalloc_matches_gemm_run_on_two_calls_in_a_row():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call, p in enumerate(PROBLEMS):
+        inp = I.generate(p, 300 + call)
+        ref = H.DeviceProblem(inp)
+        plan = H.make_plan(p)
+        ref.run(plan)                                  # the existing entry point
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        assert plan.last_config()["kernel"] == G.GEMM_KERNEL_TC_INT8
+        plan.close()
+
+        got = H.DeviceProblem(inp)
+        _noalloc_run(got, status.data_ptr() if call == 1 else None)
+        torch.cuda.synchronize()
+        got.check_guards()
+        H.check_close(got.result(), ref.result().cpu().numpy(), "s32", f"no-alloc call {call + 1}")
+    assert int(status.item()) == 0
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    p = I.Problem("noalloc_big", "s8", "T", "N", 4096, 4096, 4096, d="s32")
+    need = 2 * (p.M * p.K + p.N * p.K)
+    assert need > G.NOALLOC_SCRATCH_BYTES
+    D = torch.empty((p.M, p.N), dtype=torch.int32, device="cuda")
+    A = torch.zeros((p.M, p.K), dtype=torch.int8, device="cuda")
+    B = torch.zeros((p.N, p.K), dtype=torch.int8, device="cuda")
+    with pytest.raises(G.GemmError) as e:
+        G.gemm_run_s8_noalloc(G.GEMM_OP_T, G.GEMM_OP_N, p.M, p.N, p.K, 1.0, A.data_ptr(), p.K,
+                              B.data_ptr(), p.K, 0.0, None, 0, D.data_ptr(), p.N,
+                              G.make_epilogue(G.GEMM_S32), None,
+                              torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == G.GEMM_ERR_UNSUPPORTED
