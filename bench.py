@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--suite", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run one named workload --iters times (profiling driver); see CASES")
+    ap.add_argument("--iters", type=int, default=3)
     return ap.parse_args()
 
 
@@ -462,9 +465,64 @@ def run_suite(G, device, warmup=3, iters=10):
         torch.cuda.empty_cache()
 
 
+def _cases():
+    from dense_gemm_epilogues_gb300 import inputs as I
+    return {
+        "square4096_tn_ab": I.square_fp16_8192("TN").with_(name="gemm_f16_tn_4096_ab", M=4096,
+                                                          N=4096, K=4096),
+        "square4096_nt_ab": I.square_fp16_8192("NT").with_(name="gemm_f16_nt_4096_ab", M=4096,
+                                                          N=4096, K=4096),
+        "square8192_tn_ab": I.square_fp16_8192("TN"),
+        "fc": I.fc_bf16_8192x4096x11008(),
+        "int8_4096": I.int8_8192().with_(name="gemm_s8_tn_4096", M=4096, N=4096, K=4096),
+        "sgemm4096": I.sgemm_4096_bias_relu(),
+        "skinny": I.skinny_fp16_16384x64x16384(),
+    }
+
+
+def run_case(name: str, iters: int):
+    """Run one workload `iters` times on cuda:0 and print per-call times
+    (a driver for profilers; its numbers are not benchmark results)."""
+    import torch
+    import dense_gemm_epilogues_gb300 as G
+    from dense_gemm_epilogues_gb300 import inputs as I
+    p = _cases()[name]
+    inp = I.generate(p, I.BASE_SEED + 7)
+    dev = torch.device("cuda", 0)
+    A, B = inp.A.to(dev), inp.B.to(dev)
+    C = inp.C.to(dev) if inp.C is not None else None
+    bias = inp.bias.to(dev) if inp.bias is not None else None
+    D = torch.empty((p.M, p.ldd), dtype=I.TORCH_DTYPES[p.d], device=dev)
+    cc = p.c or ("s32" if p.ab == "s8" else "f32")
+    plan = G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[cc], 0)
+    bm = {"none": G.GEMM_BIAS_NONE, "col": G.GEMM_BIAS_COL, "row": G.GEMM_BIAS_ROW}[p.bias_mode]
+    epi = G.make_epilogue(G.DTYPE_CODES[p.d], bias.data_ptr() if bias is not None else 0,
+                          G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32, bm,
+                          G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(iters):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M, p.N,
+                   p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                   C.data_ptr() if C is not None else None, p.ldc if C is not None else 0,
+                   D.data_ptr(), p.ldd, epi, stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": name, "iter": i, "ms": round(e0.elapsed_time(e1), 4),
+                          "config": plan.last_config()}), flush=True)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status non-zero")
+    plan.close()
+
+
 def main():
     args = parse_args()
     rank, world, local_rank = dist_info()
+    if args.case:
+        run_case(args.case, args.iters)
+        return
     if args.impl == "reference":
         bench_reference(args, rank, world)
         return
