@@ -27,10 +27,11 @@ GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S8, GEMM_S32 = range(5)
 GEMM_ACT_NONE, GEMM_ACT_RELU = 0, 1
 GEMM_BIAS_NONE, GEMM_BIAS_COL, GEMM_BIAS_ROW = 0, 1, 2
 (GEMM_KERNEL_AUTO, GEMM_KERNEL_NONE, GEMM_KERNEL_TC, GEMM_KERNEL_TC_INT8, GEMM_KERNEL_FFMA,
- GEMM_KERNEL_SIMT) = range(6)
+ GEMM_KERNEL_SIMT, GEMM_KERNEL_TC_PAIR) = range(7)
 
 KERNEL_NAMES = {GEMM_KERNEL_AUTO: "auto", GEMM_KERNEL_NONE: "none", GEMM_KERNEL_TC: "tc",
-                GEMM_KERNEL_TC_INT8: "tc_int8", GEMM_KERNEL_FFMA: "ffma", GEMM_KERNEL_SIMT: "simt"}
+                GEMM_KERNEL_TC_INT8: "tc_int8", GEMM_KERNEL_FFMA: "ffma", GEMM_KERNEL_SIMT: "simt",
+                GEMM_KERNEL_TC_PAIR: "tc_pair"}
 DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "s8": GEMM_S8, "s32": GEMM_S32}
 LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 

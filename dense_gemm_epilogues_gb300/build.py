@@ -17,7 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgemm.so")
-SOURCES = ["gemm_api.cu", "tc_kernel.cu", "simt_kernels.cu"]
+SOURCES = ["gemm_api.cu", "tc_kernel.cu", "tc2_kernel.cu", "simt_kernels.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

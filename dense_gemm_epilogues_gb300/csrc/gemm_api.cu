@@ -27,6 +27,7 @@ struct gemm_plan {
   void* stage = nullptr;             // gemm_run_host device buffers
   size_t stage_bytes = 0;
   gemm_kernel_t forced = GEMM_KERNEL_AUTO;
+  int pair_clusters = 0;             // co-resident CTA-pair clusters (0: pair kernel unavailable)
   gemm_config_t last{};
   uint64_t timeout_ns = 4000000000ull;
 };
@@ -110,9 +111,11 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
 // does half the MMA work of a 128x256 tile but keeps the fixed per-tile costs).
 double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 4096^3 and 1024^3 fp16
 
+// pair_clusters: co-resident clusters of two CTAs for the CTA-pair kernel on the
+// target device (0: that kernel is not considered unless forced).
 gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
                             int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                            int sm_count, gemm_kernel_t forced, gemm_config_t* out) {
+                            int sm_count, gemm_kernel_t forced, gemm_config_t* out, int pair_clusters = 0) {
   (void)c;
   gemm_config_t cfg{};
   cfg.split_k = 1;
@@ -134,6 +137,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
     bool type_ok = true, feasible = true;
     switch (forced) {
       case GEMM_KERNEL_TC: type_ok = is_f16ish(ab); feasible = tc_ok; break;
+      case GEMM_KERNEL_TC_PAIR: type_ok = is_f16ish(ab); feasible = tc_ok && pair_clusters > 0; break;
       case GEMM_KERNEL_TC_INT8: type_ok = ab == GEMM_S8; feasible = int8_ok; break;
       case GEMM_KERNEL_FFMA: type_ok = ab == GEMM_F32; feasible = ffma_ok; break;
       case GEMM_KERNEL_SIMT: break;
@@ -144,11 +148,28 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
   } else {
     k = tc_ok ? GEMM_KERNEL_TC
               : int8_ok ? GEMM_KERNEL_TC_INT8 : ffma_ok ? GEMM_KERNEL_FFMA : GEMM_KERNEL_SIMT;
+    // Both dimensions above one 128-wide tile: 256 x 256 tiles on CTA pairs move
+    // a third fewer operand bytes per SM for the same MMA work.
+    bool pair = k == GEMM_KERNEL_TC && pair_clusters > 0 && M > 128 && N > 128;
+    if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) pair = pair && std::atoi(env) != 1;
+    if (pair) k = GEMM_KERNEL_TC_PAIR;
   }
   (void)la;
   (void)lb;
   cfg.kernel = k;
   switch (k) {
+    case GEMM_KERNEL_TC_PAIR: {
+      cfg.bm = 2 * TC_BM;
+      cfg.bn = 256;
+      cfg.bk = TC_BK;
+      cfg.stages = tc_pair_stages();
+      cfg.cta_group = 2;
+      const int64_t tiles_m = (M + 255) / 256, tiles_n = (N + 255) / 256;
+      cfg.tiles = (int32_t)std::min<int64_t>(tiles_m * tiles_n, kMaxDim);
+      cfg.raster = (int32_t)std::min<int64_t>(8, tiles_m);
+      cfg.grid = 2 * (int32_t)std::min<int64_t>(cfg.tiles, pair_clusters);
+      break;
+    }
     case GEMM_KERNEL_TC:
     case GEMM_KERNEL_TC_INT8: {
       int bn = 128;
@@ -241,10 +262,10 @@ bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_
 // tcgen05 instruction descriptor, kind::f16 with fp32 accumulation:
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16, 1 = bf16),
 //   15 / 16 A / B MN-major, 17-22 N >> 3, 24-28 M >> 4.
-uint32_t make_idesc(bool bf16, int bn, bool a_mn_major, bool b_mn_major) {
+uint32_t make_idesc(bool bf16, int bn, bool a_mn_major, bool b_mn_major, int bm = TC_BM) {
   const uint32_t f = bf16 ? 1u : 0u;
   return (1u << 4) | (f << 7) | (f << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+         ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(bm >> 4) << 24);
 }
 
 struct DeviceGuard {
@@ -337,6 +358,41 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   return launch_tc(tp, bn, cfg.grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// The CTA-pair kernel: each CTA of a pair loads 128 rows of A and 128 columns
+// of B per K block, so both tensor maps use 128-row (K-major) or 64 x 64
+// (MN-major) boxes; the MMA instruction covers M = 256, N = 256.
+gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
+                                  int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                                  int64_t ldb, bool bf16, const EpiParams& epi, cudaStream_t stream) {
+  TcParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const bool a_mn = la == GEMM_OP_N, b_mn = lb == GEMM_OP_T;
+  bool ok;
+  if (!a_mn) ok = encode_2d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, TC_BK, TC_BM);
+  else ok = encode_2d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, 64, TC_BK);
+  if (!ok) return GEMM_ERR_CUDA;
+  if (!b_mn) ok = encode_2d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, TC_BK, 128);
+  else ok = encode_2d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, TC_BK);
+  if (!ok) return GEMM_ERR_CUDA;
+  tp.M = (int32_t)M;
+  tp.N = (int32_t)N;
+  tp.K = (int32_t)K;
+  tp.num_kb = (int32_t)((K + TC_BK - 1) / TC_BK);
+  tp.tiles_m = (int32_t)((M + 255) / 256);
+  tp.tiles_n = (int32_t)((N + 255) / 256);
+  tp.num_tiles = tp.tiles_m * tp.tiles_n;
+  tp.raster = cfg.raster > 0 ? cfg.raster : 1;
+  tp.a_mn_major = a_mn ? 1 : 0;
+  tp.b_mn_major = b_mn ? 1 : 0;
+  tp.idesc = make_idesc(bf16, 256, a_mn, b_mn, 256);
+  tp.chunk_kb = 0;
+  tp.epi = epi;
+  tp.err = plan->d_err;
+  tp.timeout_ns = plan->timeout_ns;
+  return launch_tc_pair(tp, cfg.grid / 2, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -370,7 +426,7 @@ gemm_status_t gemm_select(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gem
   const double alpha_probe = ab == GEMM_S8 ? 1.0 : 1.0;
   gemm_status_t s = validate(ab, c, la, lb, M, N, K, alpha_probe, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
-  return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out);
+  return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out, sm_count / 2);
 }
 
 gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab, gemm_dtype_t c, int device) {
@@ -397,6 +453,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab, gemm_dtype_t 
     delete p;
     return GEMM_ERR_CUDA;
   }
+  p->pair_clusters = tc_pair_max_clusters(device);
   *plan = p;
   return GEMM_OK;
 }
@@ -415,7 +472,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
 gemm_status_t gemm_plan_set_kernel(gemm_plan_t plan, gemm_kernel_t kernel) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
   if (kernel != GEMM_KERNEL_AUTO && kernel != GEMM_KERNEL_TC && kernel != GEMM_KERNEL_TC_INT8 &&
-      kernel != GEMM_KERNEL_FFMA && kernel != GEMM_KERNEL_SIMT)
+      kernel != GEMM_KERNEL_FFMA && kernel != GEMM_KERNEL_SIMT && kernel != GEMM_KERNEL_TC_PAIR)
     return GEMM_ERR_INVALID_ARG;
   plan->forced = kernel;
   return GEMM_OK;
@@ -454,7 +511,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
   gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
   gemm_config_t cfg{};
-  s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count, plan->forced, &cfg);
+  s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count, plan->forced, &cfg,
+                    plan->pair_clusters);
   if (s != GEMM_OK) return s;
   if (cfg.kernel == GEMM_KERNEL_NONE) {
     plan->last = cfg;
@@ -466,6 +524,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
   const EpiParams e = make_epi(plan, alpha, beta, C, ldc, D, ldd, epi);
 
   switch (cfg.kernel) {
+    case GEMM_KERNEL_TC_PAIR:
+      s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb, plan->ab == GEMM_BF16, e, stream);
+      break;
     case GEMM_KERNEL_TC: {
       const bool bf16 = plan->ab == GEMM_BF16;
       s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb,

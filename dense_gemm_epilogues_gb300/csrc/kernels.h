@@ -33,6 +33,13 @@ int tc_stages(int bn);
 size_t tc_smem_bytes(int bn);
 cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream);
 
+// CTA-pair tensor-core kernel (cta_group::2): 256 x 256 tiles per cluster of two CTAs.
+// Tensor-map boxes: A as for 128-row tiles, B as for 128-column tiles.
+int tc_pair_stages();
+size_t tc_pair_smem_bytes();
+int tc_pair_max_clusters(int device);   // co-resident clusters of two (0 if unknown)
+cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream);
+
 // FFMA SGEMM (fp32, CUDA cores).
 struct FfmaParams {
   const float* A;

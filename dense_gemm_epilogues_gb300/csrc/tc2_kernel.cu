@@ -1,0 +1,292 @@
+// tc2_kernel.cu -- tcgen05 GEMM on CTA pairs (cta_group::2), 256 x 256 tiles.
+//
+// Same computation and epilogue as tc_kernel.cu, with one output tile of
+// 256 (M) x 256 (N) per cluster of two CTAs on two SMs:
+//   - CTA r of the pair stages, per 64-deep K block, its own 128 rows of A
+//     (rows m0 + 128r ...) and its own half of B (columns n0 + 128r ...) --
+//     32 KiB per stage, six stages -- so each SM moves 2/3 of the operand bytes
+//     of a 128 x 256 single-CTA tile for the same MMA work;
+//   - both CTAs' TMA loads complete on the leader CTA's (rank 0) full barrier;
+//   - one thread of the leader issues tcgen05.mma.cta_group::2 (M = 256,
+//     N = 256, K = 16): the hardware takes A's rows from both CTAs and B's halves
+//     from both CTAs, and writes each CTA's 128 rows of D into that CTA's tensor
+//     memory (two 256-column fp32 accumulators per CTA, double buffered);
+//   - its commits arrive on both CTAs' barriers (multicast): the stage-free
+//     barriers that the two producers wait on and the accumulator-full barriers
+//     the two epilogues wait on;
+//   - the epilogue warps of both CTAs finish their 128 rows (alpha, beta*C,
+//     bias, ReLU, cast, 16-byte stores) and release the accumulator on the
+//     leader's barrier (the peer's four warps arrive remotely).
+// No TMA multicast is used: every CTA loads only its own data.
+// Every mbarrier wait is bounded, as in tc_kernel.cu.
+#include "kernels.h"
+
+namespace gemmlib {
+namespace {
+
+constexpr int PAIR_BN = 256;                            // tile columns (both CTAs)
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = TC_BM * TC_BK * 2;          // 16 KiB: this CTA's 128 rows of A
+constexpr int PAIR_B_BYTES = (PAIR_BN / 2) * TC_BK * 2;  // 16 KiB: this CTA's half of B
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns of TMEM
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 1;
+constexpr size_t PAIR_SMEM = 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
+constexpr int PAIR_THREADS = 192;
+constexpr uint32_t PAIR_TMEM_COLS = 512;
+constexpr int MN_BOX = 64;
+constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;
+
+__device__ __forceinline__ void pair_tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+  const int group_tiles = p.raster * p.tiles_n;
+  const int g = t / group_tiles;
+  const int first_m = g * p.raster;
+  const int gsize = min(p.tiles_m - first_m, p.raster);
+  const int r = t - g * group_tiles;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+__device__ __forceinline__ void drain_wait_pair(uint32_t bar, uint32_t parity, uint64_t user_timeout_ns) {
+  const uint64_t timeout_ns = user_timeout_ns > 1000000000ull ? user_timeout_ns : 1000000000ull;
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+__device__ __forceinline__ bool warp_wait_pair(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
+    tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;   // same offset in both CTAs
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar0 = base + (uint32_t)(PAIR_STAGES * PAIR_STAGE_BYTES);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(base_ptr + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(PAIR_STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + PAIR_ACC_BUFS + b); };
+  const uint32_t teardown_bar = bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster_id = (int)(blockIdx.x >> 1);
+  const int num_clusters = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);    // leader: its expect_tx arrival + both CTAs' TMA bytes
+      mbar_init(empty_bar(s), 1);   // the leader's multicast commit
+    }
+    for (int b = 0; b < PAIR_ACC_BUFS; ++b) {
+      mbar_init(tfull_bar(b), 1);   // the leader's multicast commit
+      mbar_init(tempty_bar(b), 8);  // leader: four epilogue warps of each CTA
+    }
+    mbar_init(teardown_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  cluster_sync();                                   // both CTAs' barriers exist
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), PAIR_TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();                                   // tensor memory allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tmA);
+      tma_prefetch_desc(&p.tmB);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        int tm, tn;
+        pair_tile_coords(t, p, tm, tn);
+        const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
+        const int n0 = tn * PAIR_BN + (int)rank * (PAIR_BN / 2);    // this CTA's half of B
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb_local = full_bar(stage);
+          if (leader) mbar_expect_tx(fb_local, 2u * PAIR_STAGE_BYTES);
+          const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, 0);
+          const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+          const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
+          const int k0 = kb * TC_BK;
+          if (p.a_mn_major) {
+#pragma unroll
+            for (int h = 0; h < TC_BM / MN_BOX; ++h)
+              tma_load_2d_pair(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, fb);
+          } else {
+            tma_load_2d_pair(sa, &p.tmA, k0, m0, fb);
+          }
+          if (p.b_mn_major) {
+#pragma unroll
+            for (int h = 0; h < (PAIR_BN / 2) / MN_BOX; ++h)
+              tma_load_2d_pair(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, fb);
+          } else {
+            tma_load_2d_pair(sb, &p.tmB, k0, n0, fb);
+          }
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // The leader's full barriers count both CTAs' bytes: once its drains pass,
+      // every copy of the pair has landed (the peer waits at the final cluster barrier).
+      if (leader) {
+        for (int s = 0; s < PAIR_STAGES; ++s)
+          if (issued & (1u << s)) drain_wait_pair(full_bar(s), (last_parity >> s) & 1u, p.timeout_ns);
+      } else if (!ok) {
+        // Wind-down after a failure: give this CTA's own copies time to land
+        // before it can leave (they complete on the leader's barrier).
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------- MMA issuer (leader CTA only) ----------------------
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_it = 0;
+      bool ok = true;
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        const int buf = (int)(acc_it % PAIR_ACC_BUFS);
+        const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
+        if (!mbar_wait(tempty_bar(buf), apar ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PAIR_BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+          const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
+                                             : smem_desc_sw128(sa + kk * 32u, 16, 1024);
+            const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
+                                             : smem_desc_sw128(sb + kk * 32u, 16, 1024);
+            tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(empty_bar(stage), 0x3);
+          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(tfull_bar(buf), 0x3);
+        ++acc_it;
+      }
+      tc_commit_pair(teardown_bar);
+      drain_wait_pair(teardown_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // ---------------------------- epilogue (both CTAs) ----------------------------
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+      int tm, tn;
+      pair_tile_coords(t, p, tm, tn);
+      const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + q * 32 + lane;
+      const int64_t n0 = (int64_t)tn * PAIR_BN;
+      const bool row_ok = m < p.M;
+      const int buf = (int)(acc_it % PAIR_ACC_BUFS);
+      const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
+      if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN);
+#pragma unroll 1
+      for (int c = 0; c < PAIR_BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+        tmem_wait_ld();
+        if (row_ok) {
+          float x[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
+          epi_finish_row32_float(p.epi, m, p.M, n0 + c * 32, p.N, x);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(buf));
+        else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+      }
+      ++acc_it;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();       // neither CTA leaves while the other may still signal it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
+}
+
+}  // namespace
+
+size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
+int tc_pair_stages() { return PAIR_STAGES; }
+
+int tc_pair_max_clusters(int device) {
+  static int cached[64] = {};
+  if (device < 0 || device >= 64) return 0;
+  if (cached[device] > 0) return cached[device];
+  if (cudaFuncSetAttribute(tc_pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PAIR_SMEM) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 512, 1, 1);
+  cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PAIR_SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached[device] = n;
+  return n;
+}
+
+cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
+  static_assert(PAIR_SMEM <= 232448, "shared memory budget");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured[64] = {};
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PAIR_SMEM);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  if (clusters <= 0) return cudaErrorInvalidValue;
+  tc_pair_gemm_kernel<<<2 * clusters, PAIR_THREADS, PAIR_SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gemmlib

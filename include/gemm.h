@@ -94,7 +94,8 @@ typedef enum {
     GEMM_KERNEL_TC = 2,     /* tcgen05 + TMA persistent warp-specialised kernel, fp16/bf16 */
     GEMM_KERNEL_TC_INT8 = 3,/* int8 exact: int8->fp16 staging, tcgen05 in K-chunks, int32 accumulation */
     GEMM_KERNEL_FFMA = 4,   /* fp32 SGEMM on CUDA cores, register-blocked FFMA */
-    GEMM_KERNEL_SIMT = 5    /* generic CUDA-core kernel: any alignment, K == 0, every dtype */
+    GEMM_KERNEL_SIMT = 5,   /* generic CUDA-core kernel: any alignment, K == 0, every dtype */
+    GEMM_KERNEL_TC_PAIR = 6 /* tcgen05 on CTA pairs (cta_group::2), 256x256 tiles, fp16/bf16 */
 } gemm_kernel_t;
 
 /* A launch configuration (what the selector returns; what a run used). */

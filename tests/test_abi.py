@@ -96,22 +96,27 @@ def _sel(ab=G.GEMM_F16, c=G.GEMM_F32, la=G.GEMM_OP_T, lb=G.GEMM_OP_N, M=8192, N=
     return G.gemm_select(ab, c, la, lb, M, N, K, A, lda, B, ldb, None, 0, P, N, 0.0, epi, sms)
 
 
-def test_selector_large_square_uses_128x256_tensor_core_tiles():
+def test_selector_large_square_uses_256x256_pair_tiles():
     cfg = _sel()
-    assert cfg["kernel"] == G.GEMM_KERNEL_TC
-    assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (128, 256, 64)
-    assert cfg["tiles"] == 64 * 32 and cfg["grid"] == 152 and cfg["raster"] == 16
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["cta_group"] == 2
+    assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (256, 256, 64)
+    assert cfg["tiles"] == 32 * 32 and cfg["grid"] == 152 and cfg["raster"] == 8
+
+
+def test_selector_single_cta_when_one_dimension_fits_one_tile():
+    cfg = _sel(M=128, N=8192)
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC and cfg["bm"] == 128
 
 
 @pytest.mark.parametrize("la,lb", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_selector_all_layouts_on_tensor_cores(la, lb):
-    assert _sel(la=la, lb=lb)["kernel"] == G.GEMM_KERNEL_TC
+    assert _sel(la=la, lb=lb)["kernel"] == G.GEMM_KERNEL_TC_PAIR
 
 
 def test_selector_narrow_and_small_shapes():
     assert _sel(N=64, M=16384, K=16384)["bn"] == 128
     cfg = _sel(M=512, N=512, K=512)
-    assert cfg["bn"] == 128 and cfg["grid"] == cfg["tiles"] == 16
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["tiles"] == 4 and cfg["grid"] == 8
 
 
 def test_selector_misaligned_operands_use_generic_kernel():

@@ -18,6 +18,8 @@ import parity_helpers as H
 pytestmark = pytest.mark.gpu
 
 LAYOUTS = ["NN", "NT", "TN", "TT"]
+TC_KERNELS = [G.GEMM_KERNEL_TC, G.GEMM_KERNEL_TC_PAIR]
+TC_IDS = ["cta1", "pair"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -31,50 +33,64 @@ def _cuda():
 
 # ------------------------------- tensor cores --------------------------------
 
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("ab", ["f16", "bf16"])
-def test_tc_ragged_alpha_beta(layout, ab):
-    """Several 128x256 tiles with ragged M, N, K tails; alpha/beta with fp32 C."""
+def test_tc_ragged_alpha_beta(layout, ab, kernel):
+    """Several tiles with ragged M, N, K tails; alpha/beta with fp32 C; both
+    tensor-core kernels (one CTA per tile, CTA pairs)."""
     p = H.tma_aligned(I.Problem("tc_ab", ab, layout[0], layout[1], 300, 520, 200, alpha=1.5,
                                   beta=0.5, c="f32"))
-    H.run_and_check_full(p, 101, expect_kernel=G.GEMM_KERNEL_TC)
+    H.run_and_check_full(p, 101, kernel=kernel, expect_kernel=kernel)
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_tc_bias_relu_bf16_out(layout):
+def test_selector_picks_pair_kernel_for_large_tiles(layout):
+    p = H.tma_aligned(I.Problem("tc_auto", "f16", layout[0], layout[1], 520, 300, 136))
+    H.run_and_check_full(p, 120, expect_kernel=G.GEMM_KERNEL_TC_PAIR)
+
+
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_tc_bias_relu_bf16_out(layout, kernel):
     p = H.tma_aligned(I.Problem("tc_fc", "bf16", layout[0], layout[1], 257, 384, 320, d="bf16",
                                 bias="f32", bias_mode="col", act="relu",
                                 dist_a=I.Dist("normal", std=1.0), dist_b=I.Dist("normal", std=0.05)))
-    H.run_and_check_full(p, 102, expect_kernel=G.GEMM_KERNEL_TC)
+    H.run_and_check_full(p, 102, kernel=kernel, expect_kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
 @pytest.mark.parametrize("n", [64, 96, 128, 129, 200])
-def test_tc_narrow_n_tiles(n):
-    """N <= 128 selects 128-wide tiles; N just above selects by the wave model."""
+def test_tc_narrow_n_tiles(n, kernel):
+    """N <= 128 selects 128-wide single-CTA tiles; forcing the pair kernel there
+    leaves the second CTA's half of B entirely out of bounds (zero-filled)."""
     p = H.tma_aligned(I.Problem("tc_n", "f16", "T", "N", 256, n, 192))
-    H.run_and_check_full(p, 103, expect_kernel=G.GEMM_KERNEL_TC)
+    H.run_and_check_full(p, 103, kernel=kernel, expect_kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
 @pytest.mark.parametrize("c,d", [("f16", "f16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f16")])
-def test_tc_c_and_d_types(c, d):
+def test_tc_c_and_d_types(c, d, kernel):
     ab = "bf16" if "bf16" in (c, d) else "f16"
     p = H.tma_aligned(I.Problem("tc_cd", ab, "N", "T", 200, 300, 136, alpha=-0.75, beta=1.25, c=c,
                                 d=d, bias="bf16" if ab == "bf16" else "f16", bias_mode="row",
                                 act="relu"))
-    H.run_and_check_full(p, 104, expect_kernel=G.GEMM_KERNEL_TC)
+    H.run_and_check_full(p, 104, kernel=kernel, expect_kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_tc_padded_leading_dims(layout):
+def test_tc_padded_leading_dims(layout, kernel):
     """Leading dimensions larger than the logical extent (poisoned padding, 16-byte
     multiples) and a padded, unaligned-width D."""
     p = H.tma_aligned(I.Problem("tc_pad", "f16", layout[0], layout[1], 190, 270, 150, beta=1.0,
                                 c="f32", pad_a=8, pad_b=16, pad_c=3, pad_d=5))
-    H.run_and_check_full(p, 105, expect_kernel=G.GEMM_KERNEL_TC)
+    H.run_and_check_full(p, 105, kernel=kernel, expect_kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_tc_small_integers_bit_exact(layout):
+def test_tc_small_integers_bit_exact(layout, kernel):
     """Small-integer data is exact in every step, so the tensor-core result must
     equal the oracle bit for bit (fp32 out)."""
     p = H.tma_aligned(I.Problem("tc_exact", "f16", layout[0], layout[1], 260, 300, 520, alpha=2.0,
@@ -84,19 +100,21 @@ def test_tc_small_integers_bit_exact(layout):
                                 act="relu"))
     inp = I.generate(p, 106)
     dp = H.DeviceProblem(inp)
-    plan = H.make_plan(p)
+    plan = H.make_plan(p, kernel)
     dp.run(plan)
     torch.cuda.synchronize()
-    assert plan.last_config()["kernel"] == G.GEMM_KERNEL_TC
+    assert plan.device_status() == 0
+    assert plan.last_config()["kernel"] == kernel
     np.testing.assert_array_equal(dp.result().cpu().numpy(), H.oracle_full(inp))
     dp.check_guards()
 
 
-def test_tc_in_place_c_equals_d():
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
+def test_tc_in_place_c_equals_d(kernel):
     p = I.Problem("inplace", "f16", "T", "N", 150, 260, 96, alpha=1.0, beta=2.0, c="f32")
     inp = I.generate(p, 107)
     ref = H.oracle_full(inp)
-    plan = H.make_plan(p)
+    plan = H.make_plan(p, kernel)
     A, B = inp.A.cuda(), inp.B.cuda()
     CD = inp.C.cuda()
     G.gemm_run(plan.handle, G.GEMM_OP_T, G.GEMM_OP_N, p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda,
@@ -106,11 +124,12 @@ def test_tc_in_place_c_equals_d():
     H.check_close(CD, ref, "f32", "in-place")
 
 
-def test_tc_many_tiles_persistent_loop():
-    """More tiles than SMs: every CTA walks several tiles (both accumulator buffers)."""
-    p = I.Problem("tc_many", "f16", "T", "N", 2560, 2560, 64, beta=0.5, c="f32")   # 200 tiles
-    cfg = H.run_and_check_full(p, 108, expect_kernel=G.GEMM_KERNEL_TC)
-    assert cfg["tiles"] > cfg["grid"]
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
+def test_tc_many_tiles_persistent_loop(kernel):
+    """More tiles than CTAs (pairs): each walks several tiles (both accumulator buffers)."""
+    p = I.Problem("tc_many", "f16", "T", "N", 3072, 2560, 64, beta=0.5, c="f32")
+    cfg = H.run_and_check_full(p, 108, kernel=kernel, expect_kernel=kernel)
+    assert cfg["tiles"] > cfg["grid"] // cfg["cta_group"]
 
 
 # ---------------------------------- int8 -------------------------------------
