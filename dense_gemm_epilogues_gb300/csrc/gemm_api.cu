@@ -166,7 +166,9 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.cta_group = 2;
       const int64_t tiles_m = (M + 255) / 256, tiles_n = (N + 255) / 256;
       cfg.tiles = (int32_t)std::min<int64_t>(tiles_m * tiles_n, kMaxDim);
-      cfg.raster = (int32_t)std::min<int64_t>(8, tiles_m);
+      int raster = 8;
+      if (const char* env = std::getenv("GEMM_TC_RASTER")) raster = std::max(1, std::atoi(env));
+      cfg.raster = (int32_t)std::min<int64_t>(raster, tiles_m);
       cfg.grid = 2 * (int32_t)std::min<int64_t>(cfg.tiles, pair_clusters);
       break;
     }
@@ -198,6 +200,18 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.raster = (int32_t)std::min<int64_t>(16, tiles_m);
       cfg.grid = (int32_t)std::min<int64_t>(cfg.tiles, sm_count);
       cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? 512 : 0;
+      bool pair_int = k == GEMM_KERNEL_TC_INT8 && pair_clusters > 0 && M > 128 && N > 128;
+      if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) pair_int = pair_int && std::atoi(env) != 1;
+      if (pair_int) {   // exact integer mode on CTA pairs: 256 x 256 tiles
+        cfg.bm = 2 * TC_BM;
+        cfg.bn = 256;
+        cfg.stages = tc_pair_stages();
+        cfg.cta_group = 2;
+        const int64_t ptm = (M + 255) / 256, ptn = (N + 255) / 256;
+        cfg.tiles = (int32_t)std::min<int64_t>(ptm * ptn, kMaxDim);
+        cfg.raster = (int32_t)std::min<int64_t>(8, ptm);
+        cfg.grid = 2 * (int32_t)std::min<int64_t>(cfg.tiles, pair_clusters);
+      }
       break;
     }
     case GEMM_KERNEL_FFMA: {
@@ -363,7 +377,8 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
 // (MN-major) boxes; the MMA instruction covers M = 256, N = 256.
 gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
                                   int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-                                  int64_t ldb, bool bf16, const EpiParams& epi, cudaStream_t stream) {
+                                  int64_t ldb, bool bf16, const EpiParams& epi, cudaStream_t stream,
+                                  int chunk_kb = 0) {
   TcParams tp;
   std::memset(&tp, 0, sizeof(tp));
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -386,7 +401,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   tp.a_mn_major = a_mn ? 1 : 0;
   tp.b_mn_major = b_mn ? 1 : 0;
   tp.idesc = make_idesc(bf16, 256, a_mn, b_mn, 256);
-  tp.chunk_kb = 0;
+  tp.chunk_kb = chunk_kb;
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
@@ -551,8 +566,12 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
         ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8, B16, N, K, ldb, stream)
                              : launch_s8_to_f16(B8, B16, K, N, ldb, stream);
       if (ce != cudaSuccess) { s = GEMM_ERR_CUDA; break; }
-      s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                            false, e, cfg.k_chunk / TC_BK, stream);
+      if (cfg.cta_group == 2)
+        s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, false, e, stream,
+                                cfg.k_chunk / TC_BK);
+      else
+        s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                              false, e, cfg.k_chunk / TC_BK, stream);
       break;
     }
     case GEMM_KERNEL_FFMA: {

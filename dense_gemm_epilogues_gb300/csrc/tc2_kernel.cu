@@ -17,6 +17,11 @@
 //   - the epilogue warps of both CTAs finish their 128 rows (alpha, beta*C,
 //     bias, ReLU, cast, 16-byte stores) and release the accumulator on the
 //     leader's barrier (the peer's four warps arrive remotely).
+// Exact integer mode (int8 operands staged as fp16): the MMA accumulates each
+// 512-deep K chunk into a fresh fp32 accumulator (exact, |sum| <= 2^23); eight
+// epilogue warps per CTA -- two per tensor-memory lane quarter, one per half of
+// the 256 columns -- convert each finished chunk to int32 and add it into 128
+// registers per thread, then apply the integer epilogue after the last chunk.
 // No TMA multicast is used: every CTA loads only its own data.
 // Every mbarrier wait is bounded, as in tc_kernel.cu.
 #include "kernels.h"
@@ -25,14 +30,20 @@ namespace gemmlib {
 namespace {
 
 constexpr int PAIR_BN = 256;                            // tile columns (both CTAs)
-constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = TC_BM * TC_BK * 2;          // 16 KiB: this CTA's 128 rows of A
 constexpr int PAIR_B_BYTES = (PAIR_BN / 2) * TC_BK * 2;  // 16 KiB: this CTA's half of B
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns of TMEM
+constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 1;
 constexpr size_t PAIR_SMEM = 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
-constexpr int PAIR_THREADS = 192;
+
+// Producer warp, MMA warp, then 4 epilogue warps (floating) or 8 (exact integer).
+template <bool INT_MODE>
+struct PairThreads {
+  static constexpr int EPI_WARPS = INT_MODE ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+};
 constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int MN_BOX = 64;
 constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;
@@ -61,8 +72,10 @@ __device__ __forceinline__ bool warp_wait_pair(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
+template <bool INT_MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
+  constexpr int EPI_WARPS = PairThreads<INT_MODE>::EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;   // same offset in both CTAs
@@ -92,7 +105,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     }
     for (int b = 0; b < PAIR_ACC_BUFS; ++b) {
       mbar_init(tfull_bar(b), 1);   // the leader's multicast commit
-      mbar_init(tempty_bar(b), 8);  // leader: four epilogue warps of each CTA
+      mbar_init(tempty_bar(b), 2 * EPI_WARPS);  // leader: every epilogue warp of both CTAs
     }
     mbar_init(teardown_bar, 1);
     *abort_flag = 0;
@@ -106,6 +119,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const int units_per_tile = INT_MODE ? (p.num_kb + p.chunk_kb - 1) / p.chunk_kb : 1;
+  const int kb_per_unit = INT_MODE ? p.chunk_kb : p.num_kb;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -167,37 +182,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
       uint32_t phase = 0, acc_it = 0;
       bool ok = true;
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-        const int buf = (int)(acc_it % PAIR_ACC_BUFS);
-        const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
-        if (!mbar_wait(tempty_bar(buf), apar ^ 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PAIR_BN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
+        for (int u = 0; ok && u < units_per_tile; ++u) {
+          const int buf = (int)(acc_it % PAIR_ACC_BUFS);
+          const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
+          if (!mbar_wait(tempty_bar(buf), apar ^ 1u, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
-          const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PAIR_BN);
+          const int kb_begin = u * kb_per_unit;
+          const int kb_end = min(p.num_kb, kb_begin + kb_per_unit);
+          for (int kb = kb_begin; kb < kb_end; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+            const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < TC_BK / 16; ++kk) {
-            const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
-                                             : smem_desc_sw128(sa + kk * 32u, 16, 1024);
-            const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
-                                             : smem_desc_sw128(sb + kk * 32u, 16, 1024);
-            tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < TC_BK / 16; ++kk) {
+              const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
+                                               : smem_desc_sw128(sa + kk * 32u, 16, 1024);
+              const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
+                                               : smem_desc_sw128(sb + kk * 32u, 16, 1024);
+              tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+            }
+            tc_commit_pair_multicast(empty_bar(stage), 0x3);
+            if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
           }
-          tc_commit_pair_multicast(empty_bar(stage), 0x3);
-          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+          tc_commit_pair_multicast(tfull_bar(buf), 0x3);
+          ++acc_it;
         }
-        if (!ok) break;
-        tc_commit_pair_multicast(tfull_bar(buf), 0x3);
-        ++acc_it;
       }
       tc_commit_pair(teardown_bar);
       drain_wait_pair(teardown_bar, 0, p.timeout_ns);
     }
   } else {
     // ---------------------------- epilogue (both CTAs) ----------------------------
-    const int q = warp & 3;
+    const int q = warp & 3;                                   // TMEM lane quarter of this warp
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t acc_it = 0;
     bool ok = true;
@@ -207,30 +226,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
       const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + q * 32 + lane;
       const int64_t n0 = (int64_t)tn * PAIR_BN;
       const bool row_ok = m < p.M;
-      const int buf = (int)(acc_it % PAIR_ACC_BUFS);
-      const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
-      if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN);
-#pragma unroll 1
-      for (int c = 0; c < PAIR_BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
-        tmem_wait_ld();
-        if (row_ok) {
-          float x[32];
+      if constexpr (INT_MODE) {
+        const int half = (warp - 2) >> 2;                     // columns 128*half ... 128*half + 127
+        int32_t acc[128];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
-          epi_finish_row32_float(p.epi, m, p.M, n0 + c * 32, p.N, x);
+        for (int j = 0; j < 128; ++j) acc[j] = 0;
+        for (int u = 0; u < units_per_tile; ++u) {
+          const int buf = (int)(acc_it % PAIR_ACC_BUFS);
+          const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
+          if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN + half * 128);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[c * 32 + j] += __float2int_rn(__uint_as_float(r[j]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(tempty_bar(buf));
+            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+          }
+          ++acc_it;
         }
+        if (!ok) break;
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            epi_finish_row32_int(p.epi, m, n0 + half * 128 + c * 32, p.N, &acc[c * 32]);
+        }
+      } else {
+        const int buf = (int)(acc_it % PAIR_ACC_BUFS);
+        const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
+        if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN);
+#pragma unroll 1
+        for (int c = 0; c < PAIR_BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+          tmem_wait_ld();
+          if (row_ok) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
+            epi_finish_row32_float(p.epi, m, p.M, n0 + c * 32, p.N, x);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(tempty_bar(buf));
+          else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+        }
+        ++acc_it;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(tempty_bar(buf));
-        else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
-      }
-      ++acc_it;
     }
   }
 
@@ -241,21 +295,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
 }
 
-}  // namespace
-
-size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
-int tc_pair_stages() { return PAIR_STAGES; }
-
-int tc_pair_max_clusters(int device) {
+template <bool INT_MODE>
+int max_clusters_for(int device) {
   static int cached[64] = {};
   if (device < 0 || device >= 64) return 0;
   if (cached[device] > 0) return cached[device];
-  if (cudaFuncSetAttribute(tc_pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PAIR_SMEM) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)PAIR_SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 512, 1, 1);
-  cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
+  cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -265,7 +315,7 @@ int tc_pair_max_clusters(int device) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -273,20 +323,37 @@ int tc_pair_max_clusters(int device) {
   return n;
 }
 
-cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
+template <bool INT_MODE>
+cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   static_assert(PAIR_SMEM <= 232448, "shared memory budget");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PAIR_SMEM);
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PAIR_SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   if (clusters <= 0) return cudaErrorInvalidValue;
-  tc_pair_gemm_kernel<<<2 * clusters, PAIR_THREADS, PAIR_SMEM, stream>>>(p);
+  tc_pair_gemm_kernel<INT_MODE><<<2 * clusters, PairThreads<INT_MODE>::THREADS, PAIR_SMEM, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_pair_stages() { return PAIR_STAGES; }
+size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
+
+int tc_pair_max_clusters(int device) {
+  const int a = max_clusters_for<false>(device);
+  const int b = max_clusters_for<true>(device);
+  return a < b ? a : b;
+}
+
+cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
+  return p.chunk_kb > 0 ? launch_mode<true>(p, clusters, stream) : launch_mode<false>(p, clusters, stream);
 }
 
 }  // namespace gemmlib

@@ -134,23 +134,43 @@ def test_tc_many_tiles_persistent_loop(kernel):
 
 # ---------------------------------- int8 -------------------------------------
 
+@pytest.fixture(params=[1, 2], ids=["cta1", "pair"])
+def cta_group(request, monkeypatch):
+    """Run the exact int8 path on single-CTA tiles (GEMM_TC_CTA_GROUP=1) or on
+    CTA pairs (the selector's choice when M and N exceed 128)."""
+    if request.param == 1:
+        monkeypatch.setenv("GEMM_TC_CTA_GROUP", "1")
+    else:
+        monkeypatch.delenv("GEMM_TC_CTA_GROUP", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_int8_exact_ragged(layout):
+def test_int8_exact_ragged(layout, cta_group):
     """K = 1100 spans two exact 512-chunks and a tail; bit-exact int32."""
     p = H.tma_aligned(I.Problem("i8", "s8", layout[0], layout[1], 260, 390, 1100, d="s32",
                                 dist_a=I.I8, dist_b=I.I8))
-    H.run_and_check_full(p, 109, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+    cfg = H.run_and_check_full(p, 109, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+    assert cfg["cta_group"] == cta_group
 
 
-def test_int8_adversarial_extremes_exact():
+def test_int8_adversarial_extremes_exact(cta_group):
     """All -128: every partial sum is 16384*k, far beyond fp32's exact range at
     K = 4096 (2^26), so a single fp32 accumulator would be wrong."""
     p = I.Problem("i8max", "s8", "T", "N", 130, 140, 4096, d="s32",
                   dist_a=I.Dist("int", -128, -128), dist_b=I.Dist("int", -128, -128))
-    H.run_and_check_full(p, 110, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+    cfg = H.run_and_check_full(p, 110, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+    assert cfg["cta_group"] == cta_group
 
 
-def test_int8_alpha_beta_bias_relu():
+def test_int8_many_tiles_and_chunks(cta_group):
+    """More tiles than CTA pairs and several exact chunks per tile."""
+    p = I.Problem("i8many", "s8", "T", "N", 2304, 2560, 1600, d="s32", dist_a=I.I8, dist_b=I.I8)
+    cfg = H.run_and_check_full(p, 121, expect_kernel=G.GEMM_KERNEL_TC_INT8)
+    assert cfg["cta_group"] == cta_group and cfg["tiles"] > cfg["grid"] // cfg["cta_group"]
+
+
+def test_int8_alpha_beta_bias_relu(cta_group):
     p = H.tma_aligned(I.Problem("i8epi", "s8", "N", "T", 200, 136, 700, alpha=3.0, beta=-2.0,
                                 c="s32", d="s32", bias="s32", bias_mode="col", act="relu",
                                 dist_a=I.I8, dist_b=I.I8, dist_c=I.Dist("int", -100000, 100000),
