@@ -82,12 +82,13 @@ __device__ __forceinline__ int32_t wrap_madd(int32_t a, int32_t b, int32_t c) {
 // The tensor-core epilogue gives each thread one row of the tile and 32
 // consecutive columns per TMEM load; these helpers finish such a chunk.
 
-// x[j] holds alpha*acc for columns n_base..n_base+31 of row m (m < M checked by caller).
-__device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64_t m, int64_t M_rows,
+// x[j] holds alpha*acc for columns n_base..n_base+31 of row m.  Called by all
+// 32 lanes of a warp together (the bias is shared by shuffles); lanes whose row
+// is outside D (row_ok false) take part but neither read C nor store.
+__device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64_t m, bool row_ok,
                                                        int64_t n_base, int64_t N, float (&x)[32]) {
-  (void)M_rows;
   const bool full = n_base + 32 <= N;
-  if (e.read_c) {
+  if (e.read_c && row_ok) {
     const int64_t off = m * e.ldc + n_base;
     if (full && e.vec_c) {
       if (e.c_dtype == GEMM_F32) {
@@ -128,14 +129,18 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
     }
   }
   if (e.bias_mode == GEMM_BIAS_COL) {
+    // Every lane needs the same 32 bias values: lane j loads bias[n_base + j]
+    // once (coalesced) and the warp shares them by shuffles.
+    const int lane = threadIdx.x & 31;
+    const float bl = (n_base + lane < N) ? load_as_float(e.bias, e.bias_dtype, n_base + lane) : 0.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n_base + j < N) x[j] += load_as_float(e.bias, e.bias_dtype, n_base + j);
-  } else if (e.bias_mode == GEMM_BIAS_ROW) {
+    for (int j = 0; j < 32; ++j) x[j] += __shfl_sync(0xffffffffu, bl, j);
+  } else if (e.bias_mode == GEMM_BIAS_ROW && row_ok) {
     const float b = load_as_float(e.bias, e.bias_dtype, m);
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] += b;
   }
+  if (!row_ok) return;
   if (e.relu) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = fmaxf(x[j], 0.0f);
@@ -172,13 +177,14 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
 }
 
 // x[j] holds the exact int32 product sums of columns n_base..n_base+31 of row m;
-// it is finished in place (alpha, beta*C, bias, ReLU) and stored.
-__device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t m, int64_t n_base,
-                                                     int64_t N, int32_t* x) {
+// it is finished in place (alpha, beta*C, bias, ReLU) and stored.  Called by all
+// 32 lanes of a warp together, as the floating version.
+__device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t m, bool row_ok,
+                                                     int64_t n_base, int64_t N, int32_t* x) {
   const bool full = n_base + 32 <= N;
 #pragma unroll
   for (int j = 0; j < 32; ++j) x[j] = wrap_madd(e.alpha_i, x[j], 0);
-  if (e.read_c) {
+  if (e.read_c && row_ok) {
     const int64_t off = m * e.ldc + n_base;
     if (full && e.vec_c) {
       const int4* c4 = reinterpret_cast<const int4*>(static_cast<const int32_t*>(e.C) + off);
@@ -197,14 +203,16 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t
     }
   }
   if (e.bias_mode == GEMM_BIAS_COL) {
+    const int lane = threadIdx.x & 31;
+    const int32_t bl = (n_base + lane < N) ? load_as_int(e.bias, GEMM_S32, n_base + lane) : 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n_base + j < N) x[j] = wrap_madd(1, load_as_int(e.bias, GEMM_S32, n_base + j), x[j]);
-  } else if (e.bias_mode == GEMM_BIAS_ROW) {
+    for (int j = 0; j < 32; ++j) x[j] = wrap_madd(1, __shfl_sync(0xffffffffu, bl, j), x[j]);
+  } else if (e.bias_mode == GEMM_BIAS_ROW && row_ok) {
     const int32_t b = load_as_int(e.bias, GEMM_S32, m);
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = wrap_madd(1, b, x[j]);
   }
+  if (!row_ok) return;
   if (e.relu) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = x[j] > 0 ? x[j] : 0;

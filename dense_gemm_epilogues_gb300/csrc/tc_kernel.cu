@@ -248,10 +248,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           ++acc_it;
         }
         if (!ok) break;
-        if (row_ok) {
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) epi_finish_row32_int(p.epi, m, n0 + c * 32, p.N, &acc[c * 32]);
-        }
+        for (int c = 0; c < BN / 32; ++c) epi_finish_row32_int(p.epi, m, row_ok, n0 + c * 32, p.N, &acc[c * 32]);
       } else {
         const int buf = (int)(acc_it % Cfg::ACC_BUFS);
         const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
@@ -263,12 +261,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           uint32_t r[32];
           tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
           tmem_wait_ld();
-          if (row_ok) {
-            float x[32];
+          float x[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
-            epi_finish_row32_float(p.epi, m, p.M, n0 + c * 32, p.N, x);
-          }
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
+          epi_finish_row32_float(p.epi, m, row_ok, n0 + c * 32, p.N, x);
         }
         tc_fence_before();
         __syncwarp();
