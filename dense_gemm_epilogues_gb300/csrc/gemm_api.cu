@@ -199,7 +199,13 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.tiles = (int32_t)std::min<int64_t>(tiles_m * tiles_n, kMaxDim);
       cfg.raster = (int32_t)std::min<int64_t>(16, tiles_m);
       cfg.grid = (int32_t)std::min<int64_t>(cfg.tiles, sm_count);
-      cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? 512 : 0;
+      // Exact int8 chunk: |sum of 1024 products| <= 1024 * 2^14 = 2^24, and every
+      // integer of that size is exact in fp32.  (GEMM_INT8_CHUNK=512 halves it.)
+      int chunk = 1024;
+      if (const char* env = std::getenv("GEMM_INT8_CHUNK")) {
+        if (std::atoi(env) == 512) chunk = 512;
+      }
+      cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? chunk : 0;
       bool pair_int = k == GEMM_KERNEL_TC_INT8 && pair_clusters > 0 && M > 128 && N > 128;
       if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) pair_int = pair_int && std::atoi(env) != 1;
       if (pair_int) {   // exact integer mode on CTA pairs: 256 x 256 tiles

@@ -18,7 +18,7 @@
 //     bias, ReLU, cast, 16-byte stores) and release the accumulator on the
 //     leader's barrier (the peer's four warps arrive remotely).
 // Exact integer mode (int8 operands staged as fp16): the MMA accumulates each
-// 512-deep K chunk into a fresh fp32 accumulator (exact, |sum| <= 2^23); eight
+// 1024-deep K chunk into a fresh fp32 accumulator (exact, |sum| <= 2^24); eight
 // epilogue warps per CTA -- two per tensor-memory lane quarter, one per half of
 // the 256 columns -- convert each finished chunk to int32 and add it into 128
 // registers per thread, then apply the integer epilogue after the last chunk.

@@ -23,7 +23,7 @@
 //     next tile into the other accumulator buffer.
 // Exact integer mode (int8 inputs): every product of two int8 values is exact
 // in fp32 and so is any sum of up to 1024 of them (|sum| <= 2^24), so the MMA
-// accumulates K in chunks of chunk_kb*64 <= 512 into a fresh fp32 accumulator;
+// accumulates K in chunks of chunk_kb*64 <= 1024 into a fresh fp32 accumulator;
 // the epilogue warps convert each finished chunk to int32 and add it into
 // registers, giving the exact int32 result for any K.
 //

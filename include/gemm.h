@@ -92,7 +92,7 @@ typedef enum {
     GEMM_KERNEL_AUTO = 0,   /* let the selector decide (default) */
     GEMM_KERNEL_NONE = 1,   /* nothing to launch (M == 0 or N == 0) */
     GEMM_KERNEL_TC = 2,     /* tcgen05 + TMA persistent warp-specialised kernel, fp16/bf16 */
-    GEMM_KERNEL_TC_INT8 = 3,/* int8 exact: int8->fp16 staging, tcgen05 in K-chunks, int32 accumulation */
+    GEMM_KERNEL_TC_INT8 = 3,/* int8 exact: int8->fp16 staging, tcgen05 in 1024-deep K-chunks, int32 accumulation */
     GEMM_KERNEL_FFMA = 4,   /* fp32 SGEMM on CUDA cores, register-blocked FFMA */
     GEMM_KERNEL_SIMT = 5,   /* generic CUDA-core kernel: any alignment, K == 0, every dtype */
     GEMM_KERNEL_TC_PAIR = 6 /* tcgen05 on CTA pairs (cta_group::2), 256x256 tiles, fp16/bf16 */

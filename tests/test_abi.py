@@ -128,7 +128,7 @@ def test_selector_misaligned_operands_use_generic_kernel():
 
 def test_selector_int8_and_fp32_paths():
     cfg = _sel(ab=G.GEMM_S8, c=G.GEMM_S32)
-    assert cfg["kernel"] == G.GEMM_KERNEL_TC_INT8 and cfg["cta_group"] == 2 and cfg["k_chunk"] == 512
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC_INT8 and cfg["cta_group"] == 2 and cfg["k_chunk"] == 1024
     cfg = _sel(ab=G.GEMM_S8, c=G.GEMM_S32, N=128)
     assert cfg["kernel"] == G.GEMM_KERNEL_TC_INT8 and cfg["bn"] == 128 and cfg["cta_group"] == 1
     assert _sel(ab=G.GEMM_S8, c=G.GEMM_S32, M=64, N=64, K=60)["kernel"] == G.GEMM_KERNEL_SIMT

@@ -147,7 +147,7 @@ def cta_group(request, monkeypatch):
 
 @pytest.mark.parametrize("layout", LAYOUTS)
 def test_int8_exact_ragged(layout, cta_group):
-    """K = 1100 spans two exact 512-chunks and a tail; bit-exact int32."""
+    """K = 1100 spans a full exact 1024-chunk and a tail; bit-exact int32."""
     p = H.tma_aligned(I.Problem("i8", "s8", layout[0], layout[1], 260, 390, 1100, d="s32",
                                 dist_a=I.I8, dist_b=I.I8))
     cfg = H.run_and_check_full(p, 109, expect_kernel=G.GEMM_KERNEL_TC_INT8)
@@ -156,7 +156,8 @@ def test_int8_exact_ragged(layout, cta_group):
 
 def test_int8_adversarial_extremes_exact(cta_group):
     """All -128: every partial sum is 16384*k, far beyond fp32's exact range at
-    K = 4096 (2^26), so a single fp32 accumulator would be wrong."""
+    K = 4096 (2^26), so a single fp32 accumulator would be wrong; each 1024-deep
+    chunk reaches exactly 2^24, the largest sum the chunking allows."""
     p = I.Problem("i8max", "s8", "T", "N", 130, 140, 4096, d="s32",
                   dist_a=I.Dist("int", -128, -128), dist_b=I.Dist("int", -128, -128))
     cfg = H.run_and_check_full(p, 110, expect_kernel=G.GEMM_KERNEL_TC_INT8)
