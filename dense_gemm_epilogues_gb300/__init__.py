@@ -50,10 +50,10 @@ class gemm_epilogue_t(ctypes.Structure):
 class gemm_config_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kernel", "bm", "bn", "bk", "stages", "cta_group", "split_k", "raster", "grid",
-                 "k_chunk", "tiles", "reserved")]
+                 "k_chunk", "tiles", "sk_tiles")]
 
     def as_dict(self) -> dict:
-        d = {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+        d = {n: getattr(self, n) for n, _ in self._fields_}
         d["kernel_name"] = KERNEL_NAMES.get(self.kernel, "?")
         return d
 

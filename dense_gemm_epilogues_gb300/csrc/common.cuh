@@ -434,6 +434,57 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// --------------------------- stream-K work division ---------------------------
+// Tiles [0, t_dp) run whole: tile t on cluster t mod G.  The K blocks of tiles
+// [t_dp, T) form one linear sequence (tile-major) of W = (T - t_dp) * KB blocks;
+// cluster c takes the contiguous range [c*W/G, (c+1)*W/G).  A segment is one
+// tile's share of a range: K blocks [kb0, kb1).
+struct SegmentIter {
+  int G, T, t_dp, KB;
+  int t;                 // next whole tile of this cluster
+  int64_t L, L1;         // remaining linear range of this cluster
+  __device__ __forceinline__ SegmentIter(int cid, int G_, int T_, int t_dp_, int KB_)
+      : G(G_), T(T_), t_dp(t_dp_), KB(KB_), t(cid) {
+    const int64_t W = (int64_t)(T - t_dp) * KB;
+    L = (int64_t)cid * W / G;
+    L1 = (int64_t)(cid + 1) * W / G;
+  }
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
+    if (t < t_dp) {
+      tile = t;
+      kb0 = 0;
+      kb1 = KB;
+      t += G;
+      return true;
+    }
+    if (L < L1) {
+      const int64_t tl = L / KB;
+      kb0 = (int)(L - tl * KB);
+      const int64_t rest = L1 - L;
+      kb1 = (int)(rest < (int64_t)(KB - kb0) ? kb0 + rest : KB);
+      tile = t_dp + (int)tl;
+      L += kb1 - kb0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Cluster whose stream-K range holds linear K-block index L (W blocks over G clusters).
+__device__ __forceinline__ int sk_cluster_of(int64_t L, int64_t W, int G) {
+  return (int)(((L + 1) * (int64_t)G + W - 1) / W) - 1;
+}
+
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format) for a 128-byte-swizzled
 // operand tile whose swizzle atoms (8 rows of 128 bytes) start on 1024-byte
 // boundaries:

@@ -28,6 +28,9 @@ struct gemm_plan {
   size_t stage_bytes = 0;
   gemm_kernel_t forced = GEMM_KERNEL_AUTO;
   int pair_clusters = 0;             // co-resident CTA-pair clusters (0: pair kernel unavailable)
+  void* sk_ws = nullptr;             // stream-K partial accumulators and flags (per cluster and CTA)
+  size_t sk_ws_bytes = 0;
+  int32_t sk_epoch = 0;
   gemm_config_t last{};
   uint64_t timeout_ns = 4000000000ull;
 };
@@ -170,6 +173,26 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       if (const char* env = std::getenv("GEMM_TC_RASTER")) raster = std::max(1, std::atoi(env));
       cfg.raster = (int32_t)std::min<int64_t>(raster, tiles_m);
       cfg.grid = 2 * (int32_t)std::min<int64_t>(cfg.tiles, pair_clusters);
+      // Stream-K tail (opt-in, GEMM_STREAM_K=1): when the tiles leave the last
+      // wave of CTA pairs partly idle, the K blocks of the last (G + T mod G)
+      // tiles -- or of all tiles when there are fewer than G -- are shared out
+      // evenly over all G pairs.  Off by default: on GB300 the fixup of split
+      // tiles cost more than the idle tail it recovers in every measured shape
+      // (the chip runs power-capped under load, so idle SMs in a tail wave let
+      // the busy ones clock higher).
+      const int64_t T = cfg.tiles, G = pair_clusters, KB = (K + TC_BK - 1) / TC_BK;
+      const int64_t q = T / G, r = T % G;
+      bool sk = r != 0 && (double)r / (double)G < 0.9;
+      int64_t sk_tiles = q >= 1 ? G + r : T;
+      if (sk_tiles * KB < 8 * G) sk = false;          // too little K work per pair
+      const char* sk_env = std::getenv("GEMM_STREAM_K");
+      sk = sk && sk_env != nullptr && std::atoi(sk_env) != 0;
+      if (sk) {
+        cfg.sk_tiles = (int32_t)sk_tiles;
+        cfg.grid = 2 * (int32_t)G;
+        const int64_t per = std::max<int64_t>(1, sk_tiles * KB / G);
+        cfg.split_k = (int32_t)std::min<int64_t>((KB + per - 1) / per + 1, KB);
+      }
       break;
     }
     case GEMM_KERNEL_TC:
@@ -375,6 +398,7 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
+  tp.sk_first_tile = tp.num_tiles;
   return launch_tc(tp, bn, cfg.grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -411,6 +435,26 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
+  tp.sk_first_tile = tp.num_tiles;
+  if (cfg.sk_tiles > 0 && chunk_kb == 0) {
+    const int clusters = cfg.grid / 2;
+    const size_t part_bytes = (size_t)clusters * 2 * TC_BM * 256 * sizeof(float);
+    const size_t need = part_bytes + (size_t)clusters * 2 * sizeof(int32_t);
+    if (plan->sk_ws_bytes < need) {
+      if (plan->sk_ws) cudaFreeAsync(plan->sk_ws, stream);
+      plan->sk_ws = nullptr;
+      plan->sk_ws_bytes = 0;
+      if (cudaMallocAsync(&plan->sk_ws, need, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+      if (cudaMemsetAsync(plan->sk_ws, 0, need, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+      plan->sk_ws_bytes = need;
+      plan->sk_epoch = 0;
+    }
+    tp.sk_first_tile = tp.num_tiles - cfg.sk_tiles;
+    tp.sk_partials = static_cast<float*>(plan->sk_ws);
+    tp.sk_flags = reinterpret_cast<int32_t*>(static_cast<char*>(plan->sk_ws) + part_bytes);
+    if (++plan->sk_epoch <= 0) plan->sk_epoch = 1;
+    tp.sk_epoch = plan->sk_epoch;
+  }
   return launch_tc_pair(tp, cfg.grid / 2, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -485,6 +529,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
   cudaDeviceSynchronize();
   if (plan->ws) cudaFree(plan->ws);
   if (plan->stage) cudaFree(plan->stage);
+  if (plan->sk_ws) cudaFree(plan->sk_ws);
   if (plan->d_err) cudaFree(plan->d_err);
   delete plan;
   return GEMM_OK;

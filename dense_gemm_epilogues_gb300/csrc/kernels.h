@@ -24,6 +24,14 @@ struct TcParams {
   EpiParams epi;
   int32_t* err;
   uint64_t timeout_ns;
+  // Stream-K tail (CTA-pair kernel, floating mode): tiles below sk_first_tile
+  // run whole, one per cluster in turn; the K blocks of the remaining tiles are
+  // split into equal contiguous ranges, one per cluster.  sk_first_tile ==
+  // num_tiles turns it off.
+  int32_t sk_first_tile;
+  int32_t sk_epoch;       // value published in sk_flags by this launch
+  float* sk_partials;     // per cluster and CTA: one 128 x 256 fp32 partial accumulator
+  int32_t* sk_flags;      // per cluster and CTA: epoch of its last published partial
 };
 
 constexpr int TC_BM = 128;

@@ -35,7 +35,7 @@ constexpr int PAIR_B_BYTES = (PAIR_BN / 2) * TC_BK * 2;  // 16 KiB: this CTA's h
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns of TMEM
 constexpr int PAIR_STAGES = 6;
-constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 1;
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
 constexpr size_t PAIR_SMEM = 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
 
 // Producer warp, MMA warp, then 4 epilogue warps (floating) or 8 (exact integer).
@@ -90,6 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
   auto tfull_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + PAIR_ACC_BUFS + b); };
   const uint32_t teardown_bar = bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
+  const uint32_t sk_bar = teardown_bar + 8u;   // epilogue warps: stream-K partial written
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -108,6 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       mbar_init(tempty_bar(b), 2 * EPI_WARPS);  // leader: every epilogue warp of both CTAs
     }
     mbar_init(teardown_bar, 1);
+    mbar_init(sk_bar, EPI_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -119,7 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
-  const int units_per_tile = INT_MODE ? (p.num_kb + p.chunk_kb - 1) / p.chunk_kb : 1;
+  // Integer mode runs whole tiles (the host turns the stream-K tail off for it).
   const int kb_per_unit = INT_MODE ? p.chunk_kb : p.num_kb;
 
   if (warp == 0) {
@@ -130,12 +132,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+      SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
         int tm, tn;
-        pair_tile_coords(t, p, tm, tn);
+        pair_tile_coords(tile, p, tm, tn);
         const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
         const int n0 = tn * PAIR_BN + (int)rank * (PAIR_BN / 2);    // this CTA's half of B
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
           if (leader) mbar_expect_tx(fb_local, 2u * PAIR_STAGE_BYTES);
@@ -181,15 +185,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       int stage = 0;
       uint32_t phase = 0, acc_it = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-        for (int u = 0; ok && u < units_per_tile; ++u) {
+      SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
+      int tile, kb0, kb1;
+      while (ok && it.next(tile, kb0, kb1)) {
+        const int units = INT_MODE ? (kb1 - kb0 + kb_per_unit - 1) / kb_per_unit : 1;
+        for (int u = 0; ok && u < units; ++u) {
           const int buf = (int)(acc_it % PAIR_ACC_BUFS);
           const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
           if (!mbar_wait(tempty_bar(buf), apar ^ 1u, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PAIR_BN);
-          const int kb_begin = u * kb_per_unit;
-          const int kb_end = min(p.num_kb, kb_begin + kb_per_unit);
+          const int kb_begin = INT_MODE ? kb0 + u * kb_per_unit : kb0;
+          const int kb_end = INT_MODE ? min(kb1, kb_begin + kb_per_unit) : kb1;
           for (int kb = kb_begin; kb < kb_end; ++kb) {
             if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
             tc_fence_after();
@@ -220,18 +227,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t acc_it = 0;
     bool ok = true;
-    for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+    SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
+    int tile, kb0, kb1;
+    while (ok && it.next(tile, kb0, kb1)) {
       int tm, tn;
-      pair_tile_coords(t, p, tm, tn);
-      const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + q * 32 + lane;
+      pair_tile_coords(tile, p, tm, tn);
+      const int row_in_cta = q * 32 + lane;
+      const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + row_in_cta;
       const int64_t n0 = (int64_t)tn * PAIR_BN;
       const bool row_ok = m < p.M;
       if constexpr (INT_MODE) {
         const int half = (warp - 2) >> 2;                     // columns 128*half ... 128*half + 127
+        const int units = (kb1 - kb0 + kb_per_unit - 1) / kb_per_unit;
         int32_t acc[128];
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0;
-        for (int u = 0; u < units_per_tile; ++u) {
+        for (int u = 0; u < units; ++u) {
           const int buf = (int)(acc_it % PAIR_ACC_BUFS);
           const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
           if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
@@ -263,21 +274,98 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
         if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN);
+        // Stream-K slots hold raw accumulators (before alpha), 128 x 256 fp32 per CTA,
+        // laid out so that each 16-byte column group of a warp's 32 rows is contiguous.
+        constexpr int SLOT_FLOATS = TC_BM * PAIR_BN;
+        if (kb0 > 0) {
+          // A later part of a tile whose first part another cluster owns: publish it.
+          float* slot = p.sk_partials + (size_t)(cluster_id * 2 + (int)rank) * SLOT_FLOATS;
 #pragma unroll 1
-        for (int c = 0; c < PAIR_BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
-          tmem_wait_ld();
-          float x[32];
+          for (int c = 0; c < PAIR_BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
-          epi_finish_row32_float(p.epi, m, row_ok, n0 + c * 32, p.N, x);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (leader) mbar_arrive(tempty_bar(buf));
-          else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<float4*>(slot)[(c * 8 + v) * TC_BM + row_in_cta] =
+                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(tempty_bar(buf));
+            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+            __threadfence();
+            mbar_arrive(sk_bar);
+          }
+          if (warp == 2 && lane == 0) {
+            // Every epilogue warp of this CTA has written its rows: release the partial.
+            if (mbar_wait(sk_bar, 0, wc)) {
+              __threadfence();
+              st_release_gpu(&p.sk_flags[cluster_id * 2 + (int)rank], p.sk_epoch);
+            }
+          }
+        } else {
+          // A whole tile, or the first part of a tile (then add the later parts).
+          int cp_first = 0, cp_last = -1;
+          if (kb1 < p.num_kb) {
+            const int64_t W = (int64_t)(p.num_tiles - p.sk_first_tile) * p.num_kb;
+            const int64_t tl = tile - p.sk_first_tile;
+            cp_first = cluster_id + 1;
+            cp_last = sk_cluster_of(tl * p.num_kb + p.num_kb - 1, W, num_clusters);
+            int good = 1;
+            if (lane == 0) {
+              for (int cp = cp_first; cp <= cp_last && good; ++cp) {
+                const int32_t* f = &p.sk_flags[cp * 2 + (int)rank];
+                if (ld_acquire_gpu(f) == p.sk_epoch) continue;
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire_gpu(f) != p.sk_epoch) {
+                  if (*wc.abort) { good = 0; break; }
+                  if (globaltimer_ns() - t0 > wc.timeout_ns) {
+                    atomicCAS(wc.err, 0, (int32_t)GEMM_ERR_TIMEOUT);
+                    *wc.abort = 1;
+                    good = 0;
+                    break;
+                  }
+                  __nanosleep(256);
+                }
+              }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            __syncwarp();
+            if (!good) cp_last = cp_first - 1;   // results are void; the error word says why
+          }
+#pragma unroll 1
+          for (int c = 0; c < PAIR_BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+            for (int cp = cp_first; cp <= cp_last; ++cp) {
+              const float4* slot = reinterpret_cast<const float4*>(
+                  p.sk_partials + (size_t)(cp * 2 + (int)rank) * SLOT_FLOATS);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const float4 y = __ldcg(&slot[(c * 8 + v) * TC_BM + row_in_cta]);
+                x[4 * v] += y.x;
+                x[4 * v + 1] += y.y;
+                x[4 * v + 2] += y.z;
+                x[4 * v + 3] += y.w;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= p.epi.alpha;
+            epi_finish_row32_float(p.epi, m, row_ok, n0 + c * 32, p.N, x);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(tempty_bar(buf));
+            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+          }
         }
         ++acc_it;
       }

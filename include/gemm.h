@@ -104,12 +104,13 @@ typedef struct {
     int32_t bm, bn, bk;   /* CTA tile (rows of D, columns of D, K per pipeline stage) */
     int32_t stages;       /* shared-memory pipeline depth */
     int32_t cta_group;    /* CTAs cooperating on one MMA tile (1 or 2) */
-    int32_t split_k;      /* K splits (1 = none) */
+    int32_t split_k;      /* most K segments any tile is split into (1 = no split) */
     int32_t raster;       /* tile rows per raster group (L2 reuse) */
     int32_t grid;         /* CTAs launched */
     int32_t k_chunk;      /* int8 path: K elements per exact fp32 chunk; 0 otherwise */
     int32_t tiles;        /* output tiles */
-    int32_t reserved;
+    int32_t sk_tiles;     /* tiles in the stream-K tail (their K blocks are shared out over
+                             all CTA pairs; 0 = every tile runs whole on one CTA pair) */
 } gemm_config_t;
 
 /* ---------------------------------------------------------------------------
@@ -153,6 +154,13 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
  * else uses the generic CUDA-core kernel.  All paths run on the GPU.
  * Errors: GEMM_ERR_INVALID_ARG / GEMM_ERR_UNSUPPORTED before any launch;
  * GEMM_ERR_CUDA when a launch or scratch allocation fails.
+ * A plan's device scratch (int8 staging, stream-K partials, host staging) is
+ * reused by every call: calls that use one plan from several streams or host
+ * threads at once race on it; use one plan per concurrent stream.
+ * Stream-K (environment GEMM_STREAM_K=1, off by default) lets CTA pairs of one
+ * launch wait for each other's partial results; it assumes the launch's CTA
+ * pairs are all resident, so kernels running concurrently on other streams can
+ * delay it (every such wait is bounded and reports GEMM_ERR_TIMEOUT).
  * ------------------------------------------------------------------------- */
 gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t layoutA, gemm_layout_t layoutB,
                        int64_t M, int64_t N, int64_t K, double alpha,

@@ -276,3 +276,44 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     assert plan.device_status() == 0
     H.check_close(dp.result(), H.oracle_full(inp), "f32", "after timeout")
+
+
+# ------------------------------ stream-K tail --------------------------------
+
+SK_SHAPES = [(1536, 1536, 2048), (2560, 2560, 512), (1000, 1800, 2000), (2304, 4352, 640)]
+
+
+@pytest.mark.parametrize("stream_k", ["on", "off"])
+@pytest.mark.parametrize("shape", SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_pair_stream_k_tail(shape, stream_k, monkeypatch):
+    """Tiles of the last wave split over all CTA pairs by K blocks (up to four
+    segments per tile here); the owning pair adds the published partials before
+    the full epilogue (alpha, beta*C, bias, ReLU, bf16 cast)."""
+    monkeypatch.setenv("GEMM_STREAM_K", "1" if stream_k == "on" else "0")
+    M, N, K = shape
+    p = H.tma_aligned(I.Problem("sk", "bf16", "T", "N", M, N, K, alpha=0.75, beta=-0.5, c="f32",
+                                d="bf16", bias="f32", bias_mode="col", act="relu"))
+    cfg = H.run_and_check_full(p, 130, expect_kernel=G.GEMM_KERNEL_TC_PAIR)
+    assert (cfg["sk_tiles"] > 0) == (stream_k == "on"), cfg
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_pair_stream_k_repeated_launches(layout, monkeypatch):
+    """Several launches on one plan reuse the partial slots and flags (each
+    launch publishes a new epoch); every result must still be right."""
+    monkeypatch.setenv("GEMM_STREAM_K", "1")
+    p = H.tma_aligned(I.Problem("sk_rep", "f16", layout[0], layout[1], 1280, 1536, 1536,
+                                alpha=1.25, beta=1.0, c="f32"))
+    inp = I.generate(p, 131)
+    ref = H.oracle_full(inp)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p)
+    for _ in range(3):
+        dp.D.fill_(0)
+        dp.run(plan)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        cfg = plan.last_config()
+        assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["sk_tiles"] > 0
+        H.check_close(dp.result(), ref, "f32", "stream-K repeat")
+    dp.check_guards()
