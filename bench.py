@@ -442,11 +442,14 @@ def run_suite(G, device, warmup=3, iters=20):
                               G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32, bm,
                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE)
 
-        def call():
+        def call_on(st):
             G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M,
                        p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
                        C.data_ptr() if C is not None else None, p.ldc if C is not None else 0,
-                       D.data_ptr(), p.ldd, epi, stream.cuda_stream)
+                       D.data_ptr(), p.ldd, epi, st.cuda_stream)
+
+        def call():
+            call_on(stream)
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
         for _ in range(warmup):
             call()
@@ -475,6 +478,31 @@ def run_suite(G, device, warmup=3, iters=20):
             times.append(c0.elapsed_time(c1) / 1e3)
         t_cold = statistics.median(times)
         t = t_b2b
+        # (3) GPU time alone: the same calls replayed from a CUDA graph on a side
+        # stream (no host work between launches).
+        t_graph = None
+        try:
+            side = torch.cuda.Stream(device)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                gr.capture_begin()
+                for _ in range(iters):
+                    call_on(side)
+                gr.capture_end()
+            side.synchronize()
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(side):    # replay() launches on the current stream
+                gr.replay()
+                side.synchronize()
+                g0.record(side)
+                gr.replay()
+                g1.record(side)
+            side.synchronize()
+            t_graph = g0.elapsed_time(g1) / 1e3 / iters
+            del gr
+        except RuntimeError:
+            t_graph = None
         status = plan.device_status()
         cfg = plan.last_config()
         eb = I.ELEM_BYTES
@@ -484,6 +512,8 @@ def run_suite(G, device, warmup=3, iters=20):
         rec = {"suite": p.name, "M": p.M, "N": p.N, "K": p.K, "kernel": cfg["kernel_name"],
                "tile": f"{cfg['bm']}x{cfg['bn']}x{cfg['bk']}", "grid": cfg["grid"],
                "median_us": round(t * 1e6, 2), "cold_us": round(t_cold * 1e6, 2),
+               "graph_us": round(t_graph * 1e6, 2) if t_graph else None,
+               "tflops_graph": round(p.flops / t_graph / 1e12, 2) if t_graph else None,
                "inputs_fit_l2": algo_bytes < 126e6, "tflops": round(tflops, 2),
                "gbs": round(algo_bytes / t / 1e9, 1), "algo_bytes": algo_bytes,
                "frac_tensor_peak": round(tflops / peaks["bf16_tflops"], 4),

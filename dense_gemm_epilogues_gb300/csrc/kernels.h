@@ -56,7 +56,10 @@ struct FfmaParams {
   int32_t M, N, K;
   EpiParams epi;
 };
-constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = 8;
+#ifndef GEMM_FFMA_BK
+#define GEMM_FFMA_BK 16
+#endif
+constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = GEMM_FFMA_BK;
 cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, cudaStream_t stream);
 
 // Generic CUDA-core kernel: any dtype, layout, alignment; K may be 0.

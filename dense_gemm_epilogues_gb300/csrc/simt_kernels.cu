@@ -24,58 +24,69 @@ constexpr int SG_PAD = 4;                       // row padding: conflict-free tr
 constexpr int SG_LDS = FFMA_BM + SG_PAD;        // 132 floats per K row (BM == BN)
 
 // Loads one BK x 128 slice of op(A) (as A^T: [k][m]) or of op(B) ([k][n]) into
-// four registers per thread.  `kmajor`: the operand is K-contiguous in global
-// memory (A row-major / B column-major), so a thread loads 4 consecutive K
-// values of one row/column; otherwise 4 consecutive M/N values of one K row.
+// registers: NV = BK/8 groups of four values per thread.  `KMAJOR`: the operand
+// is K-contiguous in global memory (A row-major / B column-major), so a thread
+// loads 4 consecutive K values of one row/column per group; otherwise 4
+// consecutive M/N values of one K row.
+constexpr int SG_NV = FFMA_BK / 8;
+
 template <bool KMAJOR>
 struct SliceLoader {
   const float* ptr;
   int64_t ld;
   int64_t extent_mn;   // M (for A) or N (for B)
   int64_t K;
-  static constexpr bool kmajor = KMAJOR;
 
-  __device__ __forceinline__ void load(int64_t mn0, int64_t k0, int tid, float (&v)[4]) const {
-    if constexpr (KMAJOR) {
-      const int64_t r = mn0 + (tid >> 1);
-      const int64_t k = k0 + (tid & 1) * 4;
-      const float* src = ptr + r * ld + k;
-      if (r < extent_mn && k + 4 <= K) {
-        const float4 f = *reinterpret_cast<const float4*>(src);
-        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-      } else {
+  __device__ __forceinline__ void load(int64_t mn0, int64_t k0, int tid, float (&v)[SG_NV][4]) const {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = (r < extent_mn && k + j < K) ? src[j] : 0.0f;
-      }
-    } else {
-      const int64_t k = k0 + (tid >> 5);
-      const int64_t c = mn0 + (tid & 31) * 4;
-      const float* src = ptr + k * ld + c;
-      if (k < K && c + 4 <= extent_mn) {
-        const float4 f = *reinterpret_cast<const float4*>(src);
-        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-      } else {
+    for (int g = 0; g < SG_NV; ++g) {
+      if constexpr (KMAJOR) {
+        const int64_t r = mn0 + (tid >> 1);
+        const int64_t k = k0 + (tid & 1) * 4 + g * 8;
+        const float* src = ptr + r * ld + k;
+        if (r < extent_mn && k + 4 <= K) {
+          const float4 f = *reinterpret_cast<const float4*>(src);
+          v[g][0] = f.x; v[g][1] = f.y; v[g][2] = f.z; v[g][3] = f.w;
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = (k < K && c + j < extent_mn) ? src[j] : 0.0f;
+          for (int j = 0; j < 4; ++j) v[g][j] = (r < extent_mn && k + j < K) ? src[j] : 0.0f;
+        }
+      } else {
+        const int64_t k = k0 + (tid >> 5) + g * 8;
+        const int64_t c = mn0 + (tid & 31) * 4;
+        const float* src = ptr + k * ld + c;
+        if (k < K && c + 4 <= extent_mn) {
+          const float4 f = *reinterpret_cast<const float4*>(src);
+          v[g][0] = f.x; v[g][1] = f.y; v[g][2] = f.z; v[g][3] = f.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[g][j] = (k < K && c + j < extent_mn) ? src[j] : 0.0f;
+        }
       }
     }
   }
 
-  // Store the four values into the [BK][SG_LDS] shared buffer.
-  __device__ __forceinline__ void store(float* s, int tid, const float (&v)[4]) const {
-    if constexpr (KMAJOR) {
-      const int r = tid >> 1, k = (tid & 1) * 4;
+  // Store the values into the [BK][SG_LDS] shared buffer.
+  __device__ __forceinline__ void store(float* s, int tid, const float (&v)[SG_NV][4]) const {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s[(k + j) * SG_LDS + r] = v[j];
-    } else {
-      const int k = tid >> 5, c = (tid & 31) * 4;
-      *reinterpret_cast<float4*>(&s[k * SG_LDS + c]) = make_float4(v[0], v[1], v[2], v[3]);
+    for (int g = 0; g < SG_NV; ++g) {
+      if constexpr (KMAJOR) {
+        const int r = tid >> 1, k = (tid & 1) * 4 + g * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[(k + j) * SG_LDS + r] = v[g][j];
+      } else {
+        const int k = (tid >> 5) + g * 8, c = (tid & 31) * 4;
+        *reinterpret_cast<float4*>(&s[k * SG_LDS + c]) = make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
+      }
     }
   }
 };
 
+#ifndef GEMM_FFMA_MINB
+#define GEMM_FFMA_MINB 2
+#endif
 template <bool A_KMAJOR, bool B_KMAJOR>
-__global__ void __launch_bounds__(SG_THREADS, 2) ffma_sgemm_kernel(const FfmaParams p) {
+__global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(const FfmaParams p) {
   __shared__ __align__(16) float As[2][FFMA_BK * SG_LDS];
   __shared__ __align__(16) float Bs[2][FFMA_BK * SG_LDS];
 
@@ -95,7 +106,7 @@ __global__ void __launch_bounds__(SG_THREADS, 2) ffma_sgemm_kernel(const FfmaPar
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
   const int nkt = (p.K + FFMA_BK - 1) / FFMA_BK;
-  float ra[4], rb[4];
+  float ra[SG_NV][4], rb[SG_NV][4];
   if (nkt > 0) {
     la.load(m0, 0, tid, ra);
     lb.load(n0, 0, tid, rb);

@@ -62,6 +62,7 @@ class Problem:
     bias: Optional[str] = None   # dtype of the bias vector
     bias_mode: str = "none"      # 'none' | 'col' | 'row'
     act: str = "none"            # 'none' | 'relu'
+    c_act: str = "none"          # transform of C as it is read: 'none' | 'relu'
     dist_a: Dist = U11
     dist_b: Dist = U11
     dist_c: Dist = Dist("normal", std=1.0)

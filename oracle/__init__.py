@@ -65,10 +65,10 @@ def _load_from(path: str):
     i64, dbl, vp, ci = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
     lib.oracle_gemm.restype = i64
     lib.oracle_gemm.argtypes = [ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
-                                dbl, ci, vp, i64, ci, vp, ci, ci, ci, vp, i64, ci, ci]
+                                dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, vp, i64, ci, ci]
     lib.oracle_gemm_entries.restype = i64
     lib.oracle_gemm_entries.argtypes = [ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
-                                        dbl, ci, vp, i64, ci, vp, ci, ci, ci, i64, vp, vp,
+                                        dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, i64, vp, vp,
                                         vp, ci]
     lib.oracle_f16_to_double.restype = dbl
     lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
@@ -106,7 +106,7 @@ def max_threads() -> int:
 def gemm(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
          beta=0.0, c_dtype=F32, C=None, ldc=0, bias_dtype=F32, bias=None,
          bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, ldd=None,
-         loop_order=0, nthreads=None):
+         loop_order=0, nthreads=None, c_act=ACT_NONE):
     """Full D (row-major M x ldd, raw bits for 16-bit outputs) and the int32
     overflow count.  Buffers are raw storage: numpy arrays or CPU tensors."""
     if ldd is None:
@@ -116,7 +116,7 @@ def gemm(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
     D = np.zeros((M, ldd), dtype=_OUT_NP[d_dtype])
     n = _load().oracle_gemm(ab_dtype, layout_a, layout_b, M, N, K, float(alpha),
                             _ptr(A), lda, _ptr(B), ldb, float(beta), c_dtype, _ptr(C), ldc,
-                            bias_dtype, _ptr(bias), bias_mode, act, d_dtype,
+                            bias_dtype, _ptr(bias), bias_mode, act, c_act, d_dtype,
                             D.ctypes.data, ldd, loop_order, nthreads)
     if n < 0:
         raise ValueError("oracle_gemm: invalid arguments")
@@ -125,7 +125,8 @@ def gemm(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
 
 def gemm_entries(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
                  rows, cols, beta=0.0, c_dtype=F32, C=None, ldc=0, bias_dtype=F32,
-                 bias=None, bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, nthreads=None):
+                 bias=None, bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, nthreads=None,
+                 c_act=ACT_NONE):
     """D at the listed (rows[e], cols[e]) entries, in d_dtype (raw bits for 16-bit)."""
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     cols = np.ascontiguousarray(cols, dtype=np.int64)
@@ -134,7 +135,7 @@ def gemm_entries(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
     out = np.zeros(rows.shape[0], dtype=_OUT_NP[d_dtype])
     n = _load().oracle_gemm_entries(ab_dtype, layout_a, layout_b, M, N, K, float(alpha),
                                     _ptr(A), lda, _ptr(B), ldb, float(beta), c_dtype, _ptr(C),
-                                    ldc, bias_dtype, _ptr(bias), bias_mode, act, d_dtype,
+                                    ldc, bias_dtype, _ptr(bias), bias_mode, act, c_act, d_dtype,
                                     rows.shape[0], rows.ctypes.data, cols.ctypes.data,
                                     out.ctypes.data, nthreads)
     if n < 0:

@@ -33,6 +33,10 @@
  *     row"); BIAS_ROW (length M, indexed by i) is the transposed counterpart.
  *   - Order: alpha*acc + beta*C + bias, then the activation, then one rounding
  *     to the output type.  The ReLU threshold is 0.
+ *   - An optional elementwise transform of C as it is read (c_act = ReLU:
+ *     C[i,j] -> max(C[i,j], 0) before the beta product): the "ReLU on C" of
+ *     "Flexible Performant GEMM Kernels on GPUs", section 5.3, Table 2, an
+ *     instance of the transforms applied after every load of section 4.2.
  *   - Floating inputs are accumulated in fp64 (products of fp32/fp16/bf16
  *     values are exact in fp64); int8 inputs in int64 with integral alpha/beta.
  *   - beta == 0 means C is not read (it may be NULL), as in BLAS.
@@ -188,6 +192,7 @@ typedef struct {
     const void *A, *B, *C, *bias;
     int64_t lda, ldb, ldc, ldd;
     int c_dtype, bias_dtype, bias_mode, act, d_dtype;
+    int c_act;   /* transform applied to each C element as it is read */
 } problem_t;
 
 static int is_int_problem(const problem_t* p) { return p->ab_dtype == OR_S8; }
@@ -196,7 +201,11 @@ static int is_int_problem(const problem_t* p) { return p->ab_dtype == OR_S8; }
  * the activation.  Returns the value before the output cast. */
 static double epilogue_float(const problem_t* p, int64_t i, int64_t j, double acc) {
     double v = p->alpha * acc;
-    if (p->beta != 0.0) v += p->beta * load_float(p->c_dtype, p->C, i * p->ldc + j);
+    if (p->beta != 0.0) {
+        double c = load_float(p->c_dtype, p->C, i * p->ldc + j);
+        if (p->c_act == OR_ACT_RELU) c = (c > 0.0) ? c : 0.0;
+        v += p->beta * c;
+    }
     if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, j);
     else if (p->bias_mode == OR_BIAS_ROW) v += load_float(p->bias_dtype, p->bias, i);
     if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;
@@ -206,7 +215,11 @@ static double epilogue_float(const problem_t* p, int64_t i, int64_t j, double ac
 static int64_t epilogue_int(const problem_t* p, int64_t i, int64_t j, int64_t acc) {
     int64_t alpha = (int64_t)p->alpha, beta = (int64_t)p->beta;
     int64_t v = alpha * acc;
-    if (beta != 0) v += beta * load_int(p->c_dtype, p->C, i * p->ldc + j);
+    if (beta != 0) {
+        int64_t c = load_int(p->c_dtype, p->C, i * p->ldc + j);
+        if (p->c_act == OR_ACT_RELU) c = (c > 0) ? c : 0;
+        v += beta * c;
+    }
     if (p->bias_mode == OR_BIAS_COL) v += load_int(p->bias_dtype, p->bias, j);
     else if (p->bias_mode == OR_BIAS_ROW) v += load_int(p->bias_dtype, p->bias, i);
     if (p->act == OR_ACT_RELU) v = (v > 0) ? v : 0;
@@ -309,6 +322,7 @@ static int valid_problem(const problem_t* p) {
     if (p->ldd < p->N) return 0;
     if (p->beta != 0.0 && (p->C == NULL || p->ldc < p->N)) return 0;
     if (p->bias_mode != OR_BIAS_NONE && p->bias == NULL) return 0;
+    if (p->c_act != OR_ACT_NONE && p->c_act != OR_ACT_RELU) return 0;
     if (is_int_problem(p)) {
         if (p->d_dtype != OR_S32) return 0;
         if (p->alpha != floor(p->alpha) || p->beta != floor(p->beta)) return 0;
@@ -330,11 +344,11 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
                     int64_t M, int64_t N, int64_t K,
                     double alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
                     double beta, int c_dtype, const void* C, int64_t ldc,
-                    int bias_dtype, const void* bias, int bias_mode, int act,
+                    int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                     int d_dtype, void* D, int64_t ldd,
                     int loop_order, int nthreads) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype};
+                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
     if (!valid_problem(&p)) return -1;
     if (M == 0 || N == 0) return 0;
     init_tables();
@@ -385,11 +399,11 @@ int64_t oracle_gemm_entries(int ab_dtype, int layout_a, int layout_b,
                             int64_t M, int64_t N, int64_t K,
                             double alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
                             double beta, int c_dtype, const void* C, int64_t ldc,
-                            int bias_dtype, const void* bias, int bias_mode, int act,
+                            int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                             int d_dtype, int64_t n_entries, const int64_t* rows, const int64_t* cols,
                             void* out, int nthreads) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype};
+                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
     if (!valid_problem(&p)) return -1;
     for (int64_t e = 0; e < n_entries; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;

@@ -30,7 +30,7 @@ def _oracle_kwargs(p: I.Problem, inp: I.Inputs) -> dict:
     return dict(beta=p.beta, c_dtype=OR_DT[p.c] if p.c else O.F32, C=inp.C,
                 ldc=p.ldc if p.c else 0, bias_dtype=OR_DT[p.bias] if p.bias else O.F32,
                 bias=inp.bias, bias_mode=OR_BIAS[p.bias_mode], act=OR_ACT[p.act],
-                d_dtype=OR_DT[p.d])
+                d_dtype=OR_DT[p.d], c_act=OR_ACT[p.c_act])
 
 
 def oracle_full(inp: I.Inputs) -> np.ndarray:

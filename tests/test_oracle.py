@@ -31,7 +31,7 @@ def run_oracle(inp: I.Inputs, loop_order=0, nthreads=None):
                     c_dtype=DT[p.c] if p.c else O.F32, C=inp.C, ldc=p.ldc if p.c else 0,
                     bias_dtype=DT[p.bias] if p.bias else O.F32, bias=inp.bias,
                     bias_mode=BIAS[p.bias_mode], act=ACT[p.act], d_dtype=DT[p.d], ldd=p.ldd,
-                    loop_order=loop_order, nthreads=nthreads)
+                    loop_order=loop_order, nthreads=nthreads, c_act=ACT[p.c_act])
     return D[:, :p.N], ovf
 
 
@@ -79,7 +79,7 @@ def test_hand_worked_examples(case, layout):
                     ldb, beta=case["beta"], c_dtype=DT[case["c"]], C=C, ldc=N,
                     bias_dtype=DT[case.get("bias_dtype", "f32")], bias=bias,
                     bias_mode=BIAS[case["bias_mode"]], act=ACT[case["act"]],
-                    d_dtype=DT[case["d"]])
+                    d_dtype=DT[case["d"]], c_act=ACT[case.get("c_act", "none")])
     assert ovf == 0
     if "D_bits" in case:
         assert D.tolist() == case["D_bits"]
@@ -128,7 +128,10 @@ def _numpy_expected(inp: I.Inputs) -> np.ndarray:
         inp.logical["b"].to(torch.float64).numpy().astype(np.int64)
     v = int(p.alpha) * (a @ b)
     if p.beta != 0:
-        v = v + int(p.beta) * inp.logical["c"].to(torch.float64).numpy().astype(np.int64)
+        c = inp.logical["c"].to(torch.float64).numpy().astype(np.int64)
+        if p.c_act == "relu":
+            c = np.maximum(c, 0)
+        v = v + int(p.beta) * c
     if p.bias_mode == "col":
         v = v + inp.bias.to(torch.float64).numpy().astype(np.int64)[None, :]
     elif p.bias_mode == "row":
@@ -140,7 +143,8 @@ def _numpy_expected(inp: I.Inputs) -> np.ndarray:
 
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("ab", ["f16", "bf16", "f32", "s8"])
-@pytest.mark.parametrize("epi", ["plain", "alpha_beta", "bias_col_relu", "bias_row_relu"])
+@pytest.mark.parametrize("epi", ["plain", "alpha_beta", "bias_col_relu", "bias_row_relu",
+                                 "relu_on_c_and_d"])
 def test_small_integers_match_numpy_int_matmul(layout, ab, epi):
     """Small-integer data makes every step exact, so the oracle must equal
     numpy's int64 matmul of the logical matrices bit for bit.  Non-square
@@ -157,6 +161,9 @@ def test_small_integers_match_numpy_int_matmul(layout, ab, epi):
                   alpha=2.0, beta=1.0, c=cd, dist_c=I.Dist("small", -5, 5))
     elif epi == "bias_row_relu":
         kw.update(bias=cd, bias_mode="row", act="relu", dist_bias=I.Dist("small", -20, 20))
+    elif epi == "relu_on_c_and_d":
+        kw.update(bias=cd, bias_mode="col", act="relu", c_act="relu", alpha=1.0, beta=2.0, c=cd,
+                  dist_c=I.Dist("small", -30, 30), dist_bias=I.Dist("small", -20, 20))
     p = I.Problem("small", ab, layout[0], layout[1], M, N, K, d=cd, **kw)
     inp = I.generate(p, 3, keep_logical=True)
     D, ovf = run_oracle(inp)

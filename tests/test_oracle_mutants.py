@@ -17,7 +17,8 @@ import test_oracle as T
 SRC = os.path.join(os.path.dirname(O.__file__), "oracle.c")
 
 MUTANTS = {
-    "drop_beta_term": ("v += p->beta * load_float", "v += 0.0 * load_float"),
+    "drop_beta_term": ("v += p->beta * c;", "v += 0.0 * c;"),
+    "c_relu_dropped": ("if (p->c_act == OR_ACT_RELU) c = (c > 0.0) ? c : 0.0;", ""),
     "negated_alpha": ("double v = p->alpha * acc;", "double v = -p->alpha * acc;"),
     "transposed_A_index": ("? i + k * lda : i * lda + k", "? k + i * lda : i * lda + k"),
     "transposed_B_index": ("? k + j * ldb : k * ldb + j", "? k + j * ldb : j * ldb + k"),
@@ -25,7 +26,7 @@ MUTANTS = {
                             "if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, i);"),
     "relu_dropped": ("if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;", ""),
     "ties_round_up": ("(fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0", "fl + 1.0"),
-    "int_beta_sign": ("if (beta != 0) v += beta *", "if (beta != 0) v -= beta *"),
+    "int_beta_sign": ("v += beta * c;", "v -= beta * c;"),
     "k_loop_short_f16": ("for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += f16_table",
                          "for (int64_t k = 1; k < p->K; ++k, ia += da, ib += db) acc += f16_table"),
     "k_loop_short_int": ("for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += (int64_t)",
@@ -40,7 +41,8 @@ PINS = [
     lambda: [T.test_hand_worked_examples(c, lay) for c in T._golden_cases() for lay in T.LAYOUTS],
     lambda: [T.test_small_integers_match_numpy_int_matmul(lay, ab, epi)
              for lay in T.LAYOUTS for ab in ["f16", "s8"]
-             for epi in ["plain", "alpha_beta", "bias_col_relu", "bias_row_relu"]],
+             for epi in ["plain", "alpha_beta", "bias_col_relu", "bias_row_relu",
+                         "relu_on_c_and_d"]],
     lambda: [T.test_identity_A_gives_op_B(lay, "f32") for lay in T.LAYOUTS],
     lambda: [T.test_f16_rounding_cases(x, b) for x, b in T.F16_CASES],
     lambda: [T.test_bf16_rounding_cases(x, b) for x, b in T.BF16_CASES],
