@@ -37,6 +37,7 @@ struct EpiParams {
   int32_t bias_dtype;
   int32_t bias_mode;          // gemm_bias_mode_t
   int32_t relu;
+  int32_t c_relu;             // ReLU applied to each C element as it is read
   int32_t vec_c;              // C rows may be read with 16-byte vectors
   int32_t vec_d;              // D rows may be written with 16-byte vectors
   int32_t read_c;             // beta != 0
@@ -96,6 +97,9 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float4 c = c4[q];
+          if (e.c_relu) {
+            c.x = fmaxf(c.x, 0.0f); c.y = fmaxf(c.y, 0.0f); c.z = fmaxf(c.z, 0.0f); c.w = fmaxf(c.w, 0.0f);
+          }
           x[4 * q + 0] = fmaf(e.beta, c.x, x[4 * q + 0]);
           x[4 * q + 1] = fmaf(e.beta, c.y, x[4 * q + 1]);
           x[4 * q + 2] = fmaf(e.beta, c.z, x[4 * q + 2]);
@@ -117,6 +121,10 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
               __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[h]);
               lo = __low2float(v); hi = __high2float(v);
             }
+            if (e.c_relu) {
+              lo = fmaxf(lo, 0.0f);
+              hi = fmaxf(hi, 0.0f);
+            }
             x[8 * q + 2 * h + 0] = fmaf(e.beta, lo, x[8 * q + 2 * h + 0]);
             x[8 * q + 2 * h + 1] = fmaf(e.beta, hi, x[8 * q + 2 * h + 1]);
           }
@@ -125,7 +133,11 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (n_base + j < N) x[j] = fmaf(e.beta, load_as_float(e.C, e.c_dtype, off + j), x[j]);
+        if (n_base + j < N) {
+          float c = load_as_float(e.C, e.c_dtype, off + j);
+          if (e.c_relu) c = fmaxf(c, 0.0f);
+          x[j] = fmaf(e.beta, c, x[j]);
+        }
     }
   }
   if (e.bias_mode == GEMM_BIAS_COL) {
@@ -191,6 +203,9 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         int4 c = c4[q];
+        if (e.c_relu) {
+          c.x = c.x > 0 ? c.x : 0; c.y = c.y > 0 ? c.y : 0; c.z = c.z > 0 ? c.z : 0; c.w = c.w > 0 ? c.w : 0;
+        }
         x[4 * q + 0] = wrap_madd(e.beta_i, c.x, x[4 * q + 0]);
         x[4 * q + 1] = wrap_madd(e.beta_i, c.y, x[4 * q + 1]);
         x[4 * q + 2] = wrap_madd(e.beta_i, c.z, x[4 * q + 2]);
@@ -199,7 +214,11 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (n_base + j < N) x[j] = wrap_madd(e.beta_i, load_as_int(e.C, GEMM_S32, off + j), x[j]);
+        if (n_base + j < N) {
+          int32_t c = load_as_int(e.C, GEMM_S32, off + j);
+          if (e.c_relu) c = c > 0 ? c : 0;
+          x[j] = wrap_madd(e.beta_i, c, x[j]);
+        }
     }
   }
   if (e.bias_mode == GEMM_BIAS_COL) {

@@ -161,13 +161,20 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
       if (e.read_c) {
         const int64_t off = m * e.ldc + nb;
         if (full && e.vec_c && e.c_dtype == GEMM_F32) {
-          const float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(e.C) + off);
+          float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(e.C) + off);
+          if (e.c_relu) {
+            c.x = fmaxf(c.x, 0.0f); c.y = fmaxf(c.y, 0.0f); c.z = fmaxf(c.z, 0.0f); c.w = fmaxf(c.w, 0.0f);
+          }
           x[0] = fmaf(e.beta, c.x, x[0]); x[1] = fmaf(e.beta, c.y, x[1]);
           x[2] = fmaf(e.beta, c.z, x[2]); x[3] = fmaf(e.beta, c.w, x[3]);
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (nb + j < p.N) x[j] = fmaf(e.beta, load_as_float(e.C, e.c_dtype, off + j), x[j]);
+            if (nb + j < p.N) {
+              float c = load_as_float(e.C, e.c_dtype, off + j);
+              if (e.c_relu) c = fmaxf(c, 0.0f);
+              x[j] = fmaf(e.beta, c, x[j]);
+            }
         }
       }
       if (e.bias_mode == GEMM_BIAS_COL) {
@@ -246,14 +253,22 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
   const EpiParams& e = p.epi;
   if constexpr (IS_INT) {
     int32_t v = wrap_madd(e.alpha_i, acc, 0);
-    if (e.read_c) v = wrap_madd(e.beta_i, load_as_int(e.C, GEMM_S32, i * e.ldc + j), v);
+    if (e.read_c) {
+      int32_t c = load_as_int(e.C, GEMM_S32, i * e.ldc + j);
+      if (e.c_relu) c = c > 0 ? c : 0;
+      v = wrap_madd(e.beta_i, c, v);
+    }
     if (e.bias_mode == GEMM_BIAS_COL) v = wrap_madd(1, load_as_int(e.bias, GEMM_S32, j), v);
     else if (e.bias_mode == GEMM_BIAS_ROW) v = wrap_madd(1, load_as_int(e.bias, GEMM_S32, i), v);
     if (e.relu) v = v > 0 ? v : 0;
     static_cast<int32_t*>(e.D)[i * e.ldd + j] = v;
   } else {
     float v = acc * e.alpha;
-    if (e.read_c) v = fmaf(e.beta, load_as_float(e.C, e.c_dtype, i * e.ldc + j), v);
+    if (e.read_c) {
+      float c = load_as_float(e.C, e.c_dtype, i * e.ldc + j);
+      if (e.c_relu) c = fmaxf(c, 0.0f);
+      v = fmaf(e.beta, c, v);
+    }
     if (e.bias_mode == GEMM_BIAS_COL) v += load_as_float(e.bias, e.bias_dtype, j);
     else if (e.bias_mode == GEMM_BIAS_ROW) v += load_as_float(e.bias, e.bias_dtype, i);
     if (e.relu) v = fmaxf(v, 0.0f);

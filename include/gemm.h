@@ -74,15 +74,19 @@ typedef enum {
     GEMM_BIAS_ROW = 2  /* bias has M entries; bias[i] is added to row i (transposed use) */
 } gemm_bias_mode_t;
 
-/* Fused epilogue.  Order: v = alpha*acc + beta*C[i,j] + bias; v = act(v);
+/* Fused epilogue.  Order: v = alpha*acc + beta*c_act(C[i,j]) + bias; v = act(v);
  * D[i,j] = cast to out_dtype (round to nearest even).  NULL epilogue pointer
- * means: no bias, no activation, out_dtype equal to the plan's c_dtype. */
+ * means: no bias, no activations, out_dtype equal to the plan's c_dtype.
+ * c_act is the elementwise transform applied to C as it is read ("ReLU on C",
+ * "Flexible Performant GEMM Kernels on GPUs", section 5.3, Table 2); it only
+ * matters when beta != 0. */
 typedef struct {
     const void* bias;             /* device pointer, or NULL when bias_mode == GEMM_BIAS_NONE */
     gemm_dtype_t bias_dtype;      /* F32/F16/BF16 for floating plans, S32 for int8 plans */
     gemm_bias_mode_t bias_mode;
-    gemm_act_t act;
+    gemm_act_t act;               /* activation of the result (before the cast) */
     gemm_dtype_t out_dtype;       /* dtype of D */
+    gemm_act_t c_act;             /* transform of C as it is read (GEMM_ACT_NONE / GEMM_ACT_RELU) */
 } gemm_epilogue_t;
 
 typedef struct gemm_plan* gemm_plan_t;
@@ -236,7 +240,7 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 101 (gemm_epilogue_t.c_act). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------

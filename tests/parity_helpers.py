@@ -101,7 +101,8 @@ class DeviceProblem:
                                self.bias.data_ptr() if self.bias is not None else 0,
                                G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
                                G_BIAS[p.bias_mode],
-                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE)
+                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE,
+                               G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE)
 
     def run(self, plan: G.Plan, stream=None):
         p = self.p

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings():
-    assert G.gemm_abi_version() == 100
+    assert G.gemm_abi_version() == 101
     for s in range(6):
         assert G.gemm_status_string(s).startswith("GEMM_")
     assert "unknown" in G.gemm_status_string(99)
@@ -74,6 +74,7 @@ def test_validation_accepts_a_plain_problem():
     (dict(epi=G.make_epilogue(G.GEMM_F32, P, G.GEMM_S8, G.GEMM_BIAS_COL)),
      G.GEMM_ERR_INVALID_ARG),                                        # bias type
     (dict(M=1 << 31), G.GEMM_ERR_UNSUPPORTED),
+    (dict(epi=G.make_epilogue(G.GEMM_F32, c_act=7)), G.GEMM_ERR_INVALID_ARG),
 ])
 def test_validation_rejects(kw, status):
     assert _v(**kw) == status

@@ -317,3 +317,21 @@ def test_pair_stream_k_repeated_launches(layout, monkeypatch):
         assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["sk_tiles"] > 0
         H.check_close(dp.result(), ref, "f32", "stream-K repeat")
     dp.check_guards()
+
+
+# ------------------------- transform of C as it is read ----------------------
+
+@pytest.mark.parametrize("kernel,ab", [(G.GEMM_KERNEL_TC_PAIR, "f16"), (G.GEMM_KERNEL_TC, "bf16"),
+                                       (G.GEMM_KERNEL_TC_INT8, "s8"), (G.GEMM_KERNEL_FFMA, "f32"),
+                                       (G.GEMM_KERNEL_SIMT, "f16")],
+                         ids=["pair", "cta1", "int8", "ffma", "simt"])
+def test_bias_relu_on_c_and_d(kernel, ab):
+    """The last row of the paper's fusion table: bias, ReLU on C (as it is read)
+    and ReLU on D, in one kernel."""
+    is_int = ab == "s8"
+    cd = "s32" if is_int else "f32"
+    kw = dict(dist_a=I.I8, dist_b=I.I8, dist_c=I.Dist("int", -200000, 200000),
+              dist_bias=I.Dist("int", -3000, 3000)) if is_int else {}
+    p = H.tma_aligned(I.Problem("relu_c", ab, "T", "N", 300, 264, 320, alpha=1.0, beta=1.5, c=cd,
+                                d=cd, bias=cd, bias_mode="col", act="relu", c_act="relu", **kw))
+    H.run_and_check_full(p, 140, kernel=kernel, expect_kernel=kernel)
