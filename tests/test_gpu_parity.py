@@ -332,6 +332,7 @@ def test_bias_relu_on_c_and_d(kernel, ab):
     cd = "s32" if is_int else "f32"
     kw = dict(dist_a=I.I8, dist_b=I.I8, dist_c=I.Dist("int", -200000, 200000),
               dist_bias=I.Dist("int", -3000, 3000)) if is_int else {}
-    p = H.tma_aligned(I.Problem("relu_c", ab, "T", "N", 300, 264, 320, alpha=1.0, beta=1.5, c=cd,
+    beta = 2.0 if is_int else 1.5      # the int8 path takes integral alpha and beta
+    p = H.tma_aligned(I.Problem("relu_c", ab, "T", "N", 300, 264, 320, alpha=1.0, beta=beta, c=cd,
                                 d=cd, bias=cd, bias_mode="col", act="relu", c_act="relu", **kw))
     H.run_and_check_full(p, 140, kernel=kernel, expect_kernel=kernel)
