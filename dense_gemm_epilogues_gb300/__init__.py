@@ -39,7 +39,7 @@ LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host", "gemm_validate",
             "gemm_select", "gemm_plan_set_kernel", "gemm_plan_last_config", "gemm_plan_device_status",
             "gemm_plan_set_timeout", "gemm_status_string", "gemm_abi_version",
-            "gemm_run_s8_noalloc"]
+            "gemm_run_s8_noalloc", "gemm_run_strided_batched"]
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -95,6 +95,9 @@ def load_library(path: str = LIB_PATH):
     lib.gemm_status_string.argtypes = [ci]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_abi_version.argtypes = []
+    lib.gemm_run_strided_batched.argtypes = [vp, ci, ci, i64, i64, i64, dbl, vp, i64, i64, vp, i64, i64,
+                                             dbl, vp, i64, i64, vp, i64, i64, i64,
+                                             ctypes.POINTER(gemm_epilogue_t), i64, vp]
     lib.gemm_run_s8_noalloc.argtypes = [ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64,
                                         vp, i64, ctypes.POINTER(gemm_epilogue_t), vp, vp]
     for name in EXPORTED:
@@ -150,6 +153,17 @@ def gemm_run_host(plan, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta
                   epi: Optional[gemm_epilogue_t] = None, stream: int = 0) -> None:
     _check(load_library().gemm_run_host(plan, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
                                         beta, C, ldc, D, ldd, _epi_ptr(epi), stream), "gemm_run_host")
+
+
+def gemm_run_strided_batched(plan, layout_a, layout_b, M, N, K, alpha, A, lda, stride_a, B, ldb,
+                             stride_b, beta, C, ldc, stride_c, D, ldd, stride_d, batch,
+                             epi: Optional[gemm_epilogue_t] = None, stride_bias: int = 0,
+                             stream: int = 0) -> None:
+    _check(load_library().gemm_run_strided_batched(plan, layout_a, layout_b, M, N, K, alpha, A, lda,
+                                                   stride_a, B, ldb, stride_b, beta, C, ldc,
+                                                   stride_c, D, ldd, stride_d, batch,
+                                                   _epi_ptr(epi), stride_bias, stream),
+           "gemm_run_strided_batched")
 
 
 def gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd,

@@ -41,6 +41,16 @@ struct EpiParams {
   int32_t vec_c;              // C rows may be read with 16-byte vectors
   int32_t vec_d;              // D rows may be written with 16-byte vectors
   int32_t read_c;             // beta != 0
+  int64_t stride_c;           // batched problems: elements between consecutive C, D and bias
+  int64_t stride_d;
+  int64_t stride_bias;
+};
+
+// The C, D and bias of one problem of a (strided) batch.
+struct EpiPtrs {
+  const void* C;
+  void* D;
+  const void* bias;
 };
 
 __host__ __device__ inline int dtype_bytes(int dt) {
@@ -48,6 +58,14 @@ __host__ __device__ inline int dtype_bytes(int dt) {
 }
 
 #if defined(__CUDACC__)
+
+__device__ __forceinline__ EpiPtrs epi_ptrs(const EpiParams& e, int64_t bz) {
+  EpiPtrs q;
+  q.C = static_cast<const char*>(e.C) + bz * e.stride_c * dtype_bytes(e.c_dtype);
+  q.D = static_cast<char*>(e.D) + bz * e.stride_d * dtype_bytes(e.d_dtype);
+  q.bias = static_cast<const char*>(e.bias) + bz * e.stride_bias * dtype_bytes(e.bias_dtype);
+  return q;
+}
 
 // --------------------------- scalar element access -------------------------
 
@@ -86,14 +104,14 @@ __device__ __forceinline__ int32_t wrap_madd(int32_t a, int32_t b, int32_t c) {
 // x[j] holds alpha*acc for columns n_base..n_base+31 of row m.  Called by all
 // 32 lanes of a warp together (the bias is shared by shuffles); lanes whose row
 // is outside D (row_ok false) take part but neither read C nor store.
-__device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64_t m, bool row_ok,
-                                                       int64_t n_base, int64_t N, float (&x)[32]) {
+__device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, const EpiPtrs& ptr, int64_t m,
+                                                       bool row_ok, int64_t n_base, int64_t N, float (&x)[32]) {
   const bool full = n_base + 32 <= N;
   if (e.read_c && row_ok) {
     const int64_t off = m * e.ldc + n_base;
     if (full && e.vec_c) {
       if (e.c_dtype == GEMM_F32) {
-        const float4* c4 = reinterpret_cast<const float4*>(static_cast<const float*>(e.C) + off);
+        const float4* c4 = reinterpret_cast<const float4*>(static_cast<const float*>(ptr.C) + off);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float4 c = c4[q];
@@ -106,7 +124,7 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
           x[4 * q + 3] = fmaf(e.beta, c.w, x[4 * q + 3]);
         }
       } else {
-        const uint4* c4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(e.C) + off);
+        const uint4* c4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(ptr.C) + off);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 c = c4[q];
@@ -134,7 +152,7 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (n_base + j < N) {
-          float c = load_as_float(e.C, e.c_dtype, off + j);
+          float c = load_as_float(ptr.C, e.c_dtype, off + j);
           if (e.c_relu) c = fmaxf(c, 0.0f);
           x[j] = fmaf(e.beta, c, x[j]);
         }
@@ -144,11 +162,11 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
     // Every lane needs the same 32 bias values: lane j loads bias[n_base + j]
     // once (coalesced) and the warp shares them by shuffles.
     const int lane = threadIdx.x & 31;
-    const float bl = (n_base + lane < N) ? load_as_float(e.bias, e.bias_dtype, n_base + lane) : 0.0f;
+    const float bl = (n_base + lane < N) ? load_as_float(ptr.bias, e.bias_dtype, n_base + lane) : 0.0f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] += __shfl_sync(0xffffffffu, bl, j);
   } else if (e.bias_mode == GEMM_BIAS_ROW && row_ok) {
-    const float b = load_as_float(e.bias, e.bias_dtype, m);
+    const float b = load_as_float(ptr.bias, e.bias_dtype, m);
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] += b;
   }
@@ -160,11 +178,11 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
   const int64_t doff = m * e.ldd + n_base;
   if (full && e.vec_d) {
     if (e.d_dtype == GEMM_F32) {
-      float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(e.D) + doff);
+      float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(ptr.D) + doff);
 #pragma unroll
       for (int q = 0; q < 8; ++q) d4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     } else {
-      uint4* d4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.D) + doff);
+      uint4* d4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ptr.D) + doff);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t w[4];
@@ -184,22 +202,22 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, int64
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (n_base + j < N) store_float_as(e.D, e.d_dtype, doff + j, x[j]);
+      if (n_base + j < N) store_float_as(ptr.D, e.d_dtype, doff + j, x[j]);
   }
 }
 
 // x[j] holds the exact int32 product sums of columns n_base..n_base+31 of row m;
 // it is finished in place (alpha, beta*C, bias, ReLU) and stored.  Called by all
 // 32 lanes of a warp together, as the floating version.
-__device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t m, bool row_ok,
-                                                     int64_t n_base, int64_t N, int32_t* x) {
+__device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, const EpiPtrs& ptr, int64_t m,
+                                                     bool row_ok, int64_t n_base, int64_t N, int32_t* x) {
   const bool full = n_base + 32 <= N;
 #pragma unroll
   for (int j = 0; j < 32; ++j) x[j] = wrap_madd(e.alpha_i, x[j], 0);
   if (e.read_c && row_ok) {
     const int64_t off = m * e.ldc + n_base;
     if (full && e.vec_c) {
-      const int4* c4 = reinterpret_cast<const int4*>(static_cast<const int32_t*>(e.C) + off);
+      const int4* c4 = reinterpret_cast<const int4*>(static_cast<const int32_t*>(ptr.C) + off);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         int4 c = c4[q];
@@ -215,7 +233,7 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (n_base + j < N) {
-          int32_t c = load_as_int(e.C, GEMM_S32, off + j);
+          int32_t c = load_as_int(ptr.C, GEMM_S32, off + j);
           if (e.c_relu) c = c > 0 ? c : 0;
           x[j] = wrap_madd(e.beta_i, c, x[j]);
         }
@@ -223,11 +241,11 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t
   }
   if (e.bias_mode == GEMM_BIAS_COL) {
     const int lane = threadIdx.x & 31;
-    const int32_t bl = (n_base + lane < N) ? load_as_int(e.bias, GEMM_S32, n_base + lane) : 0;
+    const int32_t bl = (n_base + lane < N) ? load_as_int(ptr.bias, GEMM_S32, n_base + lane) : 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = wrap_madd(1, __shfl_sync(0xffffffffu, bl, j), x[j]);
   } else if (e.bias_mode == GEMM_BIAS_ROW && row_ok) {
-    const int32_t b = load_as_int(e.bias, GEMM_S32, m);
+    const int32_t b = load_as_int(ptr.bias, GEMM_S32, m);
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = wrap_madd(1, b, x[j]);
   }
@@ -236,7 +254,7 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, int64_t
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = x[j] > 0 ? x[j] : 0;
   }
-  int32_t* d = static_cast<int32_t*>(e.D) + m * e.ldd + n_base;
+  int32_t* d = static_cast<int32_t*>(ptr.D) + m * e.ldd + n_base;
   if (full && e.vec_d) {
     int4* d4 = reinterpret_cast<int4*>(d);
 #pragma unroll
@@ -318,6 +336,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 3-D tiled TMA load (x innermost, z = problem of a batch).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 
@@ -413,6 +440,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
+                                                 int32_t z, uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr)
       : "memory");
 }
 

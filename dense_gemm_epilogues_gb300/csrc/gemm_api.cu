@@ -119,7 +119,8 @@ double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 40
 // target device (0: that kernel is not considered unless forced).
 gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
                             int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                            int sm_count, gemm_kernel_t forced, gemm_config_t* out, int pair_clusters = 0) {
+                            int sm_count, gemm_kernel_t forced, gemm_config_t* out, int pair_clusters = 0,
+                            int64_t batch = 1) {
   (void)c;
   gemm_config_t cfg{};
   cfg.split_k = 1;
@@ -169,7 +170,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.stages = tc_pair_stages();
       cfg.cta_group = 2;
       const int64_t tiles_m = (M + 255) / 256, tiles_n = (N + 255) / 256;
-      cfg.tiles = (int32_t)std::min<int64_t>(tiles_m * tiles_n, kMaxDim);
+      cfg.tiles = (int32_t)std::min<int64_t>(batch * tiles_m * tiles_n, kMaxDim);
       int raster = 8;
       if (const char* env = std::getenv("GEMM_TC_RASTER")) raster = std::max(1, std::atoi(env));
       cfg.raster = (int32_t)std::min<int64_t>(raster, tiles_m);
@@ -204,7 +205,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         // (the largest tile that fits, unless it leaves SMs idle).
         double best = 1e300;
         for (int cand : {256, 128}) {
-          const int64_t tiles = ((M + 127) / 128) * ((N + cand - 1) / cand);
+          const int64_t tiles = batch * ((M + 127) / 128) * ((N + cand - 1) / cand);
           const int64_t waves = (tiles + sm_count - 1) / sm_count;
           const double cost = (double)waves * tc_tile_cost(cand);
           if (cost < best - 1e-9) { best = cost; bn = cand; }
@@ -220,7 +221,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.bk = TC_BK;
       cfg.stages = tc_stages(bn);
       const int64_t tiles_m = (M + 127) / 128, tiles_n = (N + bn - 1) / bn;
-      cfg.tiles = (int32_t)std::min<int64_t>(tiles_m * tiles_n, kMaxDim);
+      cfg.tiles = (int32_t)std::min<int64_t>(batch * tiles_m * tiles_n, kMaxDim);
       cfg.raster = (int32_t)std::min<int64_t>(16, tiles_m);
       cfg.grid = (int32_t)std::min<int64_t>(cfg.tiles, sm_count);
       // Exact int8 chunk: |sum of 1024 products| <= 1024 * 2^14 = 2^24, and every
@@ -238,7 +239,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         cfg.stages = tc_pair_stages();
         cfg.cta_group = 2;
         const int64_t ptm = (M + 255) / 256, ptn = (N + 255) / 256;
-        cfg.tiles = (int32_t)std::min<int64_t>(ptm * ptn, kMaxDim);
+        cfg.tiles = (int32_t)std::min<int64_t>(batch * ptm * ptn, kMaxDim);
         cfg.raster = (int32_t)std::min<int64_t>(8, ptm);
         cfg.grid = 2 * (int32_t)std::min<int64_t>(cfg.tiles, pair_clusters);
       }
@@ -249,7 +250,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.bn = FFMA_BN;
       cfg.bk = FFMA_BK;
       cfg.stages = 2;
-      const int64_t tiles = ((M + FFMA_BM - 1) / FFMA_BM) * ((N + FFMA_BN - 1) / FFMA_BN);
+      const int64_t tiles = batch * ((M + FFMA_BM - 1) / FFMA_BM) * ((N + FFMA_BN - 1) / FFMA_BN);
       cfg.tiles = (int32_t)std::min<int64_t>(tiles, kMaxDim);
       cfg.grid = cfg.tiles;
       cfg.raster = 1;
@@ -260,7 +261,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.bn = 16;
       cfg.bk = 16;
       cfg.stages = 1;
-      const int64_t tiles = ((M + 15) / 16) * ((N + 15) / 16);
+      const int64_t tiles = batch * ((M + 15) / 16) * ((N + 15) / 16);
       cfg.tiles = (int32_t)std::min<int64_t>(tiles, kMaxDim);
       cfg.grid = cfg.tiles;
       cfg.raster = 1;
@@ -288,20 +289,32 @@ bool encode_fn() {
   return g_encode != nullptr;
 }
 
-// Row-pitched 2-D tensor (inner elements contiguous, `ld` elements between rows
-// of the outer dimension), 16-bit elements, 128-byte swizzle, zero fill out of bounds.
-bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
-               uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+// A row-pitched tensor of 16-bit elements (inner elements contiguous, `ld`
+// elements between rows of the outer dimension) with a third, outermost
+// dimension: `nbatch` problems `bstride` elements apart (one problem when
+// nbatch == 1).  128-byte swizzle; out-of-bounds elements read as zero.
+bool encode_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t ld, uint64_t nbatch, uint64_t bstride, uint32_t box_inner, uint32_t box_outer) {
   if (!encode_fn()) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  if (nbatch <= 1) {
+    nbatch = 1;
+    bstride = (ld * outer + 7) / 8 * 8;   // unused; any 16-byte multiple past the problem
+  }
+  cuuint64_t dims[3] = {inner, outer, nbatch};
+  cuuint64_t strides[2] = {ld * 2, bstride * 2};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(tm, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+// A strided batch of independent problems (count 1: one problem).
+struct Batch {
+  int64_t count = 1;
+  int64_t sa = 0, sb = 0, sc = 0, sd = 0, sbias = 0;   // element strides (0: shared by all)
+};
 
 // tcgen05 instruction descriptor, kind::f16 with fp32 accumulation:
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16, 1 = bf16),
@@ -371,19 +384,21 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
                                 int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                                 int64_t ldb, CUtensorMapDataType dt, bool bf16, const EpiParams& epi,
-                                int chunk_kb, cudaStream_t stream) {
+                                int chunk_kb, cudaStream_t stream, const Batch& bt = Batch()) {
   TcParams tp;
   std::memset(&tp, 0, sizeof(tp));
   const int bn = cfg.bn;
   const bool a_mn = la == GEMM_OP_N, b_mn = lb == GEMM_OP_T;
+  const uint64_t na = (bt.count > 1 && bt.sa != 0) ? (uint64_t)bt.count : 1;
+  const uint64_t nb = (bt.count > 1 && bt.sb != 0) ? (uint64_t)bt.count : 1;
   bool ok;
   // A: K-major (row-major A) boxes 64(K) x 128(M); M-major boxes 64(M) x 64(K).
-  if (!a_mn) ok = encode_2d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, TC_BK, TC_BM);
-  else ok = encode_2d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, 64, TC_BK);
+  if (!a_mn) ok = encode_3d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, na, bt.sa, TC_BK, TC_BM);
+  else ok = encode_3d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, na, bt.sa, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
   // B: K-major (column-major B) boxes 64(K) x BN(N); N-major boxes 64(N) x 64(K).
-  if (!b_mn) ok = encode_2d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, TC_BK, (uint32_t)bn);
-  else ok = encode_2d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, TC_BK);
+  if (!b_mn) ok = encode_3d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, (uint32_t)bn);
+  else ok = encode_3d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, bt.sb, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
   tp.M = (int32_t)M;
   tp.N = (int32_t)N;
@@ -391,7 +406,10 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   tp.num_kb = (int32_t)((K + TC_BK - 1) / TC_BK);
   tp.tiles_m = (int32_t)((M + TC_BM - 1) / TC_BM);
   tp.tiles_n = (int32_t)((N + bn - 1) / bn);
-  tp.num_tiles = tp.tiles_m * tp.tiles_n;
+  tp.tiles_per_batch = tp.tiles_m * tp.tiles_n;
+  tp.num_tiles = tp.tiles_per_batch * (int32_t)bt.count;
+  tp.a_batched = na > 1;
+  tp.b_batched = nb > 1;
   tp.raster = cfg.raster > 0 ? cfg.raster : 1;
   tp.a_mn_major = a_mn ? 1 : 0;
   tp.b_mn_major = b_mn ? 1 : 0;
@@ -410,17 +428,19 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
 gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
                                   int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                                   int64_t ldb, bool bf16, const EpiParams& epi, cudaStream_t stream,
-                                  int chunk_kb = 0) {
+                                  int chunk_kb = 0, const Batch& bt = Batch()) {
   TcParams tp;
   std::memset(&tp, 0, sizeof(tp));
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const bool a_mn = la == GEMM_OP_N, b_mn = lb == GEMM_OP_T;
+  const uint64_t na = (bt.count > 1 && bt.sa != 0) ? (uint64_t)bt.count : 1;
+  const uint64_t nb = (bt.count > 1 && bt.sb != 0) ? (uint64_t)bt.count : 1;
   bool ok;
-  if (!a_mn) ok = encode_2d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, TC_BK, TC_BM);
-  else ok = encode_2d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, 64, TC_BK);
+  if (!a_mn) ok = encode_3d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, na, bt.sa, TC_BK, TC_BM);
+  else ok = encode_3d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, na, bt.sa, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
-  if (!b_mn) ok = encode_2d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, TC_BK, 128);
-  else ok = encode_2d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, TC_BK);
+  if (!b_mn) ok = encode_3d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, 128);
+  else ok = encode_3d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, bt.sb, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
   tp.M = (int32_t)M;
   tp.N = (int32_t)N;
@@ -428,7 +448,10 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   tp.num_kb = (int32_t)((K + TC_BK - 1) / TC_BK);
   tp.tiles_m = (int32_t)((M + 255) / 256);
   tp.tiles_n = (int32_t)((N + 255) / 256);
-  tp.num_tiles = tp.tiles_m * tp.tiles_n;
+  tp.tiles_per_batch = tp.tiles_m * tp.tiles_n;
+  tp.num_tiles = tp.tiles_per_batch * (int32_t)bt.count;
+  tp.a_batched = na > 1;
+  tp.b_batched = nb > 1;
   tp.raster = cfg.raster > 0 ? cfg.raster : 1;
   tp.a_mn_major = a_mn ? 1 : 0;
   tp.b_mn_major = b_mn ? 1 : 0;
@@ -464,7 +487,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
 
 extern "C" {
 
-int gemm_abi_version(void) { return 101; }
+int gemm_abi_version(void) { return 102; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
@@ -571,16 +594,18 @@ gemm_status_t gemm_plan_device_status(gemm_plan_t plan, gemm_stream_t stream, in
   return GEMM_OK;
 }
 
-gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N, int64_t K,
+}  // extern "C"
+
+namespace {
+
+// One launch of a (strided) batch of problems whose arguments are already valid.
+gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N, int64_t K,
                        double alpha, const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
                        const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
-                       gemm_stream_t stream_) {
-  if (!plan) return GEMM_ERR_INVALID_ARG;
-  gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
-  if (s != GEMM_OK) return s;
+                       gemm_stream_t stream_, const Batch& bt) {
   gemm_config_t cfg{};
-  s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count, plan->forced, &cfg,
-                    plan->pair_clusters);
+  gemm_status_t s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count,
+                                  plan->forced, &cfg, plan->pair_clusters, bt.count);
   if (s != GEMM_OK) return s;
   if (cfg.kernel == GEMM_KERNEL_NONE) {
     plan->last = cfg;
@@ -589,23 +614,29 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
   DeviceGuard g(plan->device);
   if (!g.ok) return GEMM_ERR_CUDA;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  const EpiParams e = make_epi(plan, alpha, beta, C, ldc, D, ldd, epi);
+  EpiParams e = make_epi(plan, alpha, beta, C, ldc, D, ldd, epi);
+  e.stride_c = bt.sc;
+  e.stride_d = bt.sd;
+  e.stride_bias = bt.sbias;
 
   switch (cfg.kernel) {
     case GEMM_KERNEL_TC_PAIR:
-      s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb, plan->ab == GEMM_BF16, e, stream);
+      s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb, plan->ab == GEMM_BF16, e, stream, 0, bt);
       break;
     case GEMM_KERNEL_TC: {
       const bool bf16 = plan->ab == GEMM_BF16;
       s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb,
                             bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bf16,
-                            e, 0, stream);
+                            e, 0, stream, bt);
       break;
     }
     case GEMM_KERNEL_TC_INT8: {
-      // Stage exact fp16 copies of A and B (same layouts and leading dimensions).
-      const int64_t a_el = storage_elems(la, M, K, lda);
-      const int64_t b_el = storage_elems(lb, K, N, ldb);
+      // Stage exact fp16 copies of A and B (same layouts, leading dimensions and
+      // batch strides; a shared operand, stride 0, is staged once).
+      const int64_t na = (bt.count > 1 && bt.sa != 0) ? bt.count : 1;
+      const int64_t nb = (bt.count > 1 && bt.sb != 0) ? bt.count : 1;
+      const int64_t a_el = (na - 1) * bt.sa + storage_elems(la, M, K, lda);
+      const int64_t b_el = (nb - 1) * bt.sb + storage_elems(lb, K, N, ldb);
       const size_t a_bytes = align_up((size_t)a_el * 2, 256);
       s = ensure_ws(plan, a_bytes + (size_t)b_el * 2, stream);
       if (s != GEMM_OK) break;
@@ -613,18 +644,20 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       __half* B16 = reinterpret_cast<__half*>(static_cast<char*>(plan->ws) + a_bytes);
       const int8_t* A8 = static_cast<const int8_t*>(A);
       const int8_t* B8 = static_cast<const int8_t*>(B);
-      cudaError_t ce = la == GEMM_OP_T ? launch_s8_to_f16(A8, A16, M, K, lda, stream)
-                                       : launch_s8_to_f16(A8, A16, K, M, lda, stream);
-      if (ce == cudaSuccess)
-        ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8, B16, N, K, ldb, stream)
-                             : launch_s8_to_f16(B8, B16, K, N, ldb, stream);
+      cudaError_t ce = cudaSuccess;
+      for (int64_t z = 0; z < na && ce == cudaSuccess; ++z)
+        ce = la == GEMM_OP_T ? launch_s8_to_f16(A8 + z * bt.sa, A16 + z * bt.sa, M, K, lda, stream)
+                             : launch_s8_to_f16(A8 + z * bt.sa, A16 + z * bt.sa, K, M, lda, stream);
+      for (int64_t z = 0; z < nb && ce == cudaSuccess; ++z)
+        ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8 + z * bt.sb, B16 + z * bt.sb, N, K, ldb, stream)
+                             : launch_s8_to_f16(B8 + z * bt.sb, B16 + z * bt.sb, K, N, ldb, stream);
       if (ce != cudaSuccess) { s = GEMM_ERR_CUDA; break; }
       if (cfg.cta_group == 2)
         s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, false, e, stream,
-                                cfg.k_chunk / TC_BK);
+                                cfg.k_chunk / TC_BK, bt);
       else
         s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                              false, e, cfg.k_chunk / TC_BK, stream);
+                              false, e, cfg.k_chunk / TC_BK, stream, bt);
       break;
     }
     case GEMM_KERNEL_FFMA: {
@@ -636,8 +669,11 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       fp.M = (int32_t)M;
       fp.N = (int32_t)N;
       fp.K = (int32_t)K;
+      fp.stride_a = bt.sa;
+      fp.stride_b = bt.sb;
       fp.epi = e;
-      s = launch_ffma(fp, la == GEMM_OP_T, lb == GEMM_OP_T, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+      s = launch_ffma(fp, la == GEMM_OP_T, lb == GEMM_OP_T, (int)bt.count, stream) == cudaSuccess ? GEMM_OK
+                                                                                     : GEMM_ERR_CUDA;
       break;
     }
     default: {
@@ -652,13 +688,86 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       sp.M = M;
       sp.N = N;
       sp.K = K;
+      sp.stride_a = bt.sa;
+      sp.stride_b = bt.sb;
       sp.epi = e;
-      s = launch_simt(sp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+      s = launch_simt(sp, (int)bt.count, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
       break;
     }
   }
   if (s == GEMM_OK) plan->last = cfg;
   return s;
+}
+
+// Can the tensor-core paths take this batch as one launch (TMA batch
+// dimension, tile count within range, grid rows within range for CUDA cores)?
+bool batch_fits_one_launch(gemm_dtype_t ab, int64_t M, int64_t N, const Batch& bt) {
+  if (bt.count <= 1) return true;
+  if (bt.count > 65535) return false;
+  const int es = dtype_bytes(ab);
+  const int64_t stage_es = ab == GEMM_S8 ? 2 : es;   // int8 operands are staged as fp16
+  for (int64_t st : {bt.sa, bt.sb})
+    if (st != 0 && ((st * stage_es) % 16 != 0 || st * stage_es >= (int64_t(1) << 40))) return false;
+  const int64_t tiles = bt.count * ((M + 127) / 128) * ((N + 127) / 128);
+  return tiles <= kMaxDim;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N, int64_t K,
+                       double alpha, const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                       const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
+                       gemm_stream_t stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  return run_impl(plan, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi, stream, Batch());
+}
+
+gemm_status_t gemm_run_strided_batched(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M,
+                                       int64_t N, int64_t K, double alpha, const void* A, int64_t lda,
+                                       int64_t stride_a, const void* B, int64_t ldb, int64_t stride_b,
+                                       double beta, const void* C, int64_t ldc, int64_t stride_c, void* D,
+                                       int64_t ldd, int64_t stride_d, int64_t batch,
+                                       const gemm_epilogue_t* epi, int64_t stride_bias, gemm_stream_t stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0 || stride_d < 0 || stride_bias < 0)
+    return GEMM_ERR_INVALID_ARG;
+  if (batch == 0 || M == 0 || N == 0) return GEMM_OK;
+  // Outputs of different problems must not overlap; in-place C == D needs equal strides.
+  if (batch > 1 && stride_d < (M - 1) * ldd + N) return GEMM_ERR_INVALID_ARG;
+  if (beta != 0.0 && C == D && stride_c != stride_d) return GEMM_ERR_INVALID_ARG;
+  Batch bt;
+  bt.count = batch;
+  bt.sa = K > 0 ? stride_a : 0;
+  bt.sb = K > 0 ? stride_b : 0;
+  bt.sc = beta != 0.0 ? stride_c : 0;
+  bt.sd = stride_d;
+  bt.sbias = (epi && epi->bias_mode != GEMM_BIAS_NONE) ? stride_bias : 0;
+  if (batch_fits_one_launch(plan->ab, M, N, bt))
+    return run_impl(plan, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi, stream, bt);
+  // Otherwise one launch per problem.
+  const int es = dtype_bytes(plan->ab), cs = dtype_bytes(plan->c);
+  const gemm_dtype_t out = out_dtype_of(plan->c, epi);
+  for (int64_t z = 0; z < batch; ++z) {
+    gemm_epilogue_t ez{};
+    if (epi) {
+      ez = *epi;
+      if (ez.bias_mode != GEMM_BIAS_NONE)
+        ez.bias = static_cast<const char*>(epi->bias) + z * bt.sbias * dtype_bytes(epi->bias_dtype);
+    }
+    s = run_impl(plan, la, lb, M, N, K, alpha, static_cast<const char*>(A) + z * bt.sa * es, lda,
+                 static_cast<const char*>(B) + z * bt.sb * es, ldb, beta,
+                 C ? static_cast<const char*>(C) + z * bt.sc * cs : nullptr, ldc,
+                 static_cast<char*>(D) + z * bt.sd * dtype_bytes(out), ldd, epi ? &ez : nullptr, stream,
+                 Batch());
+    if (s != GEMM_OK) return s;
+  }
+  return GEMM_OK;
 }
 
 gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N,

@@ -16,6 +16,9 @@ struct TcParams {
   int32_t M, N, K;
   int32_t num_kb;         // K blocks of 64 elements
   int32_t tiles_m, tiles_n, num_tiles;
+  int32_t tiles_per_batch;  // tiles_m * tiles_n; num_tiles = batch * tiles_per_batch
+  int32_t a_batched;      // A's tensor map has one slice per problem (else slice 0 for all)
+  int32_t b_batched;
   int32_t raster;         // tile rows per raster group
   int32_t a_mn_major;     // A stored M-contiguous (layout N) rather than K-contiguous
   int32_t b_mn_major;     // B stored N-contiguous (layout T) rather than K-contiguous
@@ -53,6 +56,7 @@ struct FfmaParams {
   const float* A;
   const float* B;
   int64_t lda, ldb;
+  int64_t stride_a, stride_b;   // batched problems (elements); one problem per grid row
   int32_t M, N, K;
   EpiParams epi;
 };
@@ -60,7 +64,7 @@ struct FfmaParams {
 #define GEMM_FFMA_BK 16
 #endif
 constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = GEMM_FFMA_BK;
-cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, cudaStream_t stream);
+cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, int batch, cudaStream_t stream);
 
 // Generic CUDA-core kernel: any dtype, layout, alignment; K may be 0.
 struct SimtParams {
@@ -70,9 +74,11 @@ struct SimtParams {
   int32_t ab_dtype;
   int32_t a_row_major, b_row_major;
   int64_t M, N, K;
+  int64_t stride_a, stride_b;   // batched problems (elements); one problem per grid row
   EpiParams epi;
 };
-cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream);
+cudaError_t launch_simt(const SimtParams& p, int batch, cudaStream_t stream);
+inline cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) { return launch_simt(p, 1, stream); }
 
 // int8 -> fp16 staging copy of a strided matrix: dst[r*ld + c] = src[r*ld + c]
 // for r < outer, c < inner.

@@ -95,9 +95,10 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
   const int64_t tiles_n = (p.N + FFMA_BN - 1) / FFMA_BN;
   const int64_t m0 = (int64_t)(blockIdx.x / tiles_n) * FFMA_BM;
   const int64_t n0 = (int64_t)(blockIdx.x % tiles_n) * FFMA_BN;
+  const int64_t bz = blockIdx.y;                      // problem of the batch
 
-  const SliceLoader<A_KMAJOR> la{p.A, p.lda, p.M, p.K};
-  const SliceLoader<B_KMAJOR> lb{p.B, p.ldb, p.N, p.K};
+  const SliceLoader<A_KMAJOR> la{p.A + bz * p.stride_a, p.lda, p.M, p.K};
+  const SliceLoader<B_KMAJOR> lb{p.B + bz * p.stride_b, p.ldb, p.N, p.K};
 
   float acc[8][8];
 #pragma unroll
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
 
   // Fused epilogue.  Thread rows: ty*4+i and 64+ty*4+i; columns tx*4+j and 64+tx*4+j.
   const EpiParams& e = p.epi;
+  const EpiPtrs ptr = epi_ptrs(e, bz);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
       if (e.read_c) {
         const int64_t off = m * e.ldc + nb;
         if (full && e.vec_c && e.c_dtype == GEMM_F32) {
-          float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(e.C) + off);
+          float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(ptr.C) + off);
           if (e.c_relu) {
             c.x = fmaxf(c.x, 0.0f); c.y = fmaxf(c.y, 0.0f); c.z = fmaxf(c.z, 0.0f); c.w = fmaxf(c.w, 0.0f);
           }
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             if (nb + j < p.N) {
-              float c = load_as_float(e.C, e.c_dtype, off + j);
+              float c = load_as_float(ptr.C, e.c_dtype, off + j);
               if (e.c_relu) c = fmaxf(c, 0.0f);
               x[j] = fmaf(e.beta, c, x[j]);
             }
@@ -180,9 +182,9 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
       if (e.bias_mode == GEMM_BIAS_COL) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (nb + j < p.N) x[j] += load_as_float(e.bias, e.bias_dtype, nb + j);
+          if (nb + j < p.N) x[j] += load_as_float(ptr.bias, e.bias_dtype, nb + j);
       } else if (e.bias_mode == GEMM_BIAS_ROW) {
-        const float b = load_as_float(e.bias, e.bias_dtype, m);
+        const float b = load_as_float(ptr.bias, e.bias_dtype, m);
 #pragma unroll
         for (int j = 0; j < 4; ++j) x[j] += b;
       }
@@ -192,11 +194,11 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
       }
       const int64_t doff = m * e.ldd + nb;
       if (full && e.vec_d && e.d_dtype == GEMM_F32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(e.D) + doff) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(static_cast<float*>(ptr.D) + doff) = make_float4(x[0], x[1], x[2], x[3]);
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (nb + j < p.N) store_float_as(e.D, e.d_dtype, doff + j, x[j]);
+          if (nb + j < p.N) store_float_as(ptr.D, e.d_dtype, doff + j, x[j]);
       }
     }
   }
@@ -219,6 +221,9 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
   __shared__ Acc As[GT][GT + 1];
   __shared__ Acc Bs[GT][GT + 1];
   const int tx = threadIdx.x, ty = threadIdx.y;
+  const int64_t bz = blockIdx.y;                      // problem of the batch
+  const void* Ab = static_cast<const char*>(p.A) + bz * p.stride_a * dtype_bytes(p.ab_dtype);
+  const void* Bb = static_cast<const char*>(p.B) + bz * p.stride_b * dtype_bytes(p.ab_dtype);
   const int64_t tiles_n = (p.N + GT - 1) / GT;
   const int64_t bm = (int64_t)blockIdx.x / tiles_n, bn = (int64_t)blockIdx.x % tiles_n;
   const int64_t i = bm * GT + ty;
@@ -229,15 +234,15 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
       const int64_t ai = bm * GT + ty, ak = k0 + tx;
       Acc v = 0;
       if (ai < p.M && ak < p.K) {
-        if constexpr (IS_INT) v = load_as_int(p.A, p.ab_dtype, a_index(p, ai, ak));
-        else v = load_as_float(p.A, p.ab_dtype, a_index(p, ai, ak));
+        if constexpr (IS_INT) v = load_as_int(Ab, p.ab_dtype, a_index(p, ai, ak));
+        else v = load_as_float(Ab, p.ab_dtype, a_index(p, ai, ak));
       }
       As[ty][tx] = v;
       const int64_t bk = k0 + ty, bj = bn * GT + tx;
       Acc w = 0;
       if (bk < p.K && bj < p.N) {
-        if constexpr (IS_INT) w = load_as_int(p.B, p.ab_dtype, b_index(p, bk, bj));
-        else w = load_as_float(p.B, p.ab_dtype, b_index(p, bk, bj));
+        if constexpr (IS_INT) w = load_as_int(Bb, p.ab_dtype, b_index(p, bk, bj));
+        else w = load_as_float(Bb, p.ab_dtype, b_index(p, bk, bj));
       }
       Bs[ty][tx] = w;
     }
@@ -251,28 +256,29 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
   }
   if (i >= p.M || j >= p.N) return;
   const EpiParams& e = p.epi;
+  const EpiPtrs ptr = epi_ptrs(e, bz);
   if constexpr (IS_INT) {
     int32_t v = wrap_madd(e.alpha_i, acc, 0);
     if (e.read_c) {
-      int32_t c = load_as_int(e.C, GEMM_S32, i * e.ldc + j);
+      int32_t c = load_as_int(ptr.C, GEMM_S32, i * e.ldc + j);
       if (e.c_relu) c = c > 0 ? c : 0;
       v = wrap_madd(e.beta_i, c, v);
     }
-    if (e.bias_mode == GEMM_BIAS_COL) v = wrap_madd(1, load_as_int(e.bias, GEMM_S32, j), v);
-    else if (e.bias_mode == GEMM_BIAS_ROW) v = wrap_madd(1, load_as_int(e.bias, GEMM_S32, i), v);
+    if (e.bias_mode == GEMM_BIAS_COL) v = wrap_madd(1, load_as_int(ptr.bias, GEMM_S32, j), v);
+    else if (e.bias_mode == GEMM_BIAS_ROW) v = wrap_madd(1, load_as_int(ptr.bias, GEMM_S32, i), v);
     if (e.relu) v = v > 0 ? v : 0;
-    static_cast<int32_t*>(e.D)[i * e.ldd + j] = v;
+    static_cast<int32_t*>(ptr.D)[i * e.ldd + j] = v;
   } else {
     float v = acc * e.alpha;
     if (e.read_c) {
-      float c = load_as_float(e.C, e.c_dtype, i * e.ldc + j);
+      float c = load_as_float(ptr.C, e.c_dtype, i * e.ldc + j);
       if (e.c_relu) c = fmaxf(c, 0.0f);
       v = fmaf(e.beta, c, v);
     }
-    if (e.bias_mode == GEMM_BIAS_COL) v += load_as_float(e.bias, e.bias_dtype, j);
-    else if (e.bias_mode == GEMM_BIAS_ROW) v += load_as_float(e.bias, e.bias_dtype, i);
+    if (e.bias_mode == GEMM_BIAS_COL) v += load_as_float(ptr.bias, e.bias_dtype, j);
+    else if (e.bias_mode == GEMM_BIAS_ROW) v += load_as_float(ptr.bias, e.bias_dtype, i);
     if (e.relu) v = fmaxf(v, 0.0f);
-    store_float_as(e.D, e.d_dtype, i * e.ldd + j, v);
+    store_float_as(ptr.D, e.d_dtype, i * e.ldd + j, v);
   }
 }
 
@@ -309,10 +315,10 @@ __global__ void s8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restr
 
 }  // namespace
 
-cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, cudaStream_t stream) {
+cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, int batch, cudaStream_t stream) {
   const int64_t tiles = ((p.N + FFMA_BN - 1) / FFMA_BN) * ((p.M + FFMA_BM - 1) / FFMA_BM);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)tiles);
+  if (tiles > 0x7fffffffLL || batch < 1 || batch > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)tiles, (unsigned)batch);
   // A row-major (T) is K-contiguous; B column-major (N) is K-contiguous.
   const bool ak = a_row_major != 0, bk = b_row_major == 0;
   if (ak && bk) ffma_sgemm_kernel<true, true><<<grid, SG_THREADS, 0, stream>>>(p);
@@ -322,11 +328,11 @@ cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) {
+cudaError_t launch_simt(const SimtParams& p, int batch, cudaStream_t stream) {
   const dim3 block(GT, GT);
   const int64_t tiles = ((p.N + GT - 1) / GT) * ((p.M + GT - 1) / GT);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)tiles);
+  if (tiles > 0x7fffffffLL || batch < 1 || batch > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)tiles, (unsigned)batch);
   if (p.ab_dtype == GEMM_S8) simt_gemm_kernel<true><<<grid, block, 0, stream>>>(p);
   else simt_gemm_kernel<false><<<grid, block, 0, stream>>>(p);
   return cudaGetLastError();

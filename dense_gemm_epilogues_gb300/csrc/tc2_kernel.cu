@@ -48,12 +48,14 @@ constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int MN_BOX = 64;
 constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;
 
-__device__ __forceinline__ void pair_tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+__device__ __forceinline__ void pair_tile_coords(int t, const TcParams& p, int& bz, int& tm, int& tn) {
+  bz = t / p.tiles_per_batch;                     // problem of the batch
+  const int tl = t - bz * p.tiles_per_batch;
   const int group_tiles = p.raster * p.tiles_n;
-  const int g = t / group_tiles;
+  const int g = tl / group_tiles;
   const int first_m = g * p.raster;
   const int gsize = min(p.tiles_m - first_m, p.raster);
-  const int r = t - g * group_tiles;
+  const int r = tl - g * group_tiles;
   tm = first_m + r % gsize;
   tn = r / gsize;
 }
@@ -135,10 +137,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
       int tile, kb0, kb1;
       while (ok && it.next(tile, kb0, kb1)) {
-        int tm, tn;
-        pair_tile_coords(tile, p, tm, tn);
+        int bz, tm, tn;
+        pair_tile_coords(tile, p, bz, tm, tn);
         const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
         const int n0 = tn * PAIR_BN + (int)rank * (PAIR_BN / 2);    // this CTA's half of B
+        const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
@@ -150,16 +153,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           if (p.a_mn_major) {
 #pragma unroll
             for (int h = 0; h < TC_BM / MN_BOX; ++h)
-              tma_load_2d_pair(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, fb);
+              tma_load_3d_pair(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, za, fb);
           } else {
-            tma_load_2d_pair(sa, &p.tmA, k0, m0, fb);
+            tma_load_3d_pair(sa, &p.tmA, k0, m0, za, fb);
           }
           if (p.b_mn_major) {
 #pragma unroll
             for (int h = 0; h < (PAIR_BN / 2) / MN_BOX; ++h)
-              tma_load_2d_pair(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, fb);
+              tma_load_3d_pair(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
           } else {
-            tma_load_2d_pair(sb, &p.tmB, k0, n0, fb);
+            tma_load_3d_pair(sb, &p.tmB, k0, n0, zb, fb);
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -230,12 +233,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
     SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
     int tile, kb0, kb1;
     while (ok && it.next(tile, kb0, kb1)) {
-      int tm, tn;
-      pair_tile_coords(tile, p, tm, tn);
+      int bz, tm, tn;
+      pair_tile_coords(tile, p, bz, tm, tn);
       const int row_in_cta = q * 32 + lane;
       const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + row_in_cta;
       const int64_t n0 = (int64_t)tn * PAIR_BN;
       const bool row_ok = m < p.M;
+      const EpiPtrs ptr = epi_ptrs(p.epi, bz);
       if constexpr (INT_MODE) {
         const int half = (warp - 2) >> 2;                     // columns 128*half ... 128*half + 127
         const int units = (kb1 - kb0 + kb_per_unit - 1) / kb_per_unit;
@@ -267,7 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
         if (!ok) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          epi_finish_row32_int(p.epi, m, row_ok, n0 + half * 128 + c * 32, p.N, &acc[c * 32]);
+          epi_finish_row32_int(p.epi, ptr, m, row_ok, n0 + half * 128 + c * 32, p.N, &acc[c * 32]);
       } else {
         const int buf = (int)(acc_it % PAIR_ACC_BUFS);
         const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
@@ -358,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] *= p.epi.alpha;
-            epi_finish_row32_float(p.epi, m, row_ok, n0 + c * 32, p.N, x);
+            epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x);
           }
           tc_fence_before();
           __syncwarp();

@@ -54,12 +54,14 @@ constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;   // 8 KiB
 // Tile t -> (tile row, tile column), in groups of `raster` tile rows so that
 // CTAs running at the same time share A row panels and B column panels in L2
 // (the block rasterisation of the CUTLASS page's policy).
-__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& bz, int& tm, int& tn) {
+  bz = t / p.tiles_per_batch;                     // problem of the batch
+  const int tl = t - bz * p.tiles_per_batch;
   const int group_tiles = p.raster * p.tiles_n;
-  const int g = t / group_tiles;
+  const int g = tl / group_tiles;
   const int first_m = g * p.raster;
   const int gsize = min(p.tiles_m - first_m, p.raster);
-  const int r = t - g * group_tiles;
+  const int r = tl - g * group_tiles;
   tm = first_m + r % gsize;
   tn = r / gsize;
 }
@@ -137,9 +139,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       uint32_t phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        int tm, tn;
-        tile_coords(t, p, tm, tn);
+        int bz, tm, tn;
+        tile_coords(t, p, bz, tm, tn);
         const int m0 = tm * TC_BM, n0 = tn * BN;
+        const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
@@ -150,16 +153,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           if (p.a_mn_major) {
 #pragma unroll
             for (int h = 0; h < TC_BM / MN_BOX; ++h)
-              tma_load_2d(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, fb);
+              tma_load_3d(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, za, fb);
           } else {
-            tma_load_2d(sa, &p.tmA, k0, m0, fb);
+            tma_load_3d(sa, &p.tmA, k0, m0, za, fb);
           }
           if (p.b_mn_major) {
 #pragma unroll
             for (int h = 0; h < BN / MN_BOX; ++h)
-              tma_load_2d(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, fb);
+              tma_load_3d(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
           } else {
-            tma_load_2d(sb, &p.tmB, k0, n0, fb);
+            tma_load_3d(sb, &p.tmB, k0, n0, zb, fb);
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -219,11 +222,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     uint32_t acc_it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      int tm, tn;
-      tile_coords(t, p, tm, tn);
+      int bz, tm, tn;
+      tile_coords(t, p, bz, tm, tn);
       const int64_t m = (int64_t)tm * TC_BM + q * 32 + lane;
       const int64_t n0 = (int64_t)tn * BN;
       const bool row_ok = m < p.M;
+      const EpiPtrs ptr = epi_ptrs(p.epi, bz);
       if constexpr (INT_MODE) {
         int32_t acc[BN];
 #pragma unroll
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         }
         if (!ok) break;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) epi_finish_row32_int(p.epi, m, row_ok, n0 + c * 32, p.N, &acc[c * 32]);
+        for (int c = 0; c < BN / 32; ++c) epi_finish_row32_int(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, &acc[c * 32]);
       } else {
         const int buf = (int)(acc_it % Cfg::ACC_BUFS);
         const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           float x[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
-          epi_finish_row32_float(p.epi, m, row_ok, n0 + c * 32, p.N, x);
+          epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x);
         }
         tc_fence_before();
         __syncwarp();

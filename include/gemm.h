@@ -173,6 +173,32 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t layoutA, gemm_layout_t la
                        const gemm_epilogue_t* epi, gemm_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gemm_run_strided_batched -- `batch` independent problems in one call:
+ *     D_z = epilogue(alpha * op(A_z) * op(B_z) + beta * C_z),  z = 0 .. batch-1,
+ * with X_z = X + z * stride_x (element strides) for A, B, C, D and the bias.
+ * The batched GEMMs named among the motivations of "Flexible Performant GEMM
+ * Kernels on GPUs" (section 3: requirements of the tiling API; section 4.1:
+ * GEMM-based tensor contractions), run by the same kernels with the problem
+ * index as an outer tile coordinate (TMA tensor maps with a third dimension).
+ *   Arguments of one problem mean what they mean for gemm_run.
+ *   stride_a, stride_b, stride_c, stride_bias  >= 0; 0 shares one operand
+ *               (or bias vector) among all problems.
+ *   stride_d    >= (M-1)*ldd + N when batch > 1 (outputs must not overlap);
+ *               C == D requires stride_c == stride_d.
+ *   batch       >= 0 (0: nothing is launched).
+ * Strides whose byte size is not a multiple of 16, or more than 65535
+ * problems, are served by one launch per problem.  Errors as for gemm_run.
+ * ------------------------------------------------------------------------- */
+gemm_status_t gemm_run_strided_batched(gemm_plan_t plan, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                       int64_t M, int64_t N, int64_t K, double alpha,
+                                       const void* A, int64_t lda, int64_t stride_a,
+                                       const void* B, int64_t ldb, int64_t stride_b, double beta,
+                                       const void* C, int64_t ldc, int64_t stride_c,
+                                       void* D, int64_t ldd, int64_t stride_d, int64_t batch,
+                                       const gemm_epilogue_t* epi, int64_t stride_bias,
+                                       gemm_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gemm_run_host -- the same operation on HOST buffers (pinned or pageable).
  * Copies A, B, C (when beta != 0) and the bias into plan-owned device staging
  * (grown on demand), runs gemm_run on `stream`, copies D back to the host and
@@ -240,7 +266,8 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 101 (gemm_epilogue_t.c_act). */
+/* ABI version of this header (major * 100 + minor): 102 (gemm_epilogue_t.c_act,
+ * gemm_run_strided_batched). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------
