@@ -302,6 +302,8 @@ def bench_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
     if args.suite and rank == 0:
         run_suite(G, device)
+        run_batched_suite(G, device)
+        run_diag_suite(G, device)
     plan.close()
     if dist:
         dist.destroy_process_group()
@@ -524,6 +526,150 @@ def run_suite(G, device, warmup=3, iters=20):
         torch.cuda.empty_cache()
 
 
+def run_batched_suite(G, device, warmup=3, iters=20):
+    """Strided-batched workloads (one JSON line each): back-to-back calls and
+    CUDA-graph replay, as run_suite."""
+    import torch
+    peaks = load_peaks()
+    cases = [("batched_f16_tn_64x1024x1024x1024", 64, 1024, 1024, 1024, "f16", "f32"),
+             ("batched_bf16_tn_256x512x512x128", 256, 512, 512, 128, "bf16", "bf16")]
+    for name, batch, M, N, K, ab, d in cases:
+        td = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+        gen = torch.Generator().manual_seed(20261202 + 11)
+        A = (torch.rand((batch, M, K), generator=gen) * 2 - 1).to(td[ab]).to(device)
+        B = (torch.rand((batch, N, K), generator=gen) * 2 - 1).to(td[ab]).to(device)
+        D = torch.empty((batch, M, N), dtype=td[d], device=device)
+        plan = G.Plan(G.DTYPE_CODES[ab], G.GEMM_F32, device.index or 0)
+        epi = G.make_epilogue(G.DTYPE_CODES[d])
+
+        def call_on(st):
+            G.gemm_run_strided_batched(plan.handle, G.GEMM_OP_T, G.GEMM_OP_N, M, N, K, 1.0,
+                                       A.data_ptr(), K, M * K, B.data_ptr(), K, N * K, 0.0, None,
+                                       0, 0, D.data_ptr(), N, M * N, batch, epi, 0, st.cuda_stream)
+        stream = torch.cuda.current_stream(device)
+        for _ in range(warmup):
+            call_on(stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            call_on(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / iters
+        side = torch.cuda.Stream(device)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            gr.capture_begin()
+            for _ in range(iters):
+                call_on(side)
+            gr.capture_end()
+            gr.replay()
+            side.synchronize()
+            e0.record(side)
+            gr.replay()
+            e1.record(side)
+        side.synchronize()
+        tg = e0.elapsed_time(e1) / 1e3 / iters
+        flops = 2.0 * batch * M * N * K
+        eb = {"f16": 2, "bf16": 2, "f32": 4}
+        algo_bytes = batch * (M * K + N * K) * eb[ab] + batch * M * N * eb[d]
+        cfg = plan.last_config()
+        print(json.dumps({"suite": name, "batch": batch, "M": M, "N": N, "K": K,
+                          "kernel": cfg["kernel_name"], "tiles": cfg["tiles"],
+                          "median_us": round(t * 1e6, 2), "graph_us": round(tg * 1e6, 2),
+                          "tflops": round(flops / t / 1e12, 2), "tflops_graph": round(flops / tg / 1e12, 2),
+                          "gbs_graph": round(algo_bytes / tg / 1e9, 1), "algo_bytes": algo_bytes,
+                          "frac_tensor_peak": round(flops / tg / 1e12 / peaks["bf16_tflops"], 4),
+                          "frac_hbm": round(algo_bytes / tg / 1e9 / peaks["hbm_gbs"], 4),
+                          "status": plan.device_status()}), flush=True)
+        plan.close()
+        del A, B, D, gr
+        torch.cuda.empty_cache()
+
+
+def run_diag_suite(G, device, warmup=3, iters=20, sets=4):
+    """Diagonal-operand workloads (one JSON line each).  Calls rotate over
+    `sets` copies of the inputs and outputs (each copy larger than L2), so every
+    call reads its operands from HBM.  The same GEMM with the diagonal written
+    out as a dense matrix (gemm_run, tensor cores) is timed beside it."""
+    import torch
+    from dense_gemm_epilogues_gb300 import inputs as I
+    peaks = load_peaks()
+    for layout in ("N", "T"):
+        p = I.diag_fp16_4096(layout)
+        dinp = I.generate_diag(p, I.BASE_SEED + 20)
+        dg = dinp.diag.to(device)
+        Xs = [dinp.X.to(device) for _ in range(sets)]
+        Cs = [dinp.C.to(device) for _ in range(sets)]
+        Ds = [torch.empty((p.M, p.ldd), dtype=torch.float32, device=device) for _ in range(sets)]
+        plan = G.Plan(G.GEMM_F16, G.GEMM_F32, device.index or 0)
+        epi = G.make_epilogue(G.GEMM_F32)
+        side_code = G.GEMM_SIDE_LEFT if p.side == "left" else G.GEMM_SIDE_RIGHT
+
+        def diag_call(k, st):
+            G.gemm_run_diag(plan.handle, side_code, G.LAYOUT_CODES[p.layout_x], p.M, p.N, p.alpha,
+                            dg.data_ptr(), Xs[k].data_ptr(), p.ldx, p.beta, Cs[k].data_ptr(), p.ldc,
+                            Ds[k].data_ptr(), p.ldd, epi, st.cuda_stream)
+
+        sq = torch.zeros((p.M, p.M), dtype=torch.float16, device=device)
+        sq.diagonal().copy_(dg)            # symmetric, so its storage serves either layout
+        dp = p.dense()
+
+        def dense_call(k, st):
+            G.gemm_run(plan.handle, G.LAYOUT_CODES[dp.layout_a], G.LAYOUT_CODES[dp.layout_b], dp.M,
+                       dp.N, dp.K, dp.alpha, sq.data_ptr(), dp.lda, Xs[k].data_ptr(), dp.ldb,
+                       dp.beta, Cs[k].data_ptr(), dp.ldc, Ds[k].data_ptr(), dp.ldd, epi,
+                       st.cuda_stream)
+
+        def timed(call):
+            stream = torch.cuda.current_stream(device)
+            for w in range(warmup):
+                call(w % sets, stream)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for it in range(iters):
+                call(it % sets, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1e3 / iters
+            side = torch.cuda.Stream(device)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                gr.capture_begin()
+                for it in range(iters):
+                    call(it % sets, side)
+                gr.capture_end()
+                gr.replay()
+                side.synchronize()
+                e0.record(side)
+                gr.replay()
+                e1.record(side)
+            side.synchronize()
+            return t, e0.elapsed_time(e1) / 1e3 / iters
+
+        t, tg = timed(diag_call)
+        cfg = plan.last_config()
+        td, tdg = timed(dense_call)
+        dense_cfg = plan.last_config()
+        algo_bytes = p.n_diag * 2 + p.M * p.N * (2 + 4 + 4)
+        print(json.dumps({"suite": p.name, "M": p.M, "N": p.N, "side": p.side, "layout_x": p.layout_x,
+                          "kernel": cfg["kernel_name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
+                          "median_us": round(t * 1e6, 2), "graph_us": round(tg * 1e6, 2),
+                          "gbs_graph": round(algo_bytes / tg / 1e9, 1), "algo_bytes": algo_bytes,
+                          "frac_hbm": round(algo_bytes / tg / 1e9 / peaks["hbm_gbs"], 4),
+                          "dense_kernel": dense_cfg["kernel_name"], "dense_graph_us": round(tdg * 1e6, 2),
+                          "dense_median_us": round(td * 1e6, 2),
+                          "speedup_vs_dense": round(tdg / tg, 2), "rotating_sets": sets,
+                          "status": plan.device_status()}), flush=True)
+        plan.close()
+        del Xs, Cs, Ds, sq, dg
+        torch.cuda.empty_cache()
+
+
 def _cases():
     from dense_gemm_epilogues_gb300 import inputs as I
     return {
@@ -539,12 +685,43 @@ def _cases():
     }
 
 
+def run_diag_case(layout: str, iters: int):
+    """The 4096 x 4096 diagonal-operand workload `iters` times (profiling driver)."""
+    import torch
+    import dense_gemm_epilogues_gb300 as G
+    from dense_gemm_epilogues_gb300 import inputs as I
+    p = I.diag_fp16_4096(layout)
+    dinp = I.generate_diag(p, I.BASE_SEED + 20)
+    dev = torch.device("cuda", 0)
+    dg, X, C = dinp.diag.to(dev), dinp.X.to(dev), dinp.C.to(dev)
+    D = torch.empty((p.M, p.ldd), dtype=torch.float32, device=dev)
+    plan = G.Plan(G.GEMM_F16, G.GEMM_F32, 0)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(iters):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        G.gemm_run_diag(plan.handle, G.GEMM_SIDE_LEFT, G.LAYOUT_CODES[layout], p.M, p.N, p.alpha,
+                        dg.data_ptr(), X.data_ptr(), p.ldx, p.beta, C.data_ptr(), p.ldc, D.data_ptr(),
+                        p.ldd, G.make_epilogue(G.GEMM_F32), stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": p.name, "iter": i, "ms": round(e0.elapsed_time(e1), 4),
+                          "config": plan.last_config()}), flush=True)
+    if plan.device_status() != 0:
+        raise RuntimeError("device status non-zero")
+    plan.close()
+
+
 def run_case(name: str, iters: int):
     """Run one workload `iters` times on cuda:0 and print per-call times
     (a driver for profilers; its numbers are not benchmark results)."""
     import torch
     import dense_gemm_epilogues_gb300 as G
     from dense_gemm_epilogues_gb300 import inputs as I
+    if name in ("diag_n", "diag_t"):
+        run_diag_case(name[-1].upper(), iters)
+        return
     p = _cases()[name]
     inp = I.generate(p, I.BASE_SEED + 7)
     dev = torch.device("cuda", 0)

@@ -27,11 +27,12 @@ GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S8, GEMM_S32 = range(5)
 GEMM_ACT_NONE, GEMM_ACT_RELU = 0, 1
 GEMM_BIAS_NONE, GEMM_BIAS_COL, GEMM_BIAS_ROW = 0, 1, 2
 (GEMM_KERNEL_AUTO, GEMM_KERNEL_NONE, GEMM_KERNEL_TC, GEMM_KERNEL_TC_INT8, GEMM_KERNEL_FFMA,
- GEMM_KERNEL_SIMT, GEMM_KERNEL_TC_PAIR) = range(7)
+ GEMM_KERNEL_SIMT, GEMM_KERNEL_TC_PAIR, GEMM_KERNEL_DIAG) = range(8)
+GEMM_SIDE_LEFT, GEMM_SIDE_RIGHT = 0, 1
 
 KERNEL_NAMES = {GEMM_KERNEL_AUTO: "auto", GEMM_KERNEL_NONE: "none", GEMM_KERNEL_TC: "tc",
                 GEMM_KERNEL_TC_INT8: "tc_int8", GEMM_KERNEL_FFMA: "ffma", GEMM_KERNEL_SIMT: "simt",
-                GEMM_KERNEL_TC_PAIR: "tc_pair"}
+                GEMM_KERNEL_TC_PAIR: "tc_pair", GEMM_KERNEL_DIAG: "diag"}
 DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "s8": GEMM_S8, "s32": GEMM_S32}
 LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 
@@ -39,7 +40,7 @@ LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host", "gemm_validate",
             "gemm_select", "gemm_plan_set_kernel", "gemm_plan_last_config", "gemm_plan_device_status",
             "gemm_plan_set_timeout", "gemm_status_string", "gemm_abi_version",
-            "gemm_run_s8_noalloc", "gemm_run_strided_batched"]
+            "gemm_run_s8_noalloc", "gemm_run_strided_batched", "gemm_run_diag"]
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -100,6 +101,8 @@ def load_library(path: str = LIB_PATH):
                                              ctypes.POINTER(gemm_epilogue_t), i64, vp]
     lib.gemm_run_s8_noalloc.argtypes = [ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64,
                                         vp, i64, ctypes.POINTER(gemm_epilogue_t), vp, vp]
+    lib.gemm_run_diag.argtypes = [vp, ci, ci, i64, i64, dbl, vp, vp, i64, dbl, vp, i64, vp, i64,
+                                  ctypes.POINTER(gemm_epilogue_t), vp]
     for name in EXPORTED:
         if name not in ("gemm_status_string", "gemm_abi_version"):
             getattr(lib, name).restype = ci
@@ -164,6 +167,12 @@ def gemm_run_strided_batched(plan, layout_a, layout_b, M, N, K, alpha, A, lda, s
                                                    stride_c, D, ldd, stride_d, batch,
                                                    _epi_ptr(epi), stride_bias, stream),
            "gemm_run_strided_batched")
+
+
+def gemm_run_diag(plan, side, layout_x, M, N, alpha, diag, X, ldx, beta, C, ldc, D, ldd,
+                  epi: Optional[gemm_epilogue_t] = None, stream: int = 0) -> None:
+    _check(load_library().gemm_run_diag(plan, side, layout_x, M, N, alpha, diag, X, ldx, beta, C, ldc,
+                                        D, ldd, _epi_ptr(epi), stream), "gemm_run_diag")
 
 
 def gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd,

@@ -487,7 +487,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
 
 extern "C" {
 
-int gemm_abi_version(void) { return 102; }
+int gemm_abi_version(void) { return 103; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
@@ -767,6 +767,57 @@ gemm_status_t gemm_run_strided_batched(gemm_plan_t plan, gemm_layout_t la, gemm_
                  Batch());
     if (s != GEMM_OK) return s;
   }
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx, int64_t M, int64_t N,
+                            double alpha, const void* diag, const void* X, int64_t ldx, double beta,
+                            const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
+                            gemm_stream_t stream_) {
+  if (!plan || (side != GEMM_SIDE_LEFT && side != GEMM_SIDE_RIGHT)) return GEMM_ERR_INVALID_ARG;
+  const bool left = side == GEMM_SIDE_LEFT;
+  // The checks of the equivalent dense call (the diagonal as a square operand).
+  gemm_status_t s =
+      left ? validate(plan->ab, plan->c, GEMM_OP_N, lx, M, N, M, alpha, diag, std::max<int64_t>(1, M), X, ldx,
+                      beta, C, ldc, D, ldd, epi)
+           : validate(plan->ab, plan->c, lx, GEMM_OP_N, M, N, N, alpha, X, ldx, diag, std::max<int64_t>(1, N),
+                      beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  gemm_config_t cfg{};
+  cfg.split_k = 1;
+  cfg.cta_group = 1;
+  if (M == 0 || N == 0) {
+    cfg.kernel = GEMM_KERNEL_NONE;
+    plan->last = cfg;
+    return GEMM_OK;
+  }
+  DeviceGuard g(plan->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  DiagParams p{};
+  p.X = X;
+  p.diag = diag;
+  p.ldx = ldx;
+  p.M = M;
+  p.N = N;
+  p.tiles_n = (N + DIAG_TN - 1) / DIAG_TN;
+  p.num_tiles = ((M + DIAG_TM - 1) / DIAG_TM) * p.tiles_n;
+  p.ab_dtype = plan->ab;
+  p.left = left ? 1 : 0;
+  const int es = dtype_bytes(plan->ab);
+  p.vec_x = (aligned16(X) && (ldx * es) % 16 == 0) ? 1 : 0;
+  p.vec_diag = aligned16(diag) ? 1 : 0;
+  p.epi = make_epi(plan, alpha, beta, C, ldc, D, ldd, epi);
+  int grid = 0;
+  if (launch_diag(p, lx == GEMM_OP_T, plan->sm_count, &grid, reinterpret_cast<cudaStream_t>(stream_)) !=
+      cudaSuccess)
+    return GEMM_ERR_CUDA;
+  cfg.kernel = GEMM_KERNEL_DIAG;
+  cfg.bm = DIAG_TM;
+  cfg.bn = DIAG_TN;
+  cfg.stages = 1;
+  cfg.grid = grid;
+  cfg.tiles = (int32_t)std::min<int64_t>(p.num_tiles, kMaxDim);
+  plan->last = cfg;
   return GEMM_OK;
 }
 

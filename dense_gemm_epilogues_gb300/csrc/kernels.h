@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace gemmlib {
@@ -79,6 +81,25 @@ struct SimtParams {
 };
 cudaError_t launch_simt(const SimtParams& p, int batch, cudaStream_t stream);
 inline cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) { return launch_simt(p, 1, stream); }
+
+// GEMM with one diagonal operand: D = epilogue(alpha * diag(d) * x + beta * C)
+// (left) or epilogue(alpha * x * diag(d) + beta * C) (right), x the dense
+// operand seen as an M x N matrix.  One product per output, no tensor cores.
+struct DiagParams {
+  const void* X;          // dense operand, ab_dtype, row-major (layout T) or column-major (N)
+  const void* diag;       // the diagonal: M entries (left) or N entries (right), ab_dtype
+  int64_t ldx;
+  int64_t M, N;
+  int64_t tiles_n, num_tiles;   // DIAG_TM x DIAG_TN tiles of D
+  int32_t ab_dtype;
+  int32_t left;           // 1: d[i] scales row i (A = diag(d)); 0: d[j] scales column j (B = diag(d))
+  int32_t vec_x;          // x may be read as aligned 8-element vectors along its contiguous dimension
+  int32_t vec_diag;       // the diagonal may be read as aligned 8-element vectors
+  EpiParams epi;
+};
+constexpr int DIAG_TM = 64, DIAG_TN = 64;
+// Persistent launch: min(tiles, sm_count x resident CTAs per SM) CTAs; the grid used goes to *grid_out.
+cudaError_t launch_diag(const DiagParams& p, int x_row_major, int sm_count, int* grid_out, cudaStream_t stream);
 
 // int8 -> fp16 staging copy of a strided matrix: dst[r*ld + c] = src[r*ld + c]
 // for r < outer, c < inner.

@@ -157,6 +157,91 @@ def generate(p: Problem, seed: int, keep_logical: bool = False) -> Inputs:
     return Inputs(A=A, B=B, C=C, bias=bias, problem=p, logical=logical)
 
 
+@dataclass(frozen=True)
+class DiagProblem:
+    """A GEMM whose A (side 'left': A = diag(d), M x M) or B (side 'right':
+    B = diag(d), N x N) is a diagonal matrix stored as its diagonal d alone.
+    The other operand, x, is dense and seen as an M x N matrix stored in
+    layout_x ('N' column-major, 'T' row-major) with leading dimension ldx."""
+    name: str
+    ab: str
+    side: str                    # 'left' | 'right'
+    layout_x: str
+    M: int
+    N: int
+    alpha: float = 1.0
+    beta: float = 0.0
+    c: Optional[str] = None
+    d: str = "f32"
+    bias: Optional[str] = None
+    bias_mode: str = "none"
+    act: str = "none"
+    c_act: str = "none"
+    dist_diag: Dist = U11
+    dist_x: Dist = U11
+    dist_c: Dist = Dist("normal", std=1.0)
+    dist_bias: Dist = Dist("normal", std=0.1)
+    pad_x: int = 0
+    pad_c: int = 0
+    pad_d: int = 0
+
+    @property
+    def n_diag(self) -> int:
+        return self.M if self.side == "left" else self.N
+
+    @property
+    def ldx(self) -> int:
+        return (self.M if self.layout_x == "N" else self.N) + self.pad_x
+
+    @property
+    def ldc(self) -> int:
+        return self.N + self.pad_c
+
+    @property
+    def ldd(self) -> int:
+        return self.N + self.pad_d
+
+    def dense(self) -> Problem:
+        """The same GEMM with the diagonal as a square dense operand (stored
+        column-major, leading dimension = its size): x is B (left) or A (right)."""
+        common = dict(alpha=self.alpha, beta=self.beta, c=self.c, d=self.d, bias=self.bias,
+                      bias_mode=self.bias_mode, act=self.act, c_act=self.c_act,
+                      dist_c=self.dist_c, dist_bias=self.dist_bias, pad_c=self.pad_c,
+                      pad_d=self.pad_d)
+        if self.side == "left":
+            return Problem(self.name, self.ab, "N", self.layout_x, self.M, self.N, self.M,
+                           pad_b=self.pad_x, **common)
+        return Problem(self.name, self.ab, self.layout_x, "N", self.M, self.N, self.N,
+                       pad_a=self.pad_x, **common)
+
+    def with_(self, **kw) -> "DiagProblem":
+        return replace(self, **kw)
+
+
+@dataclass
+class DiagInputs:
+    diag: torch.Tensor             # the n_diag diagonal entries (host)
+    X: torch.Tensor                # storage of the dense operand (host)
+    C: Optional[torch.Tensor]
+    bias: Optional[torch.Tensor]
+    problem: DiagProblem
+    x_logical: Optional[torch.Tensor] = None
+
+
+def generate_diag(p: DiagProblem, seed: int) -> DiagInputs:
+    """Draw d, then x (logical M x N, row-major order), then C, then the bias."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    dg = _draw(gen, 1, p.n_diag, p.dist_diag, p.ab).reshape(p.n_diag)
+    x = _draw(gen, p.M, p.N, p.dist_x, p.ab)
+    c = _draw(gen, p.M, p.N, p.dist_c, p.c) if p.c is not None else None
+    nb = p.N if p.bias_mode == "col" else p.M
+    bias = _draw(gen, 1, nb, p.dist_bias, p.bias).reshape(nb) if p.bias_mode != "none" else None
+    X = _store(x, p.layout_x, p.ldx, p.ab)
+    C = _store(c, "T", p.ldc, p.c) if c is not None else None
+    return DiagInputs(diag=dg, X=X, C=C, bias=bias, problem=p, x_logical=x)
+
+
 def sha256_of(t: torch.Tensor) -> str:
     import hashlib
     return hashlib.sha256(t.contiguous().view(torch.uint8).numpy().tobytes()).hexdigest()
@@ -205,3 +290,11 @@ def square_fp16(n: int) -> Problem:
 
 def skinny_fp16_16384x64x16384() -> Problem:
     return Problem("gemm_f16_tn_skinny_16384x64x16384", "f16", "T", "N", 16384, 64, 16384)
+
+
+def diag_fp16_4096(layout_x: str = "N") -> DiagProblem:
+    """A = diag(d) (4096 fp16 entries in U[-1,1]) times a dense 4096 x 4096 fp16
+    B in U[-1,1], plus an fp32 C ~ N(0,1): D = A*B + C in fp32 (the mixed
+    precision diagonal GEMM at N = 4096)."""
+    return DiagProblem(f"diag_f16_left_{layout_x.lower()}_4096", "f16", "left", layout_x, 4096, 4096,
+                       beta=1.0, c="f32", d="f32")

@@ -99,7 +99,8 @@ typedef enum {
     GEMM_KERNEL_TC_INT8 = 3,/* int8 exact: int8->fp16 staging, tcgen05 in 1024-deep K-chunks, int32 accumulation */
     GEMM_KERNEL_FFMA = 4,   /* fp32 SGEMM on CUDA cores, register-blocked FFMA */
     GEMM_KERNEL_SIMT = 5,   /* generic CUDA-core kernel: any alignment, K == 0, every dtype */
-    GEMM_KERNEL_TC_PAIR = 6 /* tcgen05 on CTA pairs (cta_group::2), 256x256 tiles, fp16/bf16 */
+    GEMM_KERNEL_TC_PAIR = 6,/* tcgen05 on CTA pairs (cta_group::2), 256x256 tiles, fp16/bf16 */
+    GEMM_KERNEL_DIAG = 7    /* gemm_run_diag: one product per output (reported, never forced) */
 } gemm_kernel_t;
 
 /* A launch configuration (what the selector returns; what a run used). */
@@ -199,6 +200,38 @@ gemm_status_t gemm_run_strided_batched(gemm_plan_t plan, gemm_layout_t layoutA, 
                                        gemm_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gemm_run_diag -- GEMM with one diagonal operand, stored as its diagonal only:
+ *     side GEMM_SIDE_LEFT:   D = epilogue(alpha * diag(d) * op(X) + beta * C)
+ *                            (A = diag(d) is M x M, K = M, X plays B: M x N)
+ *     side GEMM_SIDE_RIGHT:  D = epilogue(alpha * op(X) * diag(d) + beta * C)
+ *                            (B = diag(d) is N x N, K = N, X plays A: M x N)
+ * The diagonal-matrix GEMM of "Flexible Performant GEMM Kernels on GPUs",
+ * section 5.2 (Table 1): a layout that yields zero off the diagonal without a
+ * memory access, and a predicate that skips the inner-loop steps on those
+ * zeros.  Together they leave one product per output, d[i]*x(i,j) (left) or
+ * x(i,j)*d[j] (right), which the library computes directly (no tensor cores);
+ * the result equals gemm_run on the materialised diagonal matrix.
+ *   plan      any plan; its ab_dtype is the type of d and X, its c_dtype that of C.
+ *   side      gemm_side_t.
+ *   layoutX   GEMM_OP_N: X column-major, x(i,j) at X[i + j*ldx], ldx >= M;
+ *             GEMM_OP_T: X row-major,    x(i,j) at X[i*ldx + j], ldx >= N.
+ *   diag      device pointer to M (left) or N (right) contiguous entries.
+ *   Other arguments mean what they mean for gemm_run (alpha, beta, C, D, the
+ *   epilogue; S8 plans: integral alpha/beta, int32 arithmetic, exact).
+ * Device pointers stay owned by the caller; nothing is allocated.
+ * Errors: those of gemm_run for the equivalent dense call, plus
+ * GEMM_ERR_INVALID_ARG for an unknown side.  gemm_plan_last_config reports
+ * kernel GEMM_KERNEL_DIAG, the 64 x 64 output tile and the grid.
+ * ------------------------------------------------------------------------- */
+typedef enum { GEMM_SIDE_LEFT = 0 /* A = diag(d) */, GEMM_SIDE_RIGHT = 1 /* B = diag(d) */ } gemm_side_t;
+
+gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t layoutX,
+                            int64_t M, int64_t N, double alpha, const void* diag,
+                            const void* X, int64_t ldx, double beta,
+                            const void* C, int64_t ldc, void* D, int64_t ldd,
+                            const gemm_epilogue_t* epi, gemm_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gemm_run_host -- the same operation on HOST buffers (pinned or pageable).
  * Copies A, B, C (when beta != 0) and the bias into plan-owned device staging
  * (grown on demand), runs gemm_run on `stream`, copies D back to the host and
@@ -266,8 +299,8 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 102 (gemm_epilogue_t.c_act,
- * gemm_run_strided_batched). */
+/* ABI version of this header (major * 100 + minor): 103 (gemm_epilogue_t.c_act,
+ * gemm_run_strided_batched, gemm_run_diag). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------

@@ -172,3 +172,70 @@ def tma_aligned(p: I.Problem, mult: int = 8) -> I.Problem:
     ra = (p.M if p.layout_a == "N" else p.K)
     rb = (p.K if p.layout_b == "N" else p.N)
     return p.with_(pad_a=p.pad_a + (-(ra + p.pad_a)) % mult, pad_b=p.pad_b + (-(rb + p.pad_b)) % mult)
+
+
+# ------------------------- diagonal-operand GEMM -----------------------------
+
+def dense_inputs_of(dinp: I.DiagInputs) -> I.Inputs:
+    """The oracle's view of a diagonal-operand problem: the diagonal written out
+    as a square dense matrix (zeros off the diagonal), x as the other operand."""
+    p = dinp.problem
+    dp = p.dense()
+    n = p.n_diag
+    square = torch.zeros((n, n), dtype=dinp.diag.dtype)
+    idx = torch.arange(n)
+    square[idx, idx] = dinp.diag
+    sq = I._store(square, "N", n, p.ab)
+    if p.side == "left":
+        return I.Inputs(A=sq, B=dinp.X, C=dinp.C, bias=dinp.bias, problem=dp)
+    return I.Inputs(A=dinp.X, B=sq, C=dinp.C, bias=dinp.bias, problem=dp)
+
+
+class DeviceDiag:
+    """Device copies of a diagonal-operand problem, plus a guarded output."""
+
+    def __init__(self, dinp: I.DiagInputs, device="cuda"):
+        p = dinp.problem
+        self.inp, self.p = dinp, p
+        self.diag = dinp.diag.to(device)
+        self.X = dinp.X.to(device)
+        self.C = dinp.C.to(device) if dinp.C is not None else None
+        self.bias = dinp.bias.to(device) if dinp.bias is not None else None
+        rows = p.M + 2 * GUARD_ROWS
+        self.Dbuf = torch.full((rows, p.ldd), SENTINEL[p.d], dtype=I.TORCH_DTYPES[p.d], device=device)
+        self.D = self.Dbuf[GUARD_ROWS:GUARD_ROWS + p.M]
+
+    def epilogue(self) -> G.gemm_epilogue_t:
+        p = self.p
+        return G.make_epilogue(G.DTYPE_CODES[p.d],
+                               self.bias.data_ptr() if self.bias is not None else 0,
+                               G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
+                               G_BIAS[p.bias_mode],
+                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE,
+                               G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE)
+
+    def run(self, plan: G.Plan, stream=None, C=None, D=None):
+        p = self.p
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        C = self.C if C is None else C
+        D = self.D if D is None else D
+        G.gemm_run_diag(plan.handle, G.GEMM_SIDE_LEFT if p.side == "left" else G.GEMM_SIDE_RIGHT,
+                        G.LAYOUT_CODES[p.layout_x], p.M, p.N, p.alpha, self.diag.data_ptr(),
+                        self.X.data_ptr(), p.ldx, p.beta, C.data_ptr() if C is not None else None,
+                        p.ldc if p.c else 0, D.data_ptr(), p.ldd, self.epilogue(), stream)
+
+    def check_guards(self):
+        p = self.p
+        s = torch.tensor(SENTINEL[p.d], dtype=I.TORCH_DTYPES[p.d])
+        for name, t in (("rows before D", self.Dbuf[:GUARD_ROWS]),
+                        ("rows after D", self.Dbuf[GUARD_ROWS + p.M:]), ("padding of D", self.D[:, p.N:])):
+            assert torch.all(t.cpu() == s), f"kernel wrote into the {name}"
+
+    def result(self) -> torch.Tensor:
+        return self.D[:, :self.p.N]
+
+
+def make_diag_plan(p: I.DiagProblem) -> G.Plan:
+    c = p.c if p.c else ("s32" if p.ab == "s8" else "f32")
+    return G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[c], torch.cuda.current_device())

@@ -242,6 +242,33 @@ def test_diagonal_operand():
     np.testing.assert_array_equal(D, expect)
 
 
+def test_diagonal_operand_right():
+    """B = diag(d) gives D[i,j] = a(i,j) * d_j (section 5.2 with the diagonal on
+    the right): column j of A scaled by d_j, in both layouts of A."""
+    M, n = 9, 13
+    d = torch.linspace(-1.5, 2.5, n, dtype=torch.float32)
+    for la in ("N", "T"):
+        p = I.Problem("diag_r", "f32", la, "N", M, n, n, dist_b=I.Dist("zeros"))
+        inp = I.generate(p, 11, keep_logical=True)
+        inp.B = I._store(torch.diag(d), "N", n, "f32")
+        D, _ = run_oracle(inp)
+        expect = (inp.logical["a"].double() * d.double()[None, :]).float().numpy()
+        np.testing.assert_array_equal(D, expect)
+
+
+def test_diagonal_operand_int8_with_c():
+    """int8, A = diag(d): D = alpha*d_i*b(i,j) + beta*C[i,j], exact in int32."""
+    n, N = 12, 7
+    p = I.Problem("diag_i8", "s8", "N", "T", n, N, n, alpha=3.0, beta=-2.0, c="s32", d="s32",
+                  dist_a=I.Dist("zeros"), dist_b=I.I8, dist_c=I.Dist("int", -1000, 1000))
+    inp = I.generate(p, 12, keep_logical=True)
+    d = torch.arange(-6, 6, dtype=torch.int64) * 21          # -126 .. 105
+    inp.A = I._store(torch.diag(d).to(torch.int8), "N", n, "s8")
+    D, _ = run_oracle(inp)
+    expect = 3 * d[:, None] * inp.logical["b"].long() - 2 * inp.logical["c"].long()
+    np.testing.assert_array_equal(D, expect.numpy().astype(np.int32))
+
+
 def test_epilogue_only_when_A_is_zero():
     """A = 0: D = cast(beta*C + bias) and ReLU output is non-negative."""
     p = I.Problem("epi", "bf16", "T", "N", 10, 12, 8, beta=0.5, c="f32", d="bf16",
