@@ -242,6 +242,104 @@ def generate_diag(p: DiagProblem, seed: int) -> DiagInputs:
     return DiagInputs(diag=dg, X=X, C=C, bias=bias, problem=p, x_logical=x)
 
 
+@dataclass(frozen=True)
+class PairProblem:
+    """A GEMM over complex numbers (unit 'complex': x + y i, i*i = -1) or dual
+    numbers (unit 'dual': x + y eps, eps*eps = 0).  Every matrix is stored
+    interleaved: the pair of the element at storage offset e (in pairs) sits at
+    scalar positions 2e (real part) and 2e + 1 (unit part).  Sizes and leading
+    dimensions count pairs; alpha and beta are real."""
+    name: str
+    unit: str                    # 'complex' | 'dual'
+    ab: str
+    layout_a: str
+    layout_b: str
+    M: int
+    N: int
+    K: int
+    alpha: float = 1.0
+    beta: float = 0.0
+    c: Optional[str] = None
+    d: str = "f32"
+    bias: Optional[str] = None
+    bias_mode: str = "none"
+    act: str = "none"
+    c_act: str = "none"
+    dist_a: Dist = U11
+    dist_b: Dist = U11
+    dist_c: Dist = Dist("normal", std=1.0)
+    dist_bias: Dist = Dist("normal", std=0.1)
+    pad_a: int = 0
+    pad_b: int = 0
+    pad_c: int = 0
+    pad_d: int = 0
+
+    @property
+    def flops(self) -> float:
+        """Real operations of the definition: 8 per complex multiply-add
+        (4 multiplies, 4 adds), 6 per dual one (a c, a d + b c)."""
+        return (8.0 if self.unit == "complex" else 6.0) * self.M * self.N * self.K
+
+    @property
+    def lda(self) -> int:
+        return (self.M if self.layout_a == "N" else self.K) + self.pad_a
+
+    @property
+    def ldb(self) -> int:
+        return (self.K if self.layout_b == "N" else self.N) + self.pad_b
+
+    @property
+    def ldc(self) -> int:
+        return self.N + self.pad_c
+
+    @property
+    def ldd(self) -> int:
+        return self.N + self.pad_d
+
+    def with_(self, **kw) -> "PairProblem":
+        return replace(self, **kw)
+
+
+@dataclass
+class PairInputs:
+    A: torch.Tensor                # storage, shape (outer, ld, 2), host
+    B: torch.Tensor
+    C: Optional[torch.Tensor]      # (M, ldc, 2)
+    bias: Optional[torch.Tensor]   # (n, 2)
+    problem: PairProblem
+    logical: dict = field(default_factory=dict)   # 'a', 'b', 'c': (rows, cols, 2)
+
+
+def _store_pairs(logical: torch.Tensor, layout: str, ld: int, dtype: str) -> torch.Tensor:
+    """Write a logical (rows x cols) matrix of pairs, shape (rows, cols, 2), into
+    interleaved column- ('N') or row-major ('T') storage, shape (outer, ld, 2)."""
+    rows, cols, _ = logical.shape
+    if layout == "T":
+        st = torch.full((rows, ld, 2), _poison(dtype), dtype=TORCH_DTYPES[dtype])
+        st[:, :cols] = logical
+    else:
+        st = torch.full((cols, ld, 2), _poison(dtype), dtype=TORCH_DTYPES[dtype])
+        st[:, :rows] = logical.transpose(0, 1)
+    return st.contiguous()
+
+
+def generate_pairs(p: PairProblem, seed: int) -> PairInputs:
+    """Draw A, B, C, bias (each as real and unit parts of every element, in
+    logical row-major order of the elements), then lay them out interleaved."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    a = _draw(gen, p.M, 2 * p.K, p.dist_a, p.ab).reshape(p.M, p.K, 2)
+    b = _draw(gen, p.K, 2 * p.N, p.dist_b, p.ab).reshape(p.K, p.N, 2)
+    c = _draw(gen, p.M, 2 * p.N, p.dist_c, p.c).reshape(p.M, p.N, 2) if p.c is not None else None
+    nb = p.N if p.bias_mode == "col" else p.M
+    bias = (_draw(gen, 1, 2 * nb, p.dist_bias, p.bias).reshape(nb, 2)
+            if p.bias_mode != "none" else None)
+    A = _store_pairs(a, p.layout_a, p.lda, p.ab)
+    B = _store_pairs(b, p.layout_b, p.ldb, p.ab)
+    C = _store_pairs(c, "T", p.ldc, p.c) if c is not None else None
+    return PairInputs(A=A, B=B, C=C, bias=bias, problem=p, logical={"a": a, "b": b, "c": c})
+
+
 def sha256_of(t: torch.Tensor) -> str:
     import hashlib
     return hashlib.sha256(t.contiguous().view(torch.uint8).numpy().tobytes()).hexdigest()
@@ -298,3 +396,10 @@ def diag_fp16_4096(layout_x: str = "N") -> DiagProblem:
     precision diagonal GEMM at N = 4096)."""
     return DiagProblem(f"diag_f16_left_{layout_x.lower()}_4096", "f16", "left", layout_x, 4096, 4096,
                        beta=1.0, c="f32", d="f32")
+
+
+def pair_fp16_4096(unit: str) -> PairProblem:
+    """Complex or dual GEMM D = A*B + C, M = N = K = 4096, fp16 A and B (both
+    parts in U[-1,1]), fp32 C ~ N(0,1) and D, A and B column-major (N)."""
+    return PairProblem(f"{'cgemm' if unit == 'complex' else 'dual_gemm'}_f16_nn_4096", unit, "f16",
+                       "N", "N", 4096, 4096, 4096, beta=1.0, c="f32", d="f32")

@@ -9,7 +9,9 @@ What it computes (see the header of ``oracle.c`` for the passages it follows):
 
     D[i,j] = cast_out(act(alpha * sum_k a(i,k) b(k,j) + beta * C[i,j] + bias))
 
-with fp64 accumulation for floating inputs, int64 for int8 inputs.
+with fp64 accumulation for floating inputs, int64 for int8 inputs; and the same
+GEMM over complex or dual numbers stored interleaved (``gemm_pairs``: the
+section 5.4 variants of "Flexible Performant GEMM Kernels on GPUs").
 
 Every function here is marshalling only: pointers, sizes and type codes go to
 the C routines unchanged.
@@ -33,6 +35,7 @@ F32, F16, BF16, S8, S32 = 0, 1, 2, 3, 4
 LAYOUT_N, LAYOUT_T = 0, 1
 ACT_NONE, ACT_RELU = 0, 1
 BIAS_NONE, BIAS_COL, BIAS_ROW = 0, 1, 2
+UNIT_IMAGINARY, UNIT_DUAL = 0, 1     # complex numbers (i*i = -1), dual numbers (eps*eps = 0)
 
 _lib = None
 _lock = threading.Lock()
@@ -70,6 +73,13 @@ def _load_from(path: str):
     lib.oracle_gemm_entries.argtypes = [ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
                                         dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, i64, vp, vp,
                                         vp, ci]
+    lib.oracle_gemm_pairs.restype = i64
+    lib.oracle_gemm_pairs.argtypes = [ci, ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
+                                      dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, vp, i64, ci]
+    lib.oracle_gemm_pairs_entries.restype = i64
+    lib.oracle_gemm_pairs_entries.argtypes = [ci, ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
+                                              dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, i64, vp,
+                                              vp, vp, ci]
     lib.oracle_f16_to_double.restype = dbl
     lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_double.restype = dbl
@@ -169,3 +179,45 @@ def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
         f = np.vectorize(lambda b: lib.oracle_bf16_to_double(int(b)), otypes=[np.float64])
         return f(bits)
     return bits.astype(np.float64)
+
+
+def gemm_pairs(unit, ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
+               beta=0.0, c_dtype=F32, C=None, ldc=0, bias_dtype=F32, bias=None,
+               bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, ldd=None, nthreads=None,
+               c_act=ACT_NONE):
+    """Complex (unit UNIT_IMAGINARY) or dual (UNIT_DUAL) GEMM on interleaved
+    storage; sizes and leading dimensions count pairs.  Returns D with shape
+    (M, ldd, 2): [..., 0] the real parts, [..., 1] the unit parts (raw bits
+    for 16-bit outputs)."""
+    if ldd is None:
+        ldd = N
+    if nthreads is None:
+        nthreads = max_threads()
+    D = np.zeros((M, ldd, 2), dtype=_OUT_NP[d_dtype])
+    n = _load().oracle_gemm_pairs(unit, ab_dtype, layout_a, layout_b, M, N, K, float(alpha),
+                                  _ptr(A), lda, _ptr(B), ldb, float(beta), c_dtype, _ptr(C), ldc,
+                                  bias_dtype, _ptr(bias), bias_mode, act, c_act, d_dtype,
+                                  D.ctypes.data, ldd, nthreads)
+    if n < 0:
+        raise ValueError("oracle_gemm_pairs: invalid arguments")
+    return D
+
+
+def gemm_pairs_entries(unit, ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
+                       rows, cols, beta=0.0, c_dtype=F32, C=None, ldc=0, bias_dtype=F32,
+                       bias=None, bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, nthreads=None,
+                       c_act=ACT_NONE):
+    """The output pairs at (rows[e], cols[e]); shape (n, 2)."""
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if nthreads is None:
+        nthreads = max_threads()
+    out = np.zeros((rows.shape[0], 2), dtype=_OUT_NP[d_dtype])
+    n = _load().oracle_gemm_pairs_entries(unit, ab_dtype, layout_a, layout_b, M, N, K,
+                                          float(alpha), _ptr(A), lda, _ptr(B), ldb, float(beta),
+                                          c_dtype, _ptr(C), ldc, bias_dtype, _ptr(bias), bias_mode,
+                                          act, c_act, d_dtype, rows.shape[0], rows.ctypes.data,
+                                          cols.ctypes.data, out.ctypes.data, nthreads)
+    if n < 0:
+        raise ValueError("oracle_gemm_pairs_entries: invalid arguments")
+    return out

@@ -416,6 +416,105 @@ int64_t oracle_gemm_entries(int ab_dtype, int layout_a, int layout_b,
     return overflow;
 }
 
+/* ------------------------------------------------------------------------ */
+/* GEMM over complex or dual numbers.                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * "Flexible Performant GEMM Kernels on GPUs", section 5.4: a complex GEMM
+ * multiplies numbers x + y*i with i*i = -1; a dual-number GEMM numbers
+ * x + y*eps with eps*eps = 0.  Writing u for the unit, one product is
+ *     (a + b u)(c + d u) = (a c + b d u^2) + (a d + b c) u,
+ * so u^2 = -1 gives (ac - bd) + (ad + bc) i and u^2 = 0 gives ac + (ad + bc) eps.
+ * The matrices are stored interleaved, as that section describes for global
+ * memory: the pair of the logical element at storage offset e (from the layout
+ * functions above, in pairs) sits at scalar positions 2e (the real part) and
+ * 2e + 1 (the u part); A, B, C, D and the bias all hold such pairs.
+ *
+ * Readings taken here:
+ *   - D = epilogue(alpha * sum_k a(i,k) b(k,j) + beta * C) with REAL alpha and
+ *     beta (the section's D = A*B + C is alpha = beta = 1); sums in fp64.
+ *   - The bias is a vector of pairs (N of them, by column, or M by row) added
+ *     to the pair of each output; c_act and act apply to each of the two parts
+ *     on its own (the pages define no activation of a complex number), and
+ *     each part is rounded on its own to the output type.
+ */
+enum { OR_UNIT_IMAGINARY = 0, OR_UNIT_DUAL = 1 };
+
+/* One finished output pair (i, j) into out[2*out_idx], out[2*out_idx + 1]. */
+static void element_pair(const problem_t* p, int unit, int64_t i, int64_t j, void* out, int64_t out_idx) {
+    const double u2 = unit == OR_UNIT_IMAGINARY ? -1.0 : 0.0;   /* the square of the unit */
+    double re = 0.0, im = 0.0;
+    for (int64_t k = 0; k < p->K; ++k) {
+        const int64_t ea = a_offset(p->layout_a, i, k, p->lda);
+        const int64_t eb = b_offset(p->layout_b, k, j, p->ldb);
+        const double a = load_float(p->ab_dtype, p->A, 2 * ea), b = load_float(p->ab_dtype, p->A, 2 * ea + 1);
+        const double c = load_float(p->ab_dtype, p->B, 2 * eb), d = load_float(p->ab_dtype, p->B, 2 * eb + 1);
+        re += a * c + u2 * (b * d);
+        im += a * d + b * c;
+    }
+    double acc[2] = {re, im};
+    for (int part = 0; part < 2; ++part) {
+        double v = p->alpha * acc[part];
+        if (p->beta != 0.0) {
+            double cv = load_float(p->c_dtype, p->C, 2 * (i * p->ldc + j) + part);
+            if (p->c_act == OR_ACT_RELU) cv = (cv > 0.0) ? cv : 0.0;
+            v += p->beta * cv;
+        }
+        if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, 2 * j + part);
+        else if (p->bias_mode == OR_BIAS_ROW) v += load_float(p->bias_dtype, p->bias, 2 * i + part);
+        if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;
+        store_float(p->d_dtype, out, 2 * out_idx + part, v);
+    }
+}
+
+static int valid_pair_problem(const problem_t* p, int unit) {
+    if (unit != OR_UNIT_IMAGINARY && unit != OR_UNIT_DUAL) return 0;
+    if (p->ab_dtype == OR_S8 || p->ab_dtype == OR_S32) return 0;   /* floating parts only */
+    return valid_problem(p);
+}
+
+/* Full complex / dual GEMM (dot-product order, rows in parallel).  Sizes and
+ * leading dimensions count pairs.  Returns 0, or -1 for invalid arguments. */
+int64_t oracle_gemm_pairs(int unit, int ab_dtype, int layout_a, int layout_b,
+                          int64_t M, int64_t N, int64_t K,
+                          double alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                          double beta, int c_dtype, const void* C, int64_t ldc,
+                          int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
+                          int d_dtype, void* D, int64_t ldd, int nthreads) {
+    problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
+                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
+    if (!valid_pair_problem(&p, unit)) return -1;
+    if (M == 0 || N == 0) return 0;
+    init_tables();
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            element_pair(&p, unit, i, j, D, i * ldd + j);
+    return 0;
+}
+
+/* Selected output pairs only: out[2e], out[2e+1] = D[rows[e], cols[e]]. */
+int64_t oracle_gemm_pairs_entries(int unit, int ab_dtype, int layout_a, int layout_b,
+                                  int64_t M, int64_t N, int64_t K,
+                                  double alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                                  double beta, int c_dtype, const void* C, int64_t ldc,
+                                  int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
+                                  int d_dtype, int64_t n_entries, const int64_t* rows,
+                                  const int64_t* cols, void* out, int nthreads) {
+    problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
+                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
+    if (!valid_pair_problem(&p, unit)) return -1;
+    for (int64_t e = 0; e < n_entries; ++e)
+        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
+    init_tables();
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads)
+    for (int64_t e = 0; e < n_entries; ++e)
+        element_pair(&p, unit, rows[e], cols[e], out, e);
+    return 0;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -13,6 +13,7 @@ import pytest
 import oracle as O
 
 import test_oracle as T
+import test_oracle_pairs as TP
 
 SRC = os.path.join(os.path.dirname(O.__file__), "oracle.c")
 
@@ -24,7 +25,7 @@ MUTANTS = {
     "transposed_B_index": ("? k + j * ldb : k * ldb + j", "? k + j * ldb : j * ldb + k"),
     "bias_indexed_by_row": ("if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, j);",
                             "if (p->bias_mode == OR_BIAS_COL) v += load_float(p->bias_dtype, p->bias, i);"),
-    "relu_dropped": ("if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;", ""),
+    "relu_dropped": ("if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;\n    return v;", "return v;"),
     "ties_round_up": ("(fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0", "fl + 1.0"),
     "int_beta_sign": ("v += beta * c;", "v -= beta * c;"),
     "k_loop_short_f16": ("for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += f16_table",
@@ -35,6 +36,19 @@ MUTANTS = {
                      "b_offset(p->layout_b, 1, j, p->ldb) - b0 + 1 : 0;\n    double acc"),
     "bf16_table_is_f16": ("acc += bf16_table[A[ia]] * bf16_table[B[ib]]",
                           "acc += f16_table[A[ia]] * bf16_table[B[ib]]"),
+    # complex / dual-number GEMM
+    "pair_unit_square_sign": ("re += a * c + u2 * (b * d);", "re += a * c - u2 * (b * d);"),
+    "pair_dual_as_complex": ("unit == OR_UNIT_IMAGINARY ? -1.0 : 0.0;", "unit == OR_UNIT_IMAGINARY ? -1.0 : -1.0;"),
+    "pair_cross_term_sign": ("im += a * d + b * c;", "im += a * d - b * c;"),
+    "pair_imag_of_A_read_as_real": ("b = load_float(p->ab_dtype, p->A, 2 * ea + 1);",
+                                    "b = load_float(p->ab_dtype, p->A, 2 * ea);"),
+    "pair_conjugated_B": ("d = load_float(p->ab_dtype, p->B, 2 * eb + 1);",
+                          "d = -load_float(p->ab_dtype, p->B, 2 * eb + 1);"),
+    "pair_c_unit_part_ignored": ("p->C, 2 * (i * p->ldc + j) + part);", "p->C, 2 * (i * p->ldc + j));"),
+    "pair_relu_dropped": ("if (p->act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;\n        store_float",
+                          "store_float"),
+    "pair_bias_not_paired": ("v += load_float(p->bias_dtype, p->bias, 2 * j + part);",
+                             "v += load_float(p->bias_dtype, p->bias, j + part);"),
 }
 
 PINS = [
@@ -47,6 +61,10 @@ PINS = [
     lambda: [T.test_f16_rounding_cases(x, b) for x, b in T.F16_CASES],
     lambda: [T.test_bf16_rounding_cases(x, b) for x, b in T.BF16_CASES],
     lambda: T.test_random_float_within_fp64_rounding_of_exact_sum(),
+    lambda: [TP.test_hand_worked_pairs(c, lay) for c in TP._golden() for lay in TP.LAYOUTS],
+    lambda: [TP.test_block_matrix_representation(u, lay) for u in ("complex", "dual")
+             for lay in TP.LAYOUTS],
+    lambda: [TP.test_complex_small_integers_match_numpy(lay, "f16") for lay in TP.LAYOUTS],
 ]
 
 
