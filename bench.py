@@ -304,6 +304,7 @@ def bench_ours(args, rank, world, local_rank):
         run_suite(G, device)
         run_batched_suite(G, device)
         run_diag_suite(G, device)
+        run_pair_suite(G, device)
     plan.close()
     if dist:
         dist.destroy_process_group()
@@ -667,6 +668,67 @@ def run_diag_suite(G, device, warmup=3, iters=20, sets=4):
                           "status": plan.device_status()}), flush=True)
         plan.close()
         del Xs, Cs, Ds, sq, dg
+        torch.cuda.empty_cache()
+
+
+def run_pair_suite(G, device, warmup=3, iters=20):
+    """Complex and dual-number GEMM workloads (one JSON line each): the whole
+    gemm_run_complex call (staging pass + tensor-core GEMM), back to back and
+    from a CUDA graph.  TFLOP/s count the definition's real operations (8 per
+    complex multiply-add, 6 per dual one)."""
+    import torch
+    from dense_gemm_epilogues_gb300 import inputs as I
+    peaks = load_peaks()
+    for unit in ("complex", "dual"):
+        p = I.pair_fp16_4096(unit)
+        inp = I.generate_pairs(p, I.BASE_SEED + 30)
+        A, B, C = inp.A.to(device), inp.B.to(device), inp.C.to(device)
+        D = torch.empty((p.M, p.ldd, 2), dtype=torch.float32, device=device)
+        plan = G.Plan(G.GEMM_F16, G.GEMM_F32, device.index or 0)
+        epi = G.make_epilogue(G.GEMM_F32)
+        code = G.GEMM_UNIT_IMAGINARY if unit == "complex" else G.GEMM_UNIT_DUAL
+
+        def call_on(st):
+            G.gemm_run_complex(plan.handle, code, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b],
+                               p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
+                               p.beta, C.data_ptr(), p.ldc, D.data_ptr(), p.ldd, epi, st.cuda_stream)
+        stream = torch.cuda.current_stream(device)
+        for _ in range(warmup):
+            call_on(stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            call_on(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / iters
+        side = torch.cuda.Stream(device)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            gr.capture_begin()
+            for _ in range(iters):
+                call_on(side)
+            gr.capture_end()
+            gr.replay()
+            side.synchronize()
+            e0.record(side)
+            gr.replay()
+            e1.record(side)
+        side.synchronize()
+        tg = e0.elapsed_time(e1) / 1e3 / iters
+        cfg = plan.last_config()
+        real_flops = 2.0 * p.M * (2 * p.N) * (2 * p.K)
+        print(json.dumps({"suite": p.name, "unit": unit, "M": p.M, "N": p.N, "K": p.K,
+                          "kernel": cfg["kernel_name"], "real_gemm": f"{p.M}x{2 * p.N}x{2 * p.K}",
+                          "median_us": round(t * 1e6, 2), "graph_us": round(tg * 1e6, 2),
+                          "tflops_graph": round(p.flops / tg / 1e12, 2),
+                          "tensor_tflops_graph": round(real_flops / tg / 1e12, 2),
+                          "frac_tensor_peak": round(real_flops / tg / 1e12 / peaks["bf16_tflops"], 4),
+                          "status": plan.device_status()}), flush=True)
+        plan.close()
+        del A, B, C, D, gr
         torch.cuda.empty_cache()
 
 

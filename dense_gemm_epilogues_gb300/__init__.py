@@ -29,6 +29,7 @@ GEMM_BIAS_NONE, GEMM_BIAS_COL, GEMM_BIAS_ROW = 0, 1, 2
 (GEMM_KERNEL_AUTO, GEMM_KERNEL_NONE, GEMM_KERNEL_TC, GEMM_KERNEL_TC_INT8, GEMM_KERNEL_FFMA,
  GEMM_KERNEL_SIMT, GEMM_KERNEL_TC_PAIR, GEMM_KERNEL_DIAG) = range(8)
 GEMM_SIDE_LEFT, GEMM_SIDE_RIGHT = 0, 1
+GEMM_UNIT_IMAGINARY, GEMM_UNIT_DUAL = 0, 1
 
 KERNEL_NAMES = {GEMM_KERNEL_AUTO: "auto", GEMM_KERNEL_NONE: "none", GEMM_KERNEL_TC: "tc",
                 GEMM_KERNEL_TC_INT8: "tc_int8", GEMM_KERNEL_FFMA: "ffma", GEMM_KERNEL_SIMT: "simt",
@@ -40,7 +41,8 @@ LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host", "gemm_validate",
             "gemm_select", "gemm_plan_set_kernel", "gemm_plan_last_config", "gemm_plan_device_status",
             "gemm_plan_set_timeout", "gemm_status_string", "gemm_abi_version",
-            "gemm_run_s8_noalloc", "gemm_run_strided_batched", "gemm_run_diag"]
+            "gemm_run_s8_noalloc", "gemm_run_strided_batched", "gemm_run_diag",
+            "gemm_run_complex"]
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -103,6 +105,8 @@ def load_library(path: str = LIB_PATH):
                                         vp, i64, ctypes.POINTER(gemm_epilogue_t), vp, vp]
     lib.gemm_run_diag.argtypes = [vp, ci, ci, i64, i64, dbl, vp, vp, i64, dbl, vp, i64, vp, i64,
                                   ctypes.POINTER(gemm_epilogue_t), vp]
+    lib.gemm_run_complex.argtypes = [vp, ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64,
+                                     vp, i64, ctypes.POINTER(gemm_epilogue_t), vp]
     for name in EXPORTED:
         if name not in ("gemm_status_string", "gemm_abi_version"):
             getattr(lib, name).restype = ci
@@ -173,6 +177,13 @@ def gemm_run_diag(plan, side, layout_x, M, N, alpha, diag, X, ldx, beta, C, ldc,
                   epi: Optional[gemm_epilogue_t] = None, stream: int = 0) -> None:
     _check(load_library().gemm_run_diag(plan, side, layout_x, M, N, alpha, diag, X, ldx, beta, C, ldc,
                                         D, ldd, _epi_ptr(epi), stream), "gemm_run_diag")
+
+
+def gemm_run_complex(plan, unit, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     D, ldd, epi: Optional[gemm_epilogue_t] = None, stream: int = 0) -> None:
+    _check(load_library().gemm_run_complex(plan, unit, layout_a, layout_b, M, N, K, alpha, A, lda, B,
+                                           ldb, beta, C, ldc, D, ldd, _epi_ptr(epi), stream),
+           "gemm_run_complex")
 
 
 def gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd,

@@ -1,6 +1,6 @@
 """Build libgemm.so (in-tree) with nvcc for sm_103a.
 
-Five translation units are compiled in parallel and linked into
+Six translation units are compiled in parallel and linked into
 ``dense_gemm_epilogues_gb300/libgemm.so``; objects go to ``_build/``.  The
 CUDA runtime is linked statically, the driver API (TMA descriptor encoding) is
 reached through the runtime's driver entry-point query, so the library has no
@@ -17,7 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgemm.so")
-SOURCES = ["gemm_api.cu", "tc_kernel.cu", "tc2_kernel.cu", "simt_kernels.cu", "diag_kernel.cu"]
+SOURCES = ["gemm_api.cu", "tc_kernel.cu", "tc2_kernel.cu", "simt_kernels.cu", "diag_kernel.cu",
+           "pair_kernel.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -487,7 +487,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
 
 extern "C" {
 
-int gemm_abi_version(void) { return 103; }
+int gemm_abi_version(void) { return 104; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
@@ -819,6 +819,60 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx
   cfg.tiles = (int32_t)std::min<int64_t>(p.num_tiles, kMaxDim);
   plan->last = cfg;
   return GEMM_OK;
+}
+
+gemm_status_t gemm_run_complex(gemm_plan_t plan, gemm_unit_t unit, gemm_layout_t la, gemm_layout_t lb,
+                               int64_t M, int64_t N, int64_t K, double alpha, const void* A, int64_t lda,
+                               const void* B, int64_t ldb, double beta, const void* C, int64_t ldc, void* D,
+                               int64_t ldd, const gemm_epilogue_t* epi, gemm_stream_t stream_) {
+  if (!plan || (unit != GEMM_UNIT_IMAGINARY && unit != GEMM_UNIT_DUAL)) return GEMM_ERR_INVALID_ARG;
+  // The argument checks of gemm_run, in pairs.
+  gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
+  if (s != GEMM_OK) return s;
+  if (plan->ab == GEMM_S8) return GEMM_ERR_UNSUPPORTED;
+  if (epi && epi->bias_mode == GEMM_BIAS_ROW) return GEMM_ERR_UNSUPPORTED;
+  if (2 * N > kMaxDim || 2 * K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) {
+    gemm_config_t none{};
+    none.kernel = GEMM_KERNEL_NONE;
+    plan->last = none;
+    return GEMM_OK;
+  }
+  DeviceGuard g(plan->device);
+  if (!g.ok) return GEMM_ERR_CUDA;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int es = dtype_bytes(plan->ab);
+  // The real problem: M x 2N x 2K; A as an M x 2K matrix, B as the staged 2K x 2N one.
+  const void* Ar = A;
+  int64_t lda_r = 2 * lda;
+  gemm_layout_t la_r = la;
+  const void* Br = B;
+  int64_t ldb_r = 0;
+  if (K > 0) {
+    // A: row-major A is read in place when TMA can address it; otherwise staged.
+    const bool stage_a = la == GEMM_OP_N || !tma_ok(A, 2 * lda, es);
+    const int64_t lds = la == GEMM_OP_N ? (M + 7) / 8 * 8 : (2 * K + 7) / 8 * 8;
+    const size_t a_bytes = stage_a ? align_up((size_t)lds * (la == GEMM_OP_N ? 2 * K : M) * es, 256) : 0;
+    ldb_r = lb == GEMM_OP_N ? (2 * K + 7) / 8 * 8 : (2 * N + 7) / 8 * 8;
+    const size_t b_bytes = (size_t)ldb_r * (lb == GEMM_OP_N ? 2 * N : 2 * K) * es;
+    s = ensure_ws(plan, a_bytes + b_bytes, stream);
+    if (s != GEMM_OK) return s;
+    char* ws = static_cast<char*>(plan->ws);
+    cudaError_t ce = cudaSuccess;
+    if (stage_a) {
+      ce = launch_pair_stage_a(A, lda, la == GEMM_OP_T, M, K, es, ws, lds, stream);
+      Ar = ws;
+      lda_r = lds;
+    }
+    if (ce == cudaSuccess)
+      ce = launch_pair_stage_b(B, ldb, lb == GEMM_OP_T, K, N, es, unit == GEMM_UNIT_DUAL, ws + a_bytes, ldb_r,
+                               stream);
+    if (ce != cudaSuccess) return GEMM_ERR_CUDA;
+    Br = ws + a_bytes;
+    la_r = la;
+  }
+  return run_impl(plan, la_r, lb, M, 2 * N, 2 * K, alpha, Ar, lda_r, Br, ldb_r, beta, C, 2 * ldc, D, 2 * ldd, epi,
+                  stream_, Batch());
 }
 
 gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int64_t M, int64_t N,

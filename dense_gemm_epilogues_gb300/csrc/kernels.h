@@ -101,6 +101,15 @@ constexpr int DIAG_TM = 64, DIAG_TN = 64;
 // Persistent launch: min(tiles, sm_count x resident CTAs per SM) CTAs; the grid used goes to *grid_out.
 cudaError_t launch_diag(const DiagParams& p, int x_row_major, int sm_count, int* grid_out, cudaStream_t stream);
 
+// Complex / dual-number GEMM staging (pair_kernel.cu): B -> the 2K x 2N real
+// matrix whose column pairs give the real and unit parts of each product; A ->
+// an M x 2K real matrix (row-major copy, or split columns for column-major A).
+// elem_bytes: 2 (f16/bf16) or 4 (f32); out is 256-byte aligned, ldo/lds even.
+cudaError_t launch_pair_stage_b(const void* B, int64_t ldb, int b_row_major, int64_t K, int64_t N, int elem_bytes,
+                                int dual, void* out, int64_t ldo, cudaStream_t stream);
+cudaError_t launch_pair_stage_a(const void* A, int64_t lda, int a_row_major, int64_t M, int64_t K, int elem_bytes,
+                                void* out, int64_t lds, cudaStream_t stream);
+
 // int8 -> fp16 staging copy of a strided matrix: dst[r*ld + c] = src[r*ld + c]
 // for r < outer, c < inner.
 cudaError_t launch_s8_to_f16(const int8_t* src, __half* dst, int64_t outer, int64_t inner, int64_t ld,

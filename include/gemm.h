@@ -232,6 +232,42 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t la
                             const gemm_epilogue_t* epi, gemm_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gemm_run_complex -- the GEMM over complex or dual numbers:
+ *     D = epilogue(alpha * op(A) * op(B) + beta * C),
+ * every element a pair x + y*u, u the imaginary unit (GEMM_UNIT_IMAGINARY:
+ * i*i = -1) or the dual unit (GEMM_UNIT_DUAL: eps*eps = 0), so that
+ *     (a + b u)(c + d u) = (a c + b d u*u) + (a d + b c) u.
+ * The complex and dual-number GEMMs of "Flexible Performant GEMM Kernels on
+ * GPUs", section 5.4 (Figure 12), with its interleaved storage in global
+ * memory: the pair of the element at storage offset e (layout and leading
+ * dimension as for gemm_run, counted in pairs) occupies scalars 2e (real
+ * part) and 2e + 1 (u part).  A, B, C, D and the bias are all interleaved.
+ *   plan        ab_dtype F16, BF16 (tensor cores, fp32 accumulation) or F32
+ *               (CUDA cores); c_dtype and the epilogue's out_dtype as for gemm_run.
+ *   unit        gemm_unit_t.
+ *   M, N, K, lda, ldb, ldc, ldd   in pairs; 2N and 2K must fit the kernels' 32-bit range.
+ *   alpha, beta real scalars (beta == 0: C is not read).
+ *   epi         bias: N pairs (GEMM_BIAS_COL; GEMM_BIAS_ROW returns
+ *               GEMM_ERR_UNSUPPORTED); act and c_act act on each part alone.
+ * Method: one real GEMM of size M x 2N x 2K on the same kernels as gemm_run.
+ * A row-major (T) A is read in place as an M x 2K real matrix; B, and a
+ * column-major (N) A, are first rearranged by a staging pass into plan-owned
+ * device scratch (grown on demand, stream-ordered): 4 x B's bytes of scratch
+ * for B, 2 x A's bytes for A (plus alignment padding).  Complex products cost
+ * exactly their 4 real multiplies; dual products multiply one zero in four.
+ * gemm_plan_last_config reports the real GEMM's launch (N' = 2N, K' = 2K).
+ * Errors: those of gemm_run; GEMM_ERR_UNSUPPORTED for S8 plans.  Calls that
+ * share a plan from several streams race on its scratch, as for gemm_run.
+ * ------------------------------------------------------------------------- */
+typedef enum { GEMM_UNIT_IMAGINARY = 0 /* complex */, GEMM_UNIT_DUAL = 1 /* dual */ } gemm_unit_t;
+
+gemm_status_t gemm_run_complex(gemm_plan_t plan, gemm_unit_t unit, gemm_layout_t layoutA,
+                               gemm_layout_t layoutB, int64_t M, int64_t N, int64_t K, double alpha,
+                               const void* A, int64_t lda, const void* B, int64_t ldb, double beta,
+                               const void* C, int64_t ldc, void* D, int64_t ldd,
+                               const gemm_epilogue_t* epi, gemm_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gemm_run_host -- the same operation on HOST buffers (pinned or pageable).
  * Copies A, B, C (when beta != 0) and the bias into plan-owned device staging
  * (grown on demand), runs gemm_run on `stream`, copies D back to the host and
@@ -299,8 +335,8 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 103 (gemm_epilogue_t.c_act,
- * gemm_run_strided_batched, gemm_run_diag). */
+/* ABI version of this header (major * 100 + minor): 104 (gemm_epilogue_t.c_act,
+ * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------

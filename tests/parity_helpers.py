@@ -239,3 +239,80 @@ class DeviceDiag:
 def make_diag_plan(p: I.DiagProblem) -> G.Plan:
     c = p.c if p.c else ("s32" if p.ab == "s8" else "f32")
     return G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[c], torch.cuda.current_device())
+
+
+# --------------------------- complex / dual GEMM -----------------------------
+
+OR_UNIT = {"complex": O.UNIT_IMAGINARY, "dual": O.UNIT_DUAL}
+G_UNIT = {"complex": G.GEMM_UNIT_IMAGINARY, "dual": G.GEMM_UNIT_DUAL}
+
+
+def _oracle_pair_kwargs(p: I.PairProblem, inp: I.PairInputs) -> dict:
+    return dict(beta=p.beta, c_dtype=OR_DT[p.c] if p.c else O.F32, C=inp.C,
+                ldc=p.ldc if p.c else 0, bias_dtype=OR_DT[p.bias] if p.bias else O.F32,
+                bias=inp.bias, bias_mode=OR_BIAS[p.bias_mode], act=OR_ACT[p.act],
+                d_dtype=OR_DT[p.d], c_act=OR_ACT[p.c_act])
+
+
+def oracle_pairs_full(inp: I.PairInputs) -> np.ndarray:
+    """(M, N, 2) output pairs (raw bits for 16-bit types)."""
+    p = inp.problem
+    return O.gemm_pairs(OR_UNIT[p.unit], OR_DT[p.ab], OR_LAY[p.layout_a], OR_LAY[p.layout_b],
+                        p.M, p.N, p.K, p.alpha, inp.A, p.lda, inp.B, p.ldb, ldd=p.N,
+                        **_oracle_pair_kwargs(p, inp))
+
+
+def oracle_pairs_entries(inp: I.PairInputs, rows, cols) -> np.ndarray:
+    p = inp.problem
+    return O.gemm_pairs_entries(OR_UNIT[p.unit], OR_DT[p.ab], OR_LAY[p.layout_a],
+                                OR_LAY[p.layout_b], p.M, p.N, p.K, p.alpha, inp.A, p.lda, inp.B,
+                                p.ldb, rows, cols, **_oracle_pair_kwargs(p, inp))
+
+
+class DevicePairs:
+    """Device copies of a complex / dual problem, plus a guarded output."""
+
+    def __init__(self, inp: I.PairInputs, device="cuda"):
+        p = inp.problem
+        self.inp, self.p = inp, p
+        self.A = inp.A.to(device)
+        self.B = inp.B.to(device)
+        self.C = inp.C.to(device) if inp.C is not None else None
+        self.bias = inp.bias.to(device) if inp.bias is not None else None
+        self.Dbuf = torch.full((p.M + 2 * GUARD_ROWS, p.ldd, 2), SENTINEL[p.d],
+                               dtype=I.TORCH_DTYPES[p.d], device=device)
+        self.D = self.Dbuf[GUARD_ROWS:GUARD_ROWS + p.M]
+
+    def epilogue(self) -> G.gemm_epilogue_t:
+        p = self.p
+        return G.make_epilogue(G.DTYPE_CODES[p.d],
+                               self.bias.data_ptr() if self.bias is not None else 0,
+                               G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
+                               G_BIAS[p.bias_mode],
+                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE,
+                               G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE)
+
+    def run(self, plan: G.Plan, stream=None, A=None, B=None):
+        p = self.p
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        A = self.A.data_ptr() if A is None else A
+        B = self.B.data_ptr() if B is None else B
+        G.gemm_run_complex(plan.handle, G_UNIT[p.unit], G.LAYOUT_CODES[p.layout_a],
+                           G.LAYOUT_CODES[p.layout_b], p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb,
+                           p.beta, self.C.data_ptr() if self.C is not None else None,
+                           p.ldc if p.c else 0, self.D.data_ptr(), p.ldd, self.epilogue(), stream)
+
+    def check_guards(self):
+        p = self.p
+        s = torch.tensor(SENTINEL[p.d], dtype=I.TORCH_DTYPES[p.d])
+        for name, t in (("rows before D", self.Dbuf[:GUARD_ROWS]),
+                        ("rows after D", self.Dbuf[GUARD_ROWS + p.M:]), ("padding of D", self.D[:, p.N:])):
+            assert torch.all(t.cpu() == s), f"kernel wrote into the {name}"
+
+    def result(self) -> torch.Tensor:
+        return self.D[:, :self.p.N]
+
+
+def make_pair_plan(p: I.PairProblem) -> G.Plan:
+    return G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[p.c or "f32"], torch.cuda.current_device())
