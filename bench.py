@@ -38,7 +38,7 @@ MAIN_N = 8192
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DOMINANT_KERNEL_SOURCES = ["dense_gemm_epilogues_gb300/csrc/tc2_kernel.cu",
                            "dense_gemm_epilogues_gb300/csrc/common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tc_gemm_f16_8192_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tc_pair_gemm_f16_8192_traffic.txt")
 
 
 def parse_args():
