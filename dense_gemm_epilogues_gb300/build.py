@@ -40,6 +40,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
+    # Extra nvcc flags for tuning builds (e.g. -DGEMM_PAIR_STAGES=7); pass force=True to rebuild.
+    flags += os.environ.get("GEMM_EXTRA_NVCC_FLAGS", "").split()
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))

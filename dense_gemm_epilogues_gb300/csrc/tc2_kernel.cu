@@ -34,7 +34,10 @@ constexpr int PAIR_A_BYTES = TC_BM * TC_BK * 2;          // 16 KiB: this CTA's 1
 constexpr int PAIR_B_BYTES = (PAIR_BN / 2) * TC_BK * 2;  // 16 KiB: this CTA's half of B
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns of TMEM
-constexpr int PAIR_STAGES = 6;
+#ifndef GEMM_PAIR_STAGES
+#define GEMM_PAIR_STAGES 6
+#endif
+constexpr int PAIR_STAGES = GEMM_PAIR_STAGES;           // 32 KiB each
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
 constexpr size_t PAIR_SMEM = 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
 
@@ -74,9 +77,14 @@ __device__ __forceinline__ bool warp_wait_pair(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <bool INT_MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
+// CL = 2: one CTA pair per cluster.  CL = 4 (floating mode): two CTA pairs per
+// cluster on vertically adjacent tiles of one 512 x 256 super-tile; both pairs
+// need the same B columns, so each CTA loads one quarter of its B half and
+// multicasts it to the CTA in the same position of the other pair.
+template <bool INT_MODE, int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
+  static_assert(CL == 2 || (CL == 4 && !INT_MODE), "two-pair clusters serve the floating mode");
   constexpr int EPI_WARPS = PairThreads<INT_MODE>::EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -96,15 +104,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;                // position in the CTA pair
+  const int pp = (int)(crank >> 1);                // pair of the cluster (0 unless CL == 4)
+  const uint32_t pair_leader = crank & ~1u;        // cluster rank of this pair's leader
   const bool leader = rank == 0;
-  const int cluster_id = (int)(blockIdx.x >> 1);
-  const int num_clusters = (int)(gridDim.x >> 1);
+  const int cluster_id = (int)(blockIdx.x / CL);
+  const int num_clusters = (int)(gridDim.x / CL);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PAIR_STAGES; ++s) {
       mbar_init(full_bar(s), 1);    // leader: its expect_tx arrival + both CTAs' TMA bytes
-      mbar_init(empty_bar(s), 1);   // the leader's multicast commit
+      mbar_init(empty_bar(s), CL / 2);   // the multicast commit of each pair's leader
     }
     for (int b = 0; b < PAIR_ACC_BUFS; ++b) {
       mbar_init(tfull_bar(b), 1);   // the leader's multicast commit
@@ -139,6 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       while (ok && it.next(tile, kb0, kb1)) {
         int bz, tm, tn;
         pair_tile_coords(tile, p, bz, tm, tn);
+        if constexpr (CL == 4) tm = 2 * tm + pp;                    // this pair's half of the super-tile
         const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
         const int n0 = tn * PAIR_BN + (int)rank * (PAIR_BN / 2);    // this CTA's half of B
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
@@ -146,7 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
           if (leader) mbar_expect_tx(fb_local, 2u * PAIR_STAGE_BYTES);
-          const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, 0);
+          const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, pair_leader);
           const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
           const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
           const int k0 = kb * TC_BK;
@@ -157,7 +169,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           } else {
             tma_load_3d_pair(sa, &p.tmA, k0, m0, za, fb);
           }
-          if (p.b_mn_major) {
+          if constexpr (CL == 4) {
+            // Quarter pp of this CTA's B half, into this CTA and its counterpart in the other pair.
+            const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+            if (p.b_mn_major)
+              tma_load_3d_pair_multicast(sb + pp * MN_BOX_BYTES, &p.tmB, n0 + pp * MN_BOX, k0, zb, fb, mask);
+            else
+              tma_load_3d_pair_multicast(sb + pp * (PAIR_B_BYTES / 2), &p.tmB, k0, n0 + pp * (PAIR_BN / 4), zb,
+                                         fb, mask);
+          } else if (p.b_mn_major) {
 #pragma unroll
             for (int h = 0; h < (PAIR_BN / 2) / MN_BOX; ++h)
               tma_load_3d_pair(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
@@ -213,11 +233,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
                                                : smem_desc_sw128(sb + kk * 32u, 16, 1024);
               tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
             }
-            tc_commit_pair_multicast(empty_bar(stage), 0x3);
+            tc_commit_pair_multicast(empty_bar(stage), CL == 4 ? 0xF : 0x3);   // every CTA it feeds
             if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          tc_commit_pair_multicast(tfull_bar(buf), 0x3);
+          tc_commit_pair_multicast(tfull_bar(buf), (uint16_t)(0x3u << pair_leader));
           ++acc_it;
         }
       }
@@ -235,6 +255,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
     while (ok && it.next(tile, kb0, kb1)) {
       int bz, tm, tn;
       pair_tile_coords(tile, p, bz, tm, tn);
+      if constexpr (CL == 4) tm = 2 * tm + pp;
       const int row_in_cta = q * 32 + lane;
       const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + row_in_cta;
       const int64_t n0 = (int64_t)tn * PAIR_BN;
@@ -264,7 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           __syncwarp();
           if (lane == 0) {
             if (leader) mbar_arrive(tempty_bar(buf));
-            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), pair_leader));
           }
           ++acc_it;
         }
@@ -299,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           __syncwarp();
           if (lane == 0) {
             if (leader) mbar_arrive(tempty_bar(buf));
-            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), pair_leader));
             __threadfence();
             mbar_arrive(sk_bar);
           }
@@ -368,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           __syncwarp();
           if (lane == 0) {
             if (leader) mbar_arrive(tempty_bar(buf));
-            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+            else mbar_arrive_cluster(mapa_shared(tempty_bar(buf), pair_leader));
           }
         }
         ++acc_it;
@@ -383,27 +404,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
   if (warp == 1) tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
 }
 
-template <bool INT_MODE>
+template <bool INT_MODE, int CL>
 int max_clusters_for(int device) {
   static int cached[64] = {};
   if (device < 0 || device >= 64) return 0;
   if (cached[device] > 0) return cached[device];
-  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)PAIR_SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 512, 1, 1);
+  cfg.gridDim = dim3(CL * 256, 1, 1);
   cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE, CL>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -411,7 +432,7 @@ int max_clusters_for(int device) {
   return n;
 }
 
-template <bool INT_MODE>
+template <bool INT_MODE, int CL>
 cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   static_assert(PAIR_SMEM <= 232448, "shared memory budget");
   int dev = 0;
@@ -419,13 +440,13 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PAIR_SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   if (clusters <= 0) return cudaErrorInvalidValue;
-  tc_pair_gemm_kernel<INT_MODE><<<2 * clusters, PairThreads<INT_MODE>::THREADS, PAIR_SMEM, stream>>>(p);
+  tc_pair_gemm_kernel<INT_MODE, CL><<<CL * clusters, PairThreads<INT_MODE>::THREADS, PAIR_SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -435,13 +456,16 @@ int tc_pair_stages() { return PAIR_STAGES; }
 size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
 
 int tc_pair_max_clusters(int device) {
-  const int a = max_clusters_for<false>(device);
-  const int b = max_clusters_for<true>(device);
+  const int a = max_clusters_for<false, 2>(device);
+  const int b = max_clusters_for<true, 2>(device);
   return a < b ? a : b;
 }
 
-cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
-  return p.chunk_kb > 0 ? launch_mode<true>(p, clusters, stream) : launch_mode<false>(p, clusters, stream);
+int tc_quad_max_clusters(int device) { return max_clusters_for<false, 4>(device); }
+
+cudaError_t launch_tc_pair(const TcParams& p, int clusters, int cluster_size, cudaStream_t stream) {
+  if (p.chunk_kb > 0) return cluster_size == 2 ? launch_mode<true, 2>(p, clusters, stream) : cudaErrorInvalidValue;
+  return cluster_size == 4 ? launch_mode<false, 4>(p, clusters, stream) : launch_mode<false, 2>(p, clusters, stream);
 }
 
 }  // namespace gemmlib

@@ -116,6 +116,8 @@ typedef struct {
     int32_t tiles;        /* output tiles */
     int32_t sk_tiles;     /* tiles in the stream-K tail (their K blocks are shared out over
                              all CTA pairs; 0 = every tile runs whole on one CTA pair) */
+    int32_t cluster;      /* CTAs per thread-block cluster: 1, 2 (one CTA pair) or 4 (two CTA
+                             pairs on vertically adjacent tiles sharing B by TMA multicast) */
 } gemm_config_t;
 
 /* ---------------------------------------------------------------------------
@@ -335,8 +337,8 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 104 (gemm_epilogue_t.c_act,
- * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex). */
+/* ABI version of this header (major * 100 + minor): 105 (gemm_epilogue_t.c_act,
+ * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex, gemm_config_t.cluster). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------
