@@ -34,11 +34,17 @@ struct gemm_plan {
   int32_t sk_epoch = 0;
   gemm_config_t last{};
   uint64_t timeout_ns = 4000000000ull;
+  // gemm_run_host's row-panel pipeline: copy-in and copy-out streams and the
+  // events that order them with the caller's stream (created on first use).
+  cudaStream_t host_in = nullptr, host_out = nullptr;
+  cudaEvent_t host_ev[36] = {};
+  bool host_pipe = false;
 };
 
 namespace {
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;   // tile indices and TMA coordinates are 32-bit
+constexpr int kHostMaxPanels = 16;           // gemm_run_host: most row panels of its copy pipeline
 
 bool is_f16ish(int t) { return t == GEMM_F16 || t == GEMM_BF16; }
 bool is_float_out(int t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
@@ -582,6 +588,11 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
   if (plan->stage) cudaFree(plan->stage);
   if (plan->sk_ws) cudaFree(plan->sk_ws);
   if (plan->d_err) cudaFree(plan->d_err);
+  if (plan->host_pipe) {
+    for (cudaEvent_t e : plan->host_ev) cudaEventDestroy(e);
+    cudaStreamDestroy(plan->host_in);
+    cudaStreamDestroy(plan->host_out);
+  }
   delete plan;
   return GEMM_OK;
 }
@@ -942,23 +953,83 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb
   void* dD = base + off_d;
   void* dC = in_place ? dD : (beta != 0.0 ? base + off_c : nullptr);
   void* dbias = has_bias ? base + off_bias : nullptr;
-  if (a_bytes && cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
-  if (b_bytes && cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
-  if (beta != 0.0) {
-    const size_t cb = (size_t)((M - 1) * ldc + N) * dtype_bytes(plan->c);
-    if (cudaMemcpyAsync(dC, C, cb, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
-  }
-  if (has_bias && cudaMemcpyAsync(dbias, epi->bias, bias_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return GEMM_ERR_CUDA;
   gemm_epilogue_t e2{};
   if (epi) {
     e2 = *epi;
     e2.bias = dbias;
   }
-  s = gemm_run(plan, la, lb, M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, dD, ldd, epi ? &e2 : nullptr,
-               stream_);
-  if (s != GEMM_OK) return s;
-  if (cudaMemcpyAsync(D, dD, d_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  const int cb = dtype_bytes(plan->c), db = dtype_bytes(out);
+
+  // Row panels: rows [m0, m0 + mi) of A (layout T: whole rows; layout N: one strip
+  // of every column), C and D.  Panel i's inputs are copied in on one stream while
+  // panel i-1 runs on the caller's stream and panel i-2's D is copied out on a
+  // third, so the host link carries both directions at once and the GEMM hides
+  // behind the copies.  Small problems run as one panel.
+  int64_t rows = M;
+  if (K > 0 && M >= 2048 && a_bytes + c_bytes + d_bytes >= ((size_t)64 << 20)) {
+    const int64_t panels = std::min<int64_t>(kHostMaxPanels, M / 1024);
+    rows = ((M + panels - 1) / panels + 255) / 256 * 256;
+  }
+  const int P = (int)((M + rows - 1) / rows);
+  if (P > 1 && !plan->host_pipe) {
+    bool ok = cudaStreamCreateWithFlags(&plan->host_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&plan->host_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t& e : plan->host_ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return GEMM_ERR_CUDA;
+    plan->host_pipe = true;
+  }
+  cudaStream_t in = P > 1 ? plan->host_in : stream, outs = P > 1 ? plan->host_out : stream;
+  cudaEvent_t* ev = plan->host_ev;   // [0] start, [1] end, [2 + i] panel i in, [2 + kHostMaxPanels + i] panel i done
+  auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+  if (P > 1) {
+    // Everything already queued on the caller's stream comes first.
+    if (!ck(cudaEventRecord(ev[0], stream)) || !ck(cudaStreamWaitEvent(in, ev[0], 0)) ||
+        !ck(cudaStreamWaitEvent(outs, ev[0], 0)))
+      return GEMM_ERR_CUDA;
+  }
+  if (b_bytes && !ck(cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, in))) return GEMM_ERR_CUDA;
+  if (has_bias && !ck(cudaMemcpyAsync(dbias, epi->bias, bias_bytes, cudaMemcpyHostToDevice, in))) return GEMM_ERR_CUDA;
+  for (int i = 0; i < P; ++i) {
+    const int64_t m0 = (int64_t)i * rows, mi = std::min<int64_t>(rows, M - m0);
+    const char* hA = static_cast<const char*>(A);
+    char* pA = static_cast<char*>(dA);
+    if (K > 0) {
+      if (la == GEMM_OP_T) {
+        if (!ck(cudaMemcpyAsync(pA + m0 * lda * ab_b, hA + m0 * lda * ab_b, (size_t)((mi - 1) * lda + K) * ab_b,
+                                cudaMemcpyHostToDevice, in)))
+          return GEMM_ERR_CUDA;
+      } else if (!ck(cudaMemcpy2DAsync(pA + m0 * ab_b, (size_t)lda * ab_b, hA + m0 * ab_b, (size_t)lda * ab_b,
+                                       (size_t)mi * ab_b, (size_t)K, cudaMemcpyHostToDevice, in))) {
+        return GEMM_ERR_CUDA;
+      }
+    }
+    if (beta != 0.0 && !ck(cudaMemcpyAsync(static_cast<char*>(dC) + m0 * ldc * cb,
+                                           static_cast<const char*>(C) + m0 * ldc * cb,
+                                           (size_t)((mi - 1) * ldc + N) * cb, cudaMemcpyHostToDevice, in)))
+      return GEMM_ERR_CUDA;
+    if (P > 1 && (!ck(cudaEventRecord(ev[2 + i], in)) || !ck(cudaStreamWaitEvent(stream, ev[2 + i], 0))))
+      return GEMM_ERR_CUDA;
+    gemm_epilogue_t ei = e2;
+    if (has_bias && epi->bias_mode == GEMM_BIAS_ROW)
+      ei.bias = static_cast<const char*>(dbias) + m0 * dtype_bytes(epi->bias_dtype);
+    const void* pAi = la == GEMM_OP_T ? (const void*)(pA + m0 * lda * ab_b) : (const void*)(pA + m0 * ab_b);
+    s = gemm_run(plan, la, lb, mi, N, K, alpha, pAi, lda, dB, ldb, beta,
+                 beta != 0.0 ? static_cast<const char*>(dC) + m0 * ldc * cb : nullptr, ldc,
+                 static_cast<char*>(dD) + m0 * ldd * db, ldd, epi ? &ei : nullptr, stream_);
+    if (s != GEMM_OK) return s;
+    if (P > 1 && (!ck(cudaEventRecord(ev[2 + kHostMaxPanels + i], stream)) ||
+                  !ck(cudaStreamWaitEvent(outs, ev[2 + kHostMaxPanels + i], 0))))
+      return GEMM_ERR_CUDA;
+    // Only the N columns of each row: the caller's padding between rows stays untouched.
+    char* hD = static_cast<char*>(D) + m0 * ldd * db;
+    const char* sD = static_cast<const char*>(dD) + m0 * ldd * db;
+    const cudaError_t ce = ldd == N ? cudaMemcpyAsync(hD, sD, (size_t)(mi * N) * db, cudaMemcpyDeviceToHost, outs)
+                                    : cudaMemcpy2DAsync(hD, (size_t)ldd * db, sD, (size_t)ldd * db, (size_t)N * db,
+                                                        (size_t)mi, cudaMemcpyDeviceToHost, outs);
+    if (!ck(ce)) return GEMM_ERR_CUDA;
+  }
+  if (P > 1 && (!ck(cudaEventRecord(ev[1], outs)) || !ck(cudaStreamWaitEvent(stream, ev[1], 0))))
+    return GEMM_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
   return GEMM_OK;
 }

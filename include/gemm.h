@@ -272,10 +272,15 @@ gemm_status_t gemm_run_complex(gemm_plan_t plan, gemm_unit_t unit, gemm_layout_t
 /* ---------------------------------------------------------------------------
  * gemm_run_host -- the same operation on HOST buffers (pinned or pageable).
  * Copies A, B, C (when beta != 0) and the bias into plan-owned device staging
- * (grown on demand), runs gemm_run on `stream`, copies D back to the host and
- * synchronises `stream` before returning.  Arguments mean what they mean for
- * gemm_run, with host pointers; the bias pointer in `epi` is a host pointer too.
- * Host buffers stay owned by the caller.
+ * (grown on demand), runs gemm_run, copies D back to the host and synchronises
+ * `stream` before returning.  Arguments mean what they mean for gemm_run, with
+ * host pointers; the bias pointer in `epi` is a host pointer too.  Host buffers
+ * stay owned by the caller; only the N columns of each row of D are written.
+ * Large problems (M >= 2048, 64 MB or more to move) run as a pipeline of row
+ * panels over two plan-owned copy streams: B first, then each panel's rows of A
+ * and C are copied in while the previous panel's GEMM runs on `stream` and the
+ * one before it is copied out, so both directions of the host link stay busy.
+ * Pinned host memory lets the copies overlap; pageable memory stays correct.
  * ------------------------------------------------------------------------- */
 gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t layoutA, gemm_layout_t layoutB,
                             int64_t M, int64_t N, int64_t K, double alpha,

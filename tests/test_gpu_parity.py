@@ -241,7 +241,7 @@ def test_empty_problems_are_noops():
 
 def test_run_host_buffers():
     p = I.Problem("host", "bf16", "T", "T", 300, 280, 96, beta=0.25, c="f32", d="bf16",
-                  bias="f32", bias_mode="col", act="relu")
+                  bias="f32", bias_mode="col", act="relu", pad_d=5)
     inp = I.generate(p, 118)
     ref = H.oracle_full(inp)
     plan = H.make_plan(p)
@@ -249,12 +249,13 @@ def test_run_host_buffers():
     B = inp.B.pin_memory()
     C = inp.C.pin_memory()
     bias = inp.bias.pin_memory()
-    D = torch.zeros((p.M, p.ldd), dtype=torch.bfloat16).pin_memory()
+    D = torch.full((p.M, p.ldd), 7.0, dtype=torch.bfloat16).pin_memory()
     epi = G.make_epilogue(G.GEMM_BF16, bias.data_ptr(), G.GEMM_F32, G.GEMM_BIAS_COL, G.GEMM_ACT_RELU)
     G.gemm_run_host(plan.handle, G.GEMM_OP_T, G.GEMM_OP_T, p.M, p.N, p.K, p.alpha, A.data_ptr(),
                     p.lda, B.data_ptr(), p.ldb, p.beta, C.data_ptr(), p.ldc, D.data_ptr(), p.ldd,
                     epi, torch.cuda.current_stream().cuda_stream)
     H.check_close(D[:, :p.N], ref, "bf16", "host entry")
+    assert torch.all(D[:, p.N:] == 7.0), "the host entry wrote into the padding of D"
 
 
 # ------------------------------- bounded waits -------------------------------
