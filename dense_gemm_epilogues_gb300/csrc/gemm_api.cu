@@ -122,6 +122,23 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
 // does half the MMA work of a 128x256 tile but keeps the fixed per-tile costs).
 double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 4096^3 and 1024^3 fp16
 
+// Run a tensor-core problem on CTA pairs?  Both dimensions must exceed one
+// 128-wide tile, and the 256 x 256 tiles must fill at least one wave of pairs
+// (or the stream-K tail, when requested, spreads them over all pairs).
+// GEMM_TC_CTA_GROUP=1 never uses pairs; =2 uses them whenever both dimensions allow.
+bool use_pairs(int64_t M, int64_t N, int64_t batch, int pair_clusters) {
+  if (pair_clusters <= 0 || M <= 128 || N <= 128) return false;
+  if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) {
+    const int v = std::atoi(env);
+    if (v == 1) return false;
+    if (v == 2) return true;
+  }
+  if (const char* sk = std::getenv("GEMM_STREAM_K"))
+    if (std::atoi(sk) != 0) return true;
+  const int64_t pair_tiles = batch * ((M + 255) / 256) * ((N + 255) / 256);
+  return pair_tiles >= pair_clusters;
+}
+
 // pair_clusters: co-resident clusters of two CTAs for the CTA-pair kernel on the
 // target device (0: that kernel is not considered unless forced).
 gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
@@ -161,11 +178,11 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
   } else {
     k = tc_ok ? GEMM_KERNEL_TC
               : int8_ok ? GEMM_KERNEL_TC_INT8 : ffma_ok ? GEMM_KERNEL_FFMA : GEMM_KERNEL_SIMT;
-    // Both dimensions above one 128-wide tile: 256 x 256 tiles on CTA pairs move
-    // a third fewer operand bytes per SM for the same MMA work.
-    bool pair = k == GEMM_KERNEL_TC && pair_clusters > 0 && M > 128 && N > 128;
-    if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) pair = pair && std::atoi(env) != 1;
-    if (pair) k = GEMM_KERNEL_TC_PAIR;
+    // 256 x 256 tiles on CTA pairs move a third fewer operand bytes per SM for the
+    // same MMA work, but a pair's fixed cost per launch is higher (~9 us against
+    // ~5 us measured) and its tiles are four times larger: below one full wave of
+    // pairs the single-CTA kernel's finer grid finishes first.
+    if (k == GEMM_KERNEL_TC && use_pairs(M, N, batch, pair_clusters)) k = GEMM_KERNEL_TC_PAIR;
   }
   (void)la;
   (void)lb;
@@ -257,8 +274,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         if (std::atoi(env) == 512) chunk = 512;
       }
       cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? chunk : 0;
-      bool pair_int = k == GEMM_KERNEL_TC_INT8 && pair_clusters > 0 && M > 128 && N > 128;
-      if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) pair_int = pair_int && std::atoi(env) != 1;
+      const bool pair_int = k == GEMM_KERNEL_TC_INT8 && use_pairs(M, N, batch, pair_clusters);
       if (pair_int) {   // exact integer mode on CTA pairs: 256 x 256 tiles
         cfg.bm = 2 * TC_BM;
         cfg.bn = 256;
@@ -546,8 +562,9 @@ gemm_status_t gemm_select(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gem
   const double alpha_probe = ab == GEMM_S8 ? 1.0 : 1.0;
   gemm_status_t s = validate(ab, c, la, lb, M, N, K, alpha_probe, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
-  return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out, sm_count / 2, 1,
-                       sm_count / 4);
+  // Host-only: a device whose SMs all pair up; clusters of four are not assumed
+  // (whether they fit is a property of the device's GPC layout).
+  return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out, sm_count / 2);
 }
 
 gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab, gemm_dtype_t c, int device) {

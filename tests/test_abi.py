@@ -116,8 +116,10 @@ def test_selector_all_layouts_on_tensor_cores(la, lb):
 
 def test_selector_narrow_and_small_shapes():
     assert _sel(N=64, M=16384, K=16384)["bn"] == 128
-    cfg = _sel(M=512, N=512, K=512)
-    assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["tiles"] == 4 and cfg["grid"] == 8
+    cfg = _sel(M=512, N=512, K=512)   # 4 pair tiles: less than a wave of pairs
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC and cfg["bm"] == 128
+    cfg = _sel(M=2560, N=2048, K=512)  # 80 pair tiles on 76 pairs
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["tiles"] == 80
 
 
 def test_selector_misaligned_operands_use_generic_kernel():

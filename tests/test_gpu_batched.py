@@ -73,7 +73,8 @@ def run_batched(p: I.Problem, batch: int, seed: int, share_b=False, gap=8, kerne
 
 
 @pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
-def test_batched_pair_kernel_alpha_beta_bias(layout):
+def test_batched_pair_kernel_alpha_beta_bias(layout, monkeypatch):
+    monkeypatch.setenv("GEMM_TC_CTA_GROUP", "2")   # pairs, although 20 tiles are less than a wave
     p = H.tma_aligned(I.Problem("bat", "f16", layout[0], layout[1], 300, 264, 200, alpha=1.25,
                                 beta=-0.5, c="f32", bias="f32", bias_mode="col", act="relu",
                                 pad_d=3))

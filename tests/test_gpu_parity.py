@@ -45,9 +45,17 @@ def test_tc_ragged_alpha_beta(layout, ab, kernel):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_selector_picks_pair_kernel_for_large_tiles(layout):
-    p = H.tma_aligned(I.Problem("tc_auto", "f16", layout[0], layout[1], 520, 300, 136))
+def test_selector_picks_pair_kernel_when_its_tiles_fill_the_pairs(layout):
+    """80 tiles of 256 x 256 (at least one per CTA pair): the selector runs pairs."""
+    p = H.tma_aligned(I.Problem("tc_auto", "f16", layout[0], layout[1], 2560, 2048, 72))
     H.run_and_check_full(p, 120, expect_kernel=G.GEMM_KERNEL_TC_PAIR)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_selector_picks_single_cta_below_a_wave_of_pairs(layout):
+    """6 pair tiles would leave most SMs idle: the single-CTA kernel's finer grid runs."""
+    p = H.tma_aligned(I.Problem("tc_small", "f16", layout[0], layout[1], 520, 300, 136))
+    H.run_and_check_full(p, 121, expect_kernel=G.GEMM_KERNEL_TC)
 
 
 @pytest.mark.parametrize("kernel", TC_KERNELS, ids=TC_IDS)
@@ -137,11 +145,8 @@ def test_tc_many_tiles_persistent_loop(kernel):
 @pytest.fixture(params=[1, 2], ids=["cta1", "pair"])
 def cta_group(request, monkeypatch):
     """Run the exact int8 path on single-CTA tiles (GEMM_TC_CTA_GROUP=1) or on
-    CTA pairs (the selector's choice when M and N exceed 128)."""
-    if request.param == 1:
-        monkeypatch.setenv("GEMM_TC_CTA_GROUP", "1")
-    else:
-        monkeypatch.delenv("GEMM_TC_CTA_GROUP", raising=False)
+    CTA pairs (GEMM_TC_CTA_GROUP=2; the selector's choice for grids of a wave or more)."""
+    monkeypatch.setenv("GEMM_TC_CTA_GROUP", str(request.param))
     return request.param
 
 
@@ -291,6 +296,7 @@ def test_pair_stream_k_tail(shape, stream_k, monkeypatch):
     segments per tile here); the owning pair adds the published partials before
     the full epilogue (alpha, beta*C, bias, ReLU, bf16 cast)."""
     monkeypatch.setenv("GEMM_STREAM_K", "1" if stream_k == "on" else "0")
+    monkeypatch.setenv("GEMM_TC_CTA_GROUP", "2")
     M, N, K = shape
     p = H.tma_aligned(I.Problem("sk", "bf16", "T", "N", M, N, K, alpha=0.75, beta=-0.5, c="f32",
                                 d="bf16", bias="f32", bias_mode="col", act="relu"))

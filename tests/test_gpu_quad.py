@@ -24,6 +24,7 @@ def _cuda():
 @pytest.fixture(params=[4, 2], ids=["quad", "pair"])
 def cluster(request, monkeypatch):
     monkeypatch.setenv("GEMM_TC_CLUSTER", str(request.param))
+    monkeypatch.setenv("GEMM_TC_CTA_GROUP", "2")   # pairs even where the grid is under a wave
     return request.param
 
 
