@@ -85,6 +85,25 @@ struct SliceLoader {
 #ifndef GEMM_FFMA_MINB
 #define GEMM_FFMA_MINB 2
 #endif
+// Paired FP32 FMA (fma.rn.f32x2): two independent fp32 FMAs, each rounded as
+// fmaf would, in one instruction -- half the issue slots of scalar FFMA for the
+// same FMA-pipe work.  Adjacent columns of a thread's tile share one packed
+// B operand; the A value is duplicated into both halves.
+#ifndef GEMM_FFMA_PAIRED
+#define GEMM_FFMA_PAIRED 1
+#endif
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
 template <bool A_KMAJOR, bool B_KMAJOR>
 __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(const FfmaParams p) {
   __shared__ __align__(16) float As[2][FFMA_BK * SG_LDS];
@@ -100,11 +119,19 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
   const SliceLoader<A_KMAJOR> la{p.A + bz * p.stride_a, p.lda, p.M, p.K};
   const SliceLoader<B_KMAJOR> lb{p.B + bz * p.stride_b, p.ldb, p.N, p.K};
 
+#if GEMM_FFMA_PAIRED
+  uint64_t acc2[8][4];   // acc2[i][q] holds columns 2q and 2q+1 of row i
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;
+#else
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+#endif
 
   const int nkt = (p.K + FFMA_BK - 1) / FFMA_BK;
   float ra[SG_NV][4], rb[SG_NV][4];
@@ -132,11 +159,21 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
       const float4 b0 = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + tx * 4]);
       const float4 b1 = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + 64 + tx * 4]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#if GEMM_FFMA_PAIRED
+      const uint64_t b2[4] = {pack2(b0.x, b0.y), pack2(b0.z, b0.w), pack2(b1.x, b1.y), pack2(b1.z, b1.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t ai = pack2(a[i], a[i]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ffma2(acc2[i][q], ai, b2[q]);
+      }
+#else
       const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+#endif
     }
     if (more) {
       la.store(As[buf ^ 1], tid, ra);
@@ -146,6 +183,13 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
     buf ^= 1;
   }
 
+#if GEMM_FFMA_PAIRED
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unpack2(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
+#endif
   // Fused epilogue.  Thread rows: ty*4+i and 64+ty*4+i; columns tx*4+j and 64+tx*4+j.
   const EpiParams& e = p.epi;
   const EpiPtrs ptr = epi_ptrs(e, bz);
