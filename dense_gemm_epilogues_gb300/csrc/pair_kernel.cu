@@ -30,84 +30,127 @@ namespace gemmlib {
 namespace {
 
 constexpr int PS_THREADS = 256;
+constexpr int PS_V = 4;   // pairs per thread step (16 bytes of fp16 pairs)
 
-template <typename U> struct PairWord;
-template <> struct PairWord<uint16_t> { using T = uint32_t; static constexpr uint16_t SIGN = 0x8000u; };
-template <> struct PairWord<uint32_t> { using T = uint2; static constexpr uint32_t SIGN = 0x80000000u; };
+template <typename U> struct Sign;
+template <> struct Sign<uint16_t> { static constexpr uint16_t BIT = 0x8000u; };
+template <> struct Sign<uint32_t> { static constexpr uint32_t BIT = 0x80000000u; };
 
+// n (<= 8) consecutive elements; `vec`: all 8 present and the address 16-byte aligned.
 template <typename U>
-__device__ __forceinline__ void load_pair(const U* p, int64_t e, bool aligned, U& re, U& im) {
-  if (aligned) {
-    const typename PairWord<U>::T w = reinterpret_cast<const typename PairWord<U>::T*>(p)[e];
-    U v[2];
-    memcpy(v, &w, sizeof(v));
-    re = v[0];
-    im = v[1];
+__device__ __forceinline__ void load8u(const U* p, bool vec, int n, U (&v)[8]) {
+  if (vec) {
+    if constexpr (sizeof(U) == 2) {
+      const uint4 r = *reinterpret_cast<const uint4*>(p);
+      memcpy(v, &r, 16);
+    } else {
+      const uint4 r0 = reinterpret_cast<const uint4*>(p)[0], r1 = reinterpret_cast<const uint4*>(p)[1];
+      memcpy(v, &r0, 16);
+      memcpy(v + 4, &r1, 16);
+    }
   } else {
-    re = p[2 * e];
-    im = p[2 * e + 1];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) v[t] = t < n ? p[t] : (U)0;
   }
 }
 
-// Two adjacent elements at an even element offset of a 256-byte aligned buffer.
 template <typename U>
-__device__ __forceinline__ void store_pair(U* p, int64_t off, U x, U y) {
-  const U v[2] = {x, y};
-  typename PairWord<U>::T w;
-  memcpy(&w, v, sizeof(v));
-  *reinterpret_cast<typename PairWord<U>::T*>(p + off) = w;
+__device__ __forceinline__ void store8u(U* p, bool vec, int n, const U (&v)[8]) {
+  if (vec) {
+    if constexpr (sizeof(U) == 2) {
+      uint4 r;
+      memcpy(&r, v, 16);
+      *reinterpret_cast<uint4*>(p) = r;
+    } else {
+      uint4 r0, r1;
+      memcpy(&r0, v, 16);
+      memcpy(&r1, v + 4, 16);
+      reinterpret_cast<uint4*>(p)[0] = r0;
+      reinterpret_cast<uint4*>(p)[1] = r1;
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < n) p[t] = v[t];
+  }
 }
 
 // Bx from B (see the file header).  B's storage: pair (k, j) at pair offset
 // k + j*ldb (column-major) or k*ldb + j (row-major).  Bx keeps B's layout with
-// leading dimension ldo (even): column-major 2K x 2N, or row-major 2K x 2N.
+// leading dimension ldo (a multiple of 8): column-major 2K x 2N, or row-major
+// 2K x 2N.  Each thread step moves PS_V consecutive pairs of one column (row).
 template <typename U, bool ROW_MAJOR>
 __global__ void __launch_bounds__(PS_THREADS)
-pair_stage_b_kernel(const U* __restrict__ B, int64_t ldb, int64_t K, int64_t N, int dual, int aligned,
+pair_stage_b_kernel(const U* __restrict__ B, int64_t ldb, int64_t K, int64_t N, int dual, int vec_in,
                     U* __restrict__ out, int64_t ldo) {
   const int64_t n_outer = ROW_MAJOR ? K : N, n_inner = ROW_MAJOR ? N : K;
-  const int64_t step = (int64_t)gridDim.x * PS_THREADS;
+  const int64_t step = (int64_t)gridDim.x * PS_THREADS * PS_V;
   for (int64_t o = blockIdx.y; o < n_outer; o += gridDim.y) {
-    for (int64_t in = (int64_t)blockIdx.x * PS_THREADS + threadIdx.x; in < n_inner; in += step) {
-      U c, d;
-      load_pair(B, o * ldb + in, aligned != 0, c, d);
-      const U ud = dual ? (U)0 : (U)(d ^ PairWord<U>::SIGN);   // u^2 * d
-      if constexpr (ROW_MAJOR) {   // o = k, in = j: rows 2k and 2k+1, columns 2j and 2j+1
-        store_pair(out, (2 * o) * ldo + 2 * in, c, d);
-        store_pair(out, (2 * o + 1) * ldo + 2 * in, ud, c);
-      } else {                     // o = j, in = k: columns 2j and 2j+1, rows 2k and 2k+1
-        store_pair(out, (2 * o) * ldo + 2 * in, c, ud);
-        store_pair(out, (2 * o + 1) * ldo + 2 * in, d, c);
+    for (int64_t in = ((int64_t)blockIdx.x * PS_THREADS + threadIdx.x) * PS_V; in < n_inner; in += step) {
+      const int n = n_inner - in < PS_V ? (int)(n_inner - in) : PS_V;
+      const bool full = n == PS_V;
+      U x[8];   // PS_V pairs: c0 d0 c1 d1 ...
+      load8u(B + 2 * (o * ldb + in), full && vec_in != 0, 2 * n, x);
+      U r0[8], r1[8];
+#pragma unroll
+      for (int t = 0; t < PS_V; ++t) {
+        const U c = x[2 * t], d = x[2 * t + 1];
+        const U ud = dual ? (U)0 : (U)(d ^ Sign<U>::BIT);   // u^2 * d
+        if constexpr (ROW_MAJOR) {   // rows 2k and 2k+1 of Bx, columns 2j and 2j+1
+          r0[2 * t] = c;  r0[2 * t + 1] = d;
+          r1[2 * t] = ud; r1[2 * t + 1] = c;
+        } else {                     // columns 2j and 2j+1 of Bx, rows 2k and 2k+1
+          r0[2 * t] = c;  r0[2 * t + 1] = ud;
+          r1[2 * t] = d;  r1[2 * t + 1] = c;
+        }
       }
+      store8u(out + (2 * o) * ldo + 2 * in, full, 2 * n, r0);
+      store8u(out + (2 * o + 1) * ldo + 2 * in, full, 2 * n, r1);
     }
   }
 }
 
 // Ax from A: row-major A is copied to a row-major M x 2K matrix (leading
-// dimension lds, even); column-major A is split into a column-major M x 2K
-// matrix (real parts in column 2k, u parts in column 2k+1, leading dimension lds).
+// dimension lds, a multiple of 8); column-major A is split into a column-major
+// M x 2K matrix (real parts in column 2k, u parts in column 2k+1, leading
+// dimension lds).  Each thread step moves PS_V (row-major) or 2*PS_V
+// (column-major) consecutive pairs.
 template <typename U, bool ROW_MAJOR>
 __global__ void __launch_bounds__(PS_THREADS)
-pair_stage_a_kernel(const U* __restrict__ A, int64_t lda, int64_t M, int64_t K, int aligned,
+pair_stage_a_kernel(const U* __restrict__ A, int64_t lda, int64_t M, int64_t K, int vec_in,
                     U* __restrict__ out, int64_t lds) {
+  constexpr int V = ROW_MAJOR ? PS_V : 2 * PS_V;
   const int64_t n_outer = ROW_MAJOR ? M : K, n_inner = ROW_MAJOR ? K : M;
-  const int64_t step = (int64_t)gridDim.x * PS_THREADS;
+  const int64_t step = (int64_t)gridDim.x * PS_THREADS * V;
   for (int64_t o = blockIdx.y; o < n_outer; o += gridDim.y) {
-    for (int64_t in = (int64_t)blockIdx.x * PS_THREADS + threadIdx.x; in < n_inner; in += step) {
-      U re, im;
-      load_pair(A, o * lda + in, aligned != 0, re, im);
-      if constexpr (ROW_MAJOR) {   // o = i, in = k
-        store_pair(out, o * lds + 2 * in, re, im);
-      } else {                     // o = k, in = i
-        out[in + (2 * o) * lds] = re;
-        out[in + (2 * o + 1) * lds] = im;
+    for (int64_t in = ((int64_t)blockIdx.x * PS_THREADS + threadIdx.x) * V; in < n_inner; in += step) {
+      const int n = n_inner - in < V ? (int)(n_inner - in) : V;
+      const bool full = n == V;
+      const U* src = A + 2 * (o * lda + in);
+      if constexpr (ROW_MAJOR) {   // o = i, in = k: a plain copy of PS_V pairs
+        U x[8];
+        load8u(src, full && vec_in != 0, 2 * n, x);
+        store8u(out + o * lds + 2 * in, full, 2 * n, x);
+      } else {                     // o = k, in = i: 8 pairs -> 8 real parts and 8 u parts
+        U x0[8], x1[8];
+        load8u(src, full && vec_in != 0, min(2 * n, 8), x0);
+        load8u(src + 8, full && vec_in != 0, max(2 * n - 8, 0), x1);
+        U re[8], im[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          re[t] = x0[2 * t];     im[t] = x0[2 * t + 1];
+          re[4 + t] = x1[2 * t]; im[4 + t] = x1[2 * t + 1];
+        }
+        store8u(out + in + (2 * o) * lds, full, n, re);
+        store8u(out + in + (2 * o + 1) * lds, full, n, im);
       }
     }
   }
 }
 
-dim3 stage_grid(int64_t n_outer, int64_t n_inner) {
-  const int64_t gx = std::min<int64_t>((n_inner + PS_THREADS - 1) / PS_THREADS, 64);
+dim3 stage_grid(int64_t n_outer, int64_t n_inner, int per_thread) {
+  const int64_t chunk = (int64_t)PS_THREADS * per_thread;
+  const int64_t gx = std::min<int64_t>((n_inner + chunk - 1) / chunk, 64);
   const int64_t gy = std::min<int64_t>(n_outer, std::max<int64_t>(1, 4096 / gx));
   return dim3((unsigned)std::max<int64_t>(gx, 1), (unsigned)std::min<int64_t>(gy, 65535));
 }
@@ -117,8 +160,9 @@ dim3 stage_grid(int64_t n_outer, int64_t n_inner) {
 cudaError_t launch_pair_stage_b(const void* B, int64_t ldb, int b_row_major, int64_t K, int64_t N, int elem_bytes,
                                 int dual, void* out, int64_t ldo, cudaStream_t stream) {
   if (K <= 0 || N <= 0) return cudaSuccess;
-  const int aligned = (reinterpret_cast<uintptr_t>(B) % (2 * elem_bytes)) == 0;
-  const dim3 grid = b_row_major ? stage_grid(K, N) : stage_grid(N, K);
+  // 16-byte vectors when every column (row) of B starts 16-byte aligned.
+  const int aligned = (reinterpret_cast<uintptr_t>(B) % 16) == 0 && (ldb * 2 * elem_bytes) % 16 == 0;
+  const dim3 grid = b_row_major ? stage_grid(K, N, PS_V) : stage_grid(N, K, PS_V);
   if (elem_bytes == 2) {
     const uint16_t* b = static_cast<const uint16_t*>(B);
     uint16_t* o = static_cast<uint16_t*>(out);
@@ -138,8 +182,8 @@ cudaError_t launch_pair_stage_b(const void* B, int64_t ldb, int b_row_major, int
 cudaError_t launch_pair_stage_a(const void* A, int64_t lda, int a_row_major, int64_t M, int64_t K, int elem_bytes,
                                 void* out, int64_t lds, cudaStream_t stream) {
   if (M <= 0 || K <= 0) return cudaSuccess;
-  const int aligned = (reinterpret_cast<uintptr_t>(A) % (2 * elem_bytes)) == 0;
-  const dim3 grid = a_row_major ? stage_grid(M, K) : stage_grid(K, M);
+  const int aligned = (reinterpret_cast<uintptr_t>(A) % 16) == 0 && (lda * 2 * elem_bytes) % 16 == 0;
+  const dim3 grid = a_row_major ? stage_grid(M, K, PS_V) : stage_grid(K, M, 2 * PS_V);
   if (elem_bytes == 2) {
     const uint16_t* a = static_cast<const uint16_t*>(A);
     uint16_t* o = static_cast<uint16_t*>(out);
