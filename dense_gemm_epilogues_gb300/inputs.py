@@ -63,6 +63,7 @@ class Problem:
     bias_mode: str = "none"      # 'none' | 'col' | 'row'
     act: str = "none"            # 'none' | 'relu'
     c_act: str = "none"          # transform of C as it is read: 'none' | 'relu'
+    out_scale: float = 1.0       # int8 output of an int8 problem: requantisation scale
     dist_a: Dist = U11
     dist_b: Dist = U11
     dist_c: Dist = Dist("normal", std=1.0)

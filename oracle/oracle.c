@@ -45,6 +45,11 @@
  *     the fp64 value in one step; fp32 output uses C's double->float conversion,
  *     which is the same rounding.  int32 output keeps the low 32 bits of the
  *     int64 value and counts every value outside the int32 range.
+ *   - int8 output of an int8 problem (the requantising cast): the int32 result v
+ *     (low 32 bits, as above) is converted to fp32, multiplied by the fp32 scale
+ *     out_scale, rounded to the nearest integer with ties to even, and saturated
+ *     to [-128, 127].  The product is formed in fp32 on purpose: a floating step
+ *     that decides an integer is taken in the precision the library takes it in.
  */
 #include <math.h>
 #include <stdint.h>
@@ -193,6 +198,7 @@ typedef struct {
     int64_t lda, ldb, ldc, ldd;
     int c_dtype, bias_dtype, bias_mode, act, d_dtype;
     int c_act;   /* transform applied to each C element as it is read */
+    double out_scale;   /* int8 output: requantisation scale (applied in fp32) */
 } problem_t;
 
 static int is_int_problem(const problem_t* p) { return p->ab_dtype == OR_S8; }
@@ -239,6 +245,18 @@ static void store_float(int dtype, void* D, int64_t idx, double v) {
 /* Returns 1 when v does not fit int32 (the low 32 bits are stored anyway). */
 static int store_int(void* D, int64_t idx, int64_t v) {
     ((int32_t*)D)[idx] = (int32_t)(uint32_t)(uint64_t)v;
+    return (v < INT32_MIN || v > INT32_MAX) ? 1 : 0;
+}
+
+/* The output of an int problem: int32, or int8 requantised (see the header). */
+static int store_int_out(const problem_t* p, void* D, int64_t idx, int64_t v) {
+    if (p->d_dtype != OR_S8) return store_int(D, idx, v);
+    const int32_t v32 = (int32_t)(uint32_t)(uint64_t)v;
+    const float prod = (float)v32 * (float)p->out_scale;    /* both roundings to nearest even, in fp32 */
+    float r = nearbyintf(prod);                             /* ties to even (default rounding mode) */
+    if (r > 127.0f) r = 127.0f;
+    if (r < -128.0f) r = -128.0f;
+    ((int8_t*)D)[idx] = (int8_t)r;
     return (v < INT32_MIN || v > INT32_MAX) ? 1 : 0;
 }
 
@@ -307,7 +325,7 @@ static int64_t dot_int(const problem_t* p, int64_t i, int64_t j) {
 
 /* One output element in the dot-product order: sum over k for fixed (i, j). */
 static int64_t element_ijk(const problem_t* p, int64_t i, int64_t j, void* D, int64_t out_idx) {
-    if (is_int_problem(p)) return store_int(D, out_idx, epilogue_int(p, i, j, dot_int(p, i, j)));
+    if (is_int_problem(p)) return store_int_out(p, D, out_idx, epilogue_int(p, i, j, dot_int(p, i, j)));
     store_float(p->d_dtype, D, out_idx, epilogue_float(p, i, j, dot_float(p, i, j)));
     return 0;
 }
@@ -324,7 +342,8 @@ static int valid_problem(const problem_t* p) {
     if (p->bias_mode != OR_BIAS_NONE && p->bias == NULL) return 0;
     if (p->c_act != OR_ACT_NONE && p->c_act != OR_ACT_RELU) return 0;
     if (is_int_problem(p)) {
-        if (p->d_dtype != OR_S32) return 0;
+        if (p->d_dtype != OR_S32 && p->d_dtype != OR_S8) return 0;
+        if (p->d_dtype == OR_S8 && !isfinite(p->out_scale)) return 0;
         if (p->alpha != floor(p->alpha) || p->beta != floor(p->beta)) return 0;
     } else if (p->d_dtype == OR_S32 || p->d_dtype == OR_S8) {
         return 0;
@@ -346,9 +365,9 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
                     double beta, int c_dtype, const void* C, int64_t ldc,
                     int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                     int d_dtype, void* D, int64_t ldd,
-                    int loop_order, int nthreads) {
+                    int loop_order, int nthreads, double out_scale) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
+                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, out_scale};
     if (!valid_problem(&p)) return -1;
     if (M == 0 || N == 0) return 0;
     init_tables();
@@ -372,7 +391,7 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
                                       load_int(ab_dtype, B, b_offset(layout_b, k, j, ldb));
         for (int64_t i = 0; i < M; ++i)
             for (int64_t j = 0; j < N; ++j)
-                overflow += store_int(D, i * ldd + j, epilogue_int(&p, i, j, acc[i * N + j]));
+                overflow += store_int_out(&p, D, i * ldd + j, epilogue_int(&p, i, j, acc[i * N + j]));
         free(acc);
         return overflow;
     }
@@ -401,9 +420,9 @@ int64_t oracle_gemm_entries(int ab_dtype, int layout_a, int layout_b,
                             double beta, int c_dtype, const void* C, int64_t ldc,
                             int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                             int d_dtype, int64_t n_entries, const int64_t* rows, const int64_t* cols,
-                            void* out, int nthreads) {
+                            void* out, int nthreads, double out_scale) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
+                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, out_scale};
     if (!valid_problem(&p)) return -1;
     for (int64_t e = 0; e < n_entries; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
@@ -482,7 +501,7 @@ int64_t oracle_gemm_pairs(int unit, int ab_dtype, int layout_a, int layout_b,
                           int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                           int d_dtype, void* D, int64_t ldd, int nthreads) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
+                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, 1.0};
     if (!valid_pair_problem(&p, unit)) return -1;
     if (M == 0 || N == 0) return 0;
     init_tables();
@@ -503,7 +522,7 @@ int64_t oracle_gemm_pairs_entries(int unit, int ab_dtype, int layout_a, int layo
                                   int d_dtype, int64_t n_entries, const int64_t* rows,
                                   const int64_t* cols, void* out, int nthreads) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act};
+                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, 1.0};
     if (!valid_pair_problem(&p, unit)) return -1;
     for (int64_t e = 0; e < n_entries; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;

@@ -23,14 +23,15 @@ G_BIAS = {"none": G.GEMM_BIAS_NONE, "col": G.GEMM_BIAS_COL, "row": G.GEMM_BIAS_R
 ABS_TOL = 1e-2
 FRO_TOL = 2e-3
 GUARD_ROWS = 3
-SENTINEL = {"f32": float.fromhex("0x1.5p+100"), "f16": 12345.0, "bf16": 1.5e30, "s32": 0x5A5A5A5A}
+SENTINEL = {"f32": float.fromhex("0x1.5p+100"), "f16": 12345.0, "bf16": 1.5e30, "s32": 0x5A5A5A5A,
+            "s8": 0x5A}
 
 
 def _oracle_kwargs(p: I.Problem, inp: I.Inputs) -> dict:
     return dict(beta=p.beta, c_dtype=OR_DT[p.c] if p.c else O.F32, C=inp.C,
                 ldc=p.ldc if p.c else 0, bias_dtype=OR_DT[p.bias] if p.bias else O.F32,
                 bias=inp.bias, bias_mode=OR_BIAS[p.bias_mode], act=OR_ACT[p.act],
-                d_dtype=OR_DT[p.d], c_act=OR_ACT[p.c_act])
+                d_dtype=OR_DT[p.d], c_act=OR_ACT[p.c_act], out_scale=p.out_scale)
 
 
 def oracle_full(inp: I.Inputs) -> np.ndarray:
@@ -61,11 +62,11 @@ def to_f64(x, dtype: str) -> np.ndarray:
 
 
 def check_close(D_gpu: torch.Tensor, D_ref_raw: np.ndarray, d_dtype: str, what: str = ""):
-    if d_dtype == "s32":
+    if d_dtype in ("s32", "s8"):
         got = D_gpu.cpu().numpy().astype(np.int64)
         ref = np.asarray(D_ref_raw).astype(np.int64)
         bad = np.argwhere(got != ref)
-        assert bad.size == 0, f"{what}: {len(bad)} int32 mismatches, first at {bad[:3].tolist()}"
+        assert bad.size == 0, f"{what}: {len(bad)} integer mismatches, first at {bad[:3].tolist()}"
         return
     got = to_f64(D_gpu, d_dtype)
     ref = to_f64(D_ref_raw, d_dtype)
@@ -102,7 +103,8 @@ class DeviceProblem:
                                G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
                                G_BIAS[p.bias_mode],
                                G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE,
-                               G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE)
+                               G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE,
+                               out_scale=p.out_scale)
 
     def run(self, plan: G.Plan, stream=None):
         p = self.p

@@ -31,7 +31,8 @@ def run_oracle(inp: I.Inputs, loop_order=0, nthreads=None):
                     c_dtype=DT[p.c] if p.c else O.F32, C=inp.C, ldc=p.ldc if p.c else 0,
                     bias_dtype=DT[p.bias] if p.bias else O.F32, bias=inp.bias,
                     bias_mode=BIAS[p.bias_mode], act=ACT[p.act], d_dtype=DT[p.d], ldd=p.ldd,
-                    loop_order=loop_order, nthreads=nthreads, c_act=ACT[p.c_act])
+                    loop_order=loop_order, nthreads=nthreads, c_act=ACT[p.c_act],
+                    out_scale=p.out_scale)
     return D[:, :p.N], ovf
 
 
@@ -419,3 +420,52 @@ def test_k_zero_is_epilogue_of_beta_c():
     D, _ = run_oracle(inp)
     v = np.maximum(np.float64(0.5) * inp.C.double().numpy() + inp.bias.double().numpy()[None, :], 0)
     np.testing.assert_array_equal(D, v.astype(np.float32))
+
+
+# ----------------------- int8 output (requantising cast) ---------------------
+# Reading (the pages define no requantisation): q = saturate_int8(rne(fp32(v) *
+# fp32(out_scale))) of the int32 epilogue result v, the product taken in fp32.
+
+def _requant_case(values, scale):
+    """An epilogue-only int8 problem whose int32 results are exactly `values`
+    (A = 0, beta = 1, C = values), requantised with `scale`."""
+    n = len(values)
+    p = I.Problem("rq", "s8", "T", "N", 1, n, 4, beta=1.0, c="s32", d="s8", out_scale=scale,
+                  dist_a=I.Dist("zeros"), dist_b=I.I8)
+    inp = I.generate(p, 60)
+    inp.C = torch.tensor([values], dtype=torch.int32)
+    D, _ = run_oracle(inp)
+    return D[0].tolist()
+
+
+def test_requant_ties_round_to_even_and_saturate():
+    # 5*0.5 = 2.5 -> 2, 7*0.5 = 3.5 -> 4, -5*0.5 = -2.5 -> -2, 3*0.5 = 1.5 -> 2,
+    # 1000 -> 127, -1000 -> -128, 255*0.5 = 127.5 -> 128 -> saturates to 127.
+    assert _requant_case([5, 7, -5, 3, 2000, -2000, 255], 0.5) == [2, 4, -2, 2, 127, -128, 127]
+
+
+def test_requant_product_is_taken_in_fp32():
+    """v = 3*2^23 - 1 is not an fp32 value: it converts to 3*2^23 (ties to even),
+    so v * 2^-24 is 1.5 in fp32 and rounds to 2; in exact arithmetic it is just
+    below 1.5 and would round to 1."""
+    v = 3 * 2**23 - 1
+    assert _requant_case([v, -v], 2.0**-24) == [2, -2]
+
+
+def test_requant_matches_numpy_closed_form():
+    """A random int8 GEMM with C, bias and ReLU: the int8 output equals numpy's
+    int64 matmul, wrapped to int32, converted to float32, times the float32
+    scale, rounded half to even (np.rint) and clipped."""
+    p = I.Problem("rqnp", "s8", "N", "T", 23, 19, 41, alpha=2.0, beta=-1.0, c="s32", d="s8",
+                  bias="s32", bias_mode="col", act="relu", out_scale=0.0123,
+                  dist_a=I.I8, dist_b=I.I8, dist_c=I.Dist("int", -5000, 5000),
+                  dist_bias=I.Dist("int", -3000, 3000))
+    inp = I.generate(p, 61, keep_logical=True)
+    D, _ = run_oracle(inp)
+    a = inp.logical["a"].numpy().astype(np.int64)
+    b = inp.logical["b"].numpy().astype(np.int64)
+    c = inp.logical["c"].numpy().astype(np.int64)
+    v = np.maximum(2 * (a @ b) - c + inp.bias.numpy().astype(np.int64)[None, :], 0)
+    v32 = v.astype(np.int32)
+    q = np.clip(np.rint(v32.astype(np.float32) * np.float32(0.0123)), -128, 127).astype(np.int8)
+    np.testing.assert_array_equal(D, q)

@@ -36,6 +36,12 @@ MUTANTS = {
                      "b_offset(p->layout_b, 1, j, p->ldb) - b0 + 1 : 0;\n    double acc"),
     "bf16_table_is_f16": ("acc += bf16_table[A[ia]] * bf16_table[B[ib]]",
                           "acc += f16_table[A[ia]] * bf16_table[B[ib]]"),
+    # int8 requantising output
+    "requant_in_fp64": ("const float prod = (float)v32 * (float)p->out_scale;    /* both roundings to nearest even, in fp32 */\n    float r = nearbyintf(prod);",
+                        "const double prod = (double)v32 * p->out_scale;\n    float r = (float)nearbyint(prod);"),
+    "requant_no_saturation": ("if (r > 127.0f) r = 127.0f;", ""),
+    "requant_round_half_away": ("float r = nearbyintf(prod);                             /* ties", "float r = roundf(prod);                             /* ties"),
+    "requant_scale_ignored": ("(float)v32 * (float)p->out_scale;", "(float)v32 * 1.0f;"),
     # complex / dual-number GEMM
     "pair_unit_square_sign": ("re += a * c + u2 * (b * d);", "re += a * c - u2 * (b * d);"),
     "pair_dual_as_complex": ("unit == OR_UNIT_IMAGINARY ? -1.0 : 0.0;", "unit == OR_UNIT_IMAGINARY ? -1.0 : -1.0;"),
@@ -61,6 +67,9 @@ PINS = [
     lambda: [T.test_f16_rounding_cases(x, b) for x, b in T.F16_CASES],
     lambda: [T.test_bf16_rounding_cases(x, b) for x, b in T.BF16_CASES],
     lambda: T.test_random_float_within_fp64_rounding_of_exact_sum(),
+    lambda: T.test_requant_ties_round_to_even_and_saturate(),
+    lambda: T.test_requant_product_is_taken_in_fp32(),
+    lambda: T.test_requant_matches_numpy_closed_form(),
     lambda: [TP.test_hand_worked_pairs(c, lay) for c in TP._golden() for lay in TP.LAYOUTS],
     lambda: [TP.test_block_matrix_representation(u, lay) for u in ("complex", "dual")
              for lay in TP.LAYOUTS],
