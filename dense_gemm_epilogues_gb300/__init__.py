@@ -47,7 +47,8 @@ EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host"
 
 class gemm_epilogue_t(ctypes.Structure):
     _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int), ("bias_mode", ctypes.c_int),
-                ("act", ctypes.c_int), ("out_dtype", ctypes.c_int), ("c_act", ctypes.c_int)]
+                ("act", ctypes.c_int), ("out_dtype", ctypes.c_int), ("c_act", ctypes.c_int),
+                ("out_scale", ctypes.c_float)]
 
 
 class gemm_config_t(ctypes.Structure):
@@ -126,8 +127,8 @@ def _epi_ptr(epi: Optional[gemm_epilogue_t]):
 
 def make_epilogue(out_dtype: int, bias: int = 0, bias_dtype: int = GEMM_F32,
                   bias_mode: int = GEMM_BIAS_NONE, act: int = GEMM_ACT_NONE,
-                  c_act: int = GEMM_ACT_NONE) -> gemm_epilogue_t:
-    return gemm_epilogue_t(bias or None, bias_dtype, bias_mode, act, out_dtype, c_act)
+                  c_act: int = GEMM_ACT_NONE, out_scale: float = 1.0) -> gemm_epilogue_t:
+    return gemm_epilogue_t(bias or None, bias_dtype, bias_mode, act, out_dtype, c_act, out_scale)
 
 
 # ---- C entry points, same names ----

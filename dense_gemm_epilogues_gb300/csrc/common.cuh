@@ -38,6 +38,7 @@ struct EpiParams {
   int32_t bias_mode;          // gemm_bias_mode_t
   int32_t relu;
   int32_t c_relu;             // ReLU applied to each C element as it is read
+  float out_scale;            // int8 D: requantisation scale
   int32_t vec_c;              // C rows may be read with 16-byte vectors
   int32_t vec_d;              // D rows may be written with 16-byte vectors
   int32_t read_c;             // beta != 0
@@ -90,6 +91,14 @@ __device__ __forceinline__ void store_float_as(void* p, int dt, int64_t idx, flo
     case GEMM_F16: static_cast<__half*>(p)[idx] = __float2half_rn(v); break;
     default: static_cast<__nv_bfloat16*>(p)[idx] = __float2bfloat16_rn(v); break;
   }
+}
+
+// int8 D of the integer path: saturate_int8(round_half_even(fp32(v) * scale)),
+// with the conversion and the product each rounded to nearest even in fp32.
+__device__ __forceinline__ int8_t requant_s8(int32_t v, float scale) {
+  float r = rintf(__fmul_rn(__int2float_rn(v), scale));
+  r = fminf(fmaxf(r, -128.0f), 127.0f);
+  return (int8_t)__float2int_rn(r);
 }
 
 // Integer epilogue arithmetic wraps modulo 2^32 (done in unsigned to keep it defined).
@@ -253,6 +262,24 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, const E
   if (e.relu) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = x[j] > 0 ? x[j] : 0;
+  }
+  if (e.d_dtype == GEMM_S8) {
+    int8_t* d8 = static_cast<int8_t*>(ptr.D) + m * e.ldd + n_base;
+    int8_t q[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) q[j] = requant_s8(x[j], e.out_scale);
+    if (full && e.vec_d) {
+      uint4 w0, w1;
+      memcpy(&w0, q, 16);
+      memcpy(&w1, q + 16, 16);
+      reinterpret_cast<uint4*>(d8)[0] = w0;
+      reinterpret_cast<uint4*>(d8)[1] = w1;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n_base + j < N) d8[j] = q[j];
+    }
+    return;
   }
   int32_t* d = static_cast<int32_t*>(ptr.D) + m * e.ldd + n_base;
   if (full && e.vec_d) {

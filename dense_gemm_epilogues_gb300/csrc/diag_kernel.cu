@@ -144,7 +144,15 @@ __device__ __forceinline__ void store8_d(void* D, int dt, int64_t idx, bool vec,
   }
 }
 
-__device__ __forceinline__ void store8_d(void* D, int, int64_t idx, bool vec, int n, const int32_t (&v)[8]) {
+__device__ __forceinline__ void store8_d(void* D, int dt, int64_t idx, bool vec, int n, const int32_t (&v)[8],
+                                         float out_scale) {
+  if (dt == GEMM_S8) {   // requantised int8 D
+    int8_t* q = static_cast<int8_t*>(D);
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < n) q[idx + t] = requant_s8(v[t], out_scale);
+    return;
+  }
   int32_t* p = static_cast<int32_t*>(D);
   if (vec && n == 8) {
     st_vec8(p + idx, v);
@@ -276,7 +284,8 @@ __global__ void __launch_bounds__(DG_THREADS) diag_gemm_kernel(const DiagParams 
 #pragma unroll
         for (int u = 0; u < 8; ++u) v[u] = v[u] > (Acc)0 ? v[u] : (Acc)0;
       }
-      store8_d(ptr.D, e.d_dtype, i * e.ldd + j, e.vec_d != 0, n_out, v);
+      if constexpr (IS_INT) store8_d(ptr.D, e.d_dtype, i * e.ldd + j, e.vec_d != 0, n_out, v, e.out_scale);
+      else store8_d(ptr.D, e.d_dtype, i * e.ldd + j, e.vec_d != 0, n_out, v);
     }
   }
 }

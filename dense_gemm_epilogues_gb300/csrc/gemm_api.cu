@@ -90,7 +90,8 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
   const gemm_dtype_t out = out_dtype_of(c, epi);
-  if (ab == GEMM_S8 ? out != GEMM_S32 : !is_float_out(out)) return GEMM_ERR_INVALID_ARG;
+  if (ab == GEMM_S8 ? (out != GEMM_S32 && out != GEMM_S8) : !is_float_out(out)) return GEMM_ERR_INVALID_ARG;
+  if (out == GEMM_S8 && !std::isfinite(epi->out_scale)) return GEMM_ERR_INVALID_ARG;
   if (epi) {
     if (epi->act != GEMM_ACT_NONE && epi->act != GEMM_ACT_RELU) return GEMM_ERR_INVALID_ARG;
     if (epi->c_act != GEMM_ACT_NONE && epi->c_act != GEMM_ACT_RELU) return GEMM_ERR_INVALID_ARG;
@@ -403,6 +404,7 @@ EpiParams make_epi(const gemm_plan* plan, double alpha, double beta, const void*
   e.bias_mode = epi ? epi->bias_mode : GEMM_BIAS_NONE;
   e.relu = (epi && epi->act == GEMM_ACT_RELU) ? 1 : 0;
   e.c_relu = (epi && epi->c_act == GEMM_ACT_RELU) ? 1 : 0;
+  e.out_scale = epi ? epi->out_scale : 1.0f;
   e.vec_c = (e.read_c && aligned16(C) && (ldc * dtype_bytes(plan->c)) % 16 == 0) ? 1 : 0;
   e.vec_d = (aligned16(D) && (ldd * dtype_bytes(out)) % 16 == 0) ? 1 : 0;
   return e;
@@ -533,7 +535,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
 
 extern "C" {
 
-int gemm_abi_version(void) { return 105; }
+int gemm_abi_version(void) { return 106; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {

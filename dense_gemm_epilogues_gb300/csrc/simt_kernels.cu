@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
     if (e.bias_mode == GEMM_BIAS_COL) v = wrap_madd(1, load_as_int(ptr.bias, GEMM_S32, j), v);
     else if (e.bias_mode == GEMM_BIAS_ROW) v = wrap_madd(1, load_as_int(ptr.bias, GEMM_S32, i), v);
     if (e.relu) v = v > 0 ? v : 0;
-    static_cast<int32_t*>(ptr.D)[i * e.ldd + j] = v;
+    if (e.d_dtype == GEMM_S8) static_cast<int8_t*>(ptr.D)[i * e.ldd + j] = requant_s8(v, e.out_scale);
+    else static_cast<int32_t*>(ptr.D)[i * e.ldd + j] = v;
   } else {
     float v = acc * e.alpha;
     if (e.read_c) {

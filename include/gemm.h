@@ -77,6 +77,10 @@ typedef enum {
 /* Fused epilogue.  Order: v = alpha*acc + beta*c_act(C[i,j]) + bias; v = act(v);
  * D[i,j] = cast to out_dtype (round to nearest even).  NULL epilogue pointer
  * means: no bias, no activations, out_dtype equal to the plan's c_dtype.
+ * S8 plans may write int8 D (out_dtype GEMM_S8): the int32 result v is
+ * requantised as D = saturate_int8(round_half_even(fp32(v) * out_scale)), the
+ * product taken in fp32 (the pages define no requantisation; this is the
+ * library's reading).  out_scale is read for that cast only.
  * c_act is the elementwise transform applied to C as it is read ("ReLU on C",
  * "Flexible Performant GEMM Kernels on GPUs", section 5.3, Table 2); it only
  * matters when beta != 0. */
@@ -87,6 +91,7 @@ typedef struct {
     gemm_act_t act;               /* activation of the result (before the cast) */
     gemm_dtype_t out_dtype;       /* dtype of D */
     gemm_act_t c_act;             /* transform of C as it is read (GEMM_ACT_NONE / GEMM_ACT_RELU) */
+    float out_scale;              /* S8 plans with out_dtype GEMM_S8: the requantisation scale (finite) */
 } gemm_epilogue_t;
 
 typedef struct gemm_plan* gemm_plan_t;
@@ -342,8 +347,9 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 105 (gemm_epilogue_t.c_act,
- * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex, gemm_config_t.cluster). */
+/* ABI version of this header (major * 100 + minor): 106 (gemm_epilogue_t.c_act,
+ * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex, gemm_config_t.cluster,
+ * gemm_epilogue_t.out_scale and int8 D). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------
