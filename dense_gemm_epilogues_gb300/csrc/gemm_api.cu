@@ -124,10 +124,16 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
 double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 4096^3 and 1024^3 fp16
 
 // Run a tensor-core problem on CTA pairs?  Both dimensions must exceed one
-// 128-wide tile, and the 256 x 256 tiles must fill at least one wave of pairs
-// (or the stream-K tail, when requested, spreads them over all pairs).
+// 128-wide tile.  Then the choice is the smaller estimated time, counted in
+// 64-deep K blocks of one 128 x 256 tile on one SM (a 256 x 256 pair tile takes
+// the same time on its two SMs):
+//   pairs:      ceil(pair tiles / pairs) waves, plus ~9 us of fixed cost;
+//   single CTA: ceil(tiles / SMs) waves of its best tile width, ~12 % slower per
+//               wave than pairs, plus ~5 us of fixed cost
+// (fixed costs and the ratio measured on 256^3 ... 8192^3 fp16 problems).  The
+// stream-K tail, when requested, spreads pair tiles over all pairs.
 // GEMM_TC_CTA_GROUP=1 never uses pairs; =2 uses them whenever both dimensions allow.
-bool use_pairs(int64_t M, int64_t N, int64_t batch, int pair_clusters) {
+bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters, int sm_count) {
   if (pair_clusters <= 0 || M <= 128 || N <= 128) return false;
   if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) {
     const int v = std::atoi(env);
@@ -136,8 +142,17 @@ bool use_pairs(int64_t M, int64_t N, int64_t batch, int pair_clusters) {
   }
   if (const char* sk = std::getenv("GEMM_STREAM_K"))
     if (std::atoi(sk) != 0) return true;
+  const double kb = (double)((K + 63) / 64);
+  const double us_per_kb = 0.284;   // 512 cycles at ~1.8 GHz
   const int64_t pair_tiles = batch * ((M + 255) / 256) * ((N + 255) / 256);
-  return pair_tiles >= pair_clusters;
+  const double t_pair = (double)((pair_tiles + pair_clusters - 1) / pair_clusters) * kb + 9.0 / us_per_kb;
+  double t_one = 1e300;
+  for (int bn : {256, 128}) {
+    const int64_t tiles = batch * ((M + 127) / 128) * ((N + bn - 1) / bn);
+    const double t = (double)((tiles + sm_count - 1) / sm_count) * kb * tc_tile_cost(bn) * 1.12 + 5.0 / us_per_kb;
+    t_one = std::min(t_one, t);
+  }
+  return t_pair < t_one;
 }
 
 // pair_clusters: co-resident clusters of two CTAs for the CTA-pair kernel on the
@@ -183,7 +198,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
     // same MMA work, but a pair's fixed cost per launch is higher (~9 us against
     // ~5 us measured) and its tiles are four times larger: below one full wave of
     // pairs the single-CTA kernel's finer grid finishes first.
-    if (k == GEMM_KERNEL_TC && use_pairs(M, N, batch, pair_clusters)) k = GEMM_KERNEL_TC_PAIR;
+    if (k == GEMM_KERNEL_TC && use_pairs(M, N, K, batch, pair_clusters, sm_count)) k = GEMM_KERNEL_TC_PAIR;
   }
   (void)la;
   (void)lb;
@@ -275,7 +290,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         if (std::atoi(env) == 512) chunk = 512;
       }
       cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? chunk : 0;
-      const bool pair_int = k == GEMM_KERNEL_TC_INT8 && use_pairs(M, N, batch, pair_clusters);
+      const bool pair_int = k == GEMM_KERNEL_TC_INT8 && use_pairs(M, N, K, batch, pair_clusters, sm_count);
       if (pair_int) {   // exact integer mode on CTA pairs: 256 x 256 tiles
         cfg.bm = 2 * TC_BM;
         cfg.bn = 256;

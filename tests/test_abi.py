@@ -118,8 +118,10 @@ def test_selector_narrow_and_small_shapes():
     assert _sel(N=64, M=16384, K=16384)["bn"] == 128
     cfg = _sel(M=512, N=512, K=512)   # 4 pair tiles: less than a wave of pairs
     assert cfg["kernel"] == G.GEMM_KERNEL_TC and cfg["bm"] == 128
-    cfg = _sel(M=2560, N=2048, K=512)  # 80 pair tiles on 76 pairs
-    assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["tiles"] == 80
+    cfg = _sel(M=2560, N=2048, K=512)  # 80 pair tiles on 76 pairs: a second, nearly empty wave
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC
+    cfg = _sel(M=8192, N=8192, K=1024)  # 1024 pair tiles: 13.5 waves
+    assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["tiles"] == 1024
 
 
 def test_selector_misaligned_operands_use_generic_kernel():

@@ -45,10 +45,23 @@ def test_tc_ragged_alpha_beta(layout, ab, kernel):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_selector_picks_pair_kernel_when_its_tiles_fill_the_pairs(layout):
-    """80 tiles of 256 x 256 (at least one per CTA pair): the selector runs pairs."""
-    p = H.tma_aligned(I.Problem("tc_auto", "f16", layout[0], layout[1], 2560, 2048, 72))
-    H.run_and_check_full(p, 120, expect_kernel=G.GEMM_KERNEL_TC_PAIR)
+def test_selector_picks_pair_kernel_when_it_is_faster(layout):
+    """72 pair tiles (one wave) and K = 7680: the pairs' better per-wave rate
+    outweighs their higher fixed cost, so the selector runs pairs.  Sampled
+    outputs (with tile edges) against the oracle."""
+    p = H.tma_aligned(I.Problem("tc_auto", "f16", layout[0], layout[1], 2048, 2304, 7680, beta=0.5,
+                                c="f32"))
+    inp = I.generate(p, 120)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0 and plan.last_config()["kernel"] == G.GEMM_KERNEL_TC_PAIR
+    dp.check_guards()
+    rows, cols = H.sample_entries(p.M, p.N, 800, 120, 256, 256)
+    got = dp.result()[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    H.check_close(got, H.oracle_entries(inp, rows, cols), p.d, p.name)
+    plan.close()
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
