@@ -332,6 +332,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the
+// stream (if it was launched as a programmatic dependent) start its prologue on
+// free SMs; wait blocks until every prerequisite grid has completed and its
+// memory is visible -- it comes before this kernel's first access to data that
+// an earlier kernel may write (operands, C, D, the error word).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Shared state of a CTA's bounded waits.
 struct WaitCtx {
   volatile int32_t* abort;   // shared: set once any role of the CTA gave up

@@ -133,6 +133,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
   cluster_sync();                                   // tensor memory allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above touches no global data: overlap it with the previous kernel.
+  pdl_launch_dependents();
+  pdl_wait();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   // Integer mode runs whole tiles (the host turns the stream-K tail off for it).
   const int kb_per_unit = INT_MODE ? p.chunk_kb : p.num_kb;
@@ -446,8 +449,20 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
     configured[dev] = true;
   }
   if (clusters <= 0) return cudaErrorInvalidValue;
-  tc_pair_gemm_kernel<INT_MODE, CL><<<CL * clusters, PairThreads<INT_MODE>::THREADS, PAIR_SMEM, stream>>>(p);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous kernel (its prologue overlaps that
+  // kernel's end) -- unless the stream-K tail is on: its CTA pairs wait for each
+  // other, so they must all start together on an otherwise free GPU.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * clusters, 1, 1);
+  cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = PAIR_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = p.sk_first_tile == p.num_tiles ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE, CL>, p);
 }
 
 }  // namespace

@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above touches no global data: overlap it with the previous kernel.
+  pdl_launch_dependents();
+  pdl_wait();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
   const int units_per_tile = p.chunk_kb > 0 ? (p.num_kb + p.chunk_kb - 1) / p.chunk_kb : 1;
@@ -299,8 +302,19 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  tc_gemm_kernel<BN, INT_MODE><<<grid, NUM_THREADS, Cfg::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous kernel: one CTA per SM, none waits
+  // for another, so starting early on free SMs is safe (see pdl_wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, INT_MODE>, p);
 }
 
 }  // namespace
