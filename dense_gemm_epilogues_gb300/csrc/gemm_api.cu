@@ -207,7 +207,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
     case GEMM_KERNEL_TC_PAIR: {
       cfg.bm = 2 * TC_BM;
       cfg.bn = 256;
-      cfg.bk = TC_BK;
+      cfg.bk = tc_pair_k_per_stage();
       cfg.stages = tc_pair_stages();
       cfg.cta_group = 2;
       const int64_t tiles_m = (M + 255) / 256, tiles_n = (N + 255) / 256;
@@ -294,6 +294,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       if (pair_int) {   // exact integer mode on CTA pairs: 256 x 256 tiles
         cfg.bm = 2 * TC_BM;
         cfg.bn = 256;
+        cfg.bk = tc_pair_k_per_stage();
         cfg.stages = tc_pair_stages();
         cfg.cta_group = 2;
         const int64_t ptm = (M + 255) / 256, ptn = (N + 255) / 256;

@@ -49,6 +49,7 @@ cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream);
 // CTA-pair tensor-core kernel (cta_group::2): 256 x 256 tiles per cluster of two CTAs.
 // Tensor-map boxes: A as for 128-row tiles, B as for 128-column tiles.
 int tc_pair_stages();
+int tc_pair_k_per_stage();              // K depth of one pipeline stage (64-deep slabs per stage x 64)
 size_t tc_pair_smem_bytes();
 // cluster_size 4 (floating mode only): two CTA pairs per cluster on a 512 x 256
 // super-tile sharing B by multicast; then tiles_m / num_tiles count super-tiles

@@ -32,12 +32,22 @@ namespace {
 constexpr int PAIR_BN = 256;                            // tile columns (both CTAs)
 constexpr int PAIR_A_BYTES = TC_BM * TC_BK * 2;          // 16 KiB: this CTA's 128 rows of A
 constexpr int PAIR_B_BYTES = (PAIR_BN / 2) * TC_BK * 2;  // 16 KiB: this CTA's half of B
-constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+// One stage holds PAIR_SLABS consecutive 64-deep K blocks (slabs).  Every stage
+// costs one stage-full wait and one tcgen05.commit in the MMA thread, and each of
+// those holds the tensor pipe for a while; two slabs per stage (eight MMAs per
+// commit) keep it busy ~91 % of the time where one slab per stage managed ~83 %
+// (measured at 8192^3).
+#ifndef GEMM_PAIR_SLABS
+#define GEMM_PAIR_SLABS 2
+#endif
+constexpr int PAIR_SLABS = GEMM_PAIR_SLABS;
+constexpr int PAIR_SLAB_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;   // 32 KiB
+constexpr int PAIR_STAGE_BYTES = PAIR_SLABS * PAIR_SLAB_BYTES;  // [A slabs][B slabs]
 constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns of TMEM
 #ifndef GEMM_PAIR_STAGES
-#define GEMM_PAIR_STAGES 6
+#define GEMM_PAIR_STAGES (6 / GEMM_PAIR_SLABS)
 #endif
-constexpr int PAIR_STAGES = GEMM_PAIR_STAGES;           // 32 KiB each
+constexpr int PAIR_STAGES = GEMM_PAIR_STAGES;
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
 constexpr size_t PAIR_SMEM = 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
 
@@ -157,14 +167,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
         const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
         const int n0 = tn * PAIR_BN + (int)rank * (PAIR_BN / 2);    // this CTA's half of B
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += PAIR_SLABS) {
+          const int nsl = kb1 - kb < PAIR_SLABS ? kb1 - kb : PAIR_SLABS;   // K blocks in this stage
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
-          if (leader) mbar_expect_tx(fb_local, 2u * PAIR_STAGE_BYTES);
+          if (leader) mbar_expect_tx(fb_local, 2u * (uint32_t)nsl * PAIR_SLAB_BYTES);
           const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, pair_leader);
-          const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
-          const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
-          const int k0 = kb * TC_BK;
+          const uint32_t st = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+          for (int sl = 0; sl < nsl; ++sl) {
+          const uint32_t sa = st + (uint32_t)(sl * PAIR_A_BYTES);
+          const uint32_t sb = st + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES + sl * PAIR_B_BYTES);
+          const int k0 = (kb + sl) * TC_BK;
           if (p.a_mn_major) {
 #pragma unroll
             for (int h = 0; h < TC_BM / MN_BOX; ++h)
@@ -186,6 +199,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
               tma_load_3d_pair(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
           } else {
             tma_load_3d_pair(sb, &p.tmB, k0, n0, zb, fb);
+          }
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -223,18 +237,24 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * PAIR_BN);
           const int kb_begin = INT_MODE ? kb0 + u * kb_per_unit : kb0;
           const int kb_end = INT_MODE ? min(kb1, kb_begin + kb_per_unit) : kb1;
-          for (int kb = kb_begin; kb < kb_end; ++kb) {
+          for (int kb = kb_begin; kb < kb_end; kb += PAIR_SLABS) {
+            const int nsl = kb_end - kb < PAIR_SLABS ? kb_end - kb : PAIR_SLABS;
             if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
-            const uint32_t sb = sa + (uint32_t)PAIR_A_BYTES;
+            const uint32_t st = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < TC_BK / 16; ++kk) {
-              const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
-                                               : smem_desc_sw128(sa + kk * 32u, 16, 1024);
-              const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
-                                               : smem_desc_sw128(sb + kk * 32u, 16, 1024);
-              tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+            for (int sl = 0; sl < PAIR_SLABS; ++sl) {
+              if (sl >= nsl) break;
+              const uint32_t sa = st + (uint32_t)(sl * PAIR_A_BYTES);
+              const uint32_t sb = st + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES + sl * PAIR_B_BYTES);
+#pragma unroll
+              for (int kk = 0; kk < TC_BK / 16; ++kk) {
+                const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
+                                                 : smem_desc_sw128(sa + kk * 32u, 16, 1024);
+                const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
+                                                 : smem_desc_sw128(sb + kk * 32u, 16, 1024);
+                tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             tc_commit_pair_multicast(empty_bar(stage), CL == 4 ? 0xF : 0x3);   // every CTA it feeds
             if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
@@ -468,6 +488,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
 }  // namespace
 
 int tc_pair_stages() { return PAIR_STAGES; }
+int tc_pair_k_per_stage() { return PAIR_SLABS * TC_BK; }
 size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
 
 int tc_pair_max_clusters(int device) {

@@ -100,7 +100,7 @@ def _sel(ab=G.GEMM_F16, c=G.GEMM_F32, la=G.GEMM_OP_T, lb=G.GEMM_OP_N, M=8192, N=
 def test_selector_large_square_uses_256x256_pair_tiles():
     cfg = _sel()
     assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["cta_group"] == 2
-    assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (256, 256, 64)
+    assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (256, 256, 128)
     assert cfg["tiles"] == 32 * 32 and cfg["grid"] == 152 and cfg["raster"] == 8
 
 
