@@ -124,14 +124,14 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
 double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 4096^3 and 1024^3 fp16
 
 // Run a tensor-core problem on CTA pairs?  Both dimensions must exceed one
-// 128-wide tile.  Then the choice is the smaller estimated time, counted in
-// 64-deep K blocks of one 128 x 256 tile on one SM (a 256 x 256 pair tile takes
-// the same time on its two SMs):
-//   pairs:      ceil(pair tiles / pairs) waves, plus ~9 us of fixed cost;
-//   single CTA: ceil(tiles / SMs) waves of its best tile width, ~12 % slower per
-//               wave than pairs, plus ~5 us of fixed cost
-// (fixed costs and the ratio measured on 256^3 ... 8192^3 fp16 problems).  The
-// stream-K tail, when requested, spreads pair tiles over all pairs.
+// 128-wide tile.  Then the choice is the smaller estimated time:
+//   waves x max(mainloop of a tile, its epilogue) + fixed cost per launch,
+// with a tile's mainloop = K/64 blocks x a per-block time.  Fitted to fp16 runs
+// from 256^3 to 8192^3 and two batches: per 64-deep block 0.323 us for a
+// 256 x 256 pair tile and 0.397 us for a 128 x 256 single-CTA tile (0.77 of that
+// for 128 x 128); epilogues of ~4.4 us (pair tile) and ~3.3 us (single-CTA
+// tile) bound tiles of small K; fixed costs ~8.3 us and ~6.6 us.  The stream-K
+// tail, when requested, spreads pair tiles over all pairs.
 // GEMM_TC_CTA_GROUP=1 never uses pairs; =2 uses them whenever both dimensions allow.
 bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters, int sm_count) {
   if (pair_clusters <= 0 || M <= 128 || N <= 128) return false;
@@ -143,14 +143,14 @@ bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters
   if (const char* sk = std::getenv("GEMM_STREAM_K"))
     if (std::atoi(sk) != 0) return true;
   const double kb = (double)((K + 63) / 64);
-  const double us_per_kb = 0.284;   // 512 cycles at ~1.8 GHz
   const int64_t pair_tiles = batch * ((M + 255) / 256) * ((N + 255) / 256);
-  const double t_pair = (double)((pair_tiles + pair_clusters - 1) / pair_clusters) * kb + 9.0 / us_per_kb;
+  const double t_pair =
+      (double)((pair_tiles + pair_clusters - 1) / pair_clusters) * std::max(kb * 0.323, 4.4) + 8.3;
   double t_one = 1e300;
   for (int bn : {256, 128}) {
     const int64_t tiles = batch * ((M + 127) / 128) * ((N + bn - 1) / bn);
-    const double t = (double)((tiles + sm_count - 1) / sm_count) * kb * tc_tile_cost(bn) * 1.12 + 5.0 / us_per_kb;
-    t_one = std::min(t_one, t);
+    const double per_tile = std::max(kb * 0.397 * tc_tile_cost(bn), 3.3 * (bn / 256.0));
+    t_one = std::min(t_one, (double)((tiles + sm_count - 1) / sm_count) * per_tile + 6.6);
   }
   return t_pair < t_one;
 }
@@ -277,7 +277,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       }
       cfg.bm = TC_BM;
       cfg.bn = bn;
-      cfg.bk = TC_BK;
+      cfg.bk = tc_k_per_stage(bn);
       cfg.stages = tc_stages(bn);
       const int64_t tiles_m = (M + 127) / 128, tiles_n = (N + bn - 1) / bn;
       cfg.tiles = (int32_t)std::min<int64_t>(batch * tiles_m * tiles_n, kMaxDim);

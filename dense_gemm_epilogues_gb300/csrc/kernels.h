@@ -43,6 +43,7 @@ constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;   // 16-bit elements: one 128-byte swizzle row
 
 int tc_stages(int bn);
+int tc_k_per_stage(int bn);             // K depth of one pipeline stage of the single-CTA kernel
 size_t tc_smem_bytes(int bn);
 cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream);
 

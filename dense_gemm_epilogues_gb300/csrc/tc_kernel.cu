@@ -35,12 +35,19 @@
 namespace gemmlib {
 namespace {
 
+// A pipeline stage holds SLABS consecutive 64-deep K blocks: one stage-full wait
+// and one tcgen05.commit per SLABS * 4 MMAs (each of those holds the tensor pipe
+// for a while; see the CTA-pair kernel).
+// 128-wide tiles: two slabs in each of 3 stages.  256-wide tiles: one slab in
+// each of 4 stages (two slabs would leave a 2-stage ring, one stage of lookahead:
+// measured 14 % slower at 8192^3).
 template <int BN>
 struct TcCfg {
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr int A_BYTES = TC_BM * TC_BK * 2;   // 16 KiB
-  static constexpr int B_BYTES = BN * TC_BK * 2;      // 32 KiB (BN=256) / 16 KiB (BN=128)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SLABS = (BN == 256) ? 1 : 2;
+  static constexpr int STAGES = ((BN == 256) ? 4 : 6) / SLABS;
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;   // 16 KiB per slab
+  static constexpr int B_BYTES = BN * TC_BK * 2;      // 32 KiB (BN=256) / 16 KiB (BN=128) per slab
+  static constexpr int STAGE_BYTES = SLABS * (A_BYTES + B_BYTES);   // [A slabs][B slabs]
   static constexpr int ACC_BUFS = 512 / BN;           // accumulators in the 512 TMEM columns
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
@@ -146,13 +153,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         tile_coords(t, p, bz, tm, tn);
         const int m0 = tm * TC_BM, n0 = tn * BN;
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb0 = 0; kb0 < p.num_kb; kb0 += Cfg::SLABS) {
+          // A unit of the exact integer mode spans an even number of K blocks, so
+          // stages never straddle two units.
+          const int nsl = p.num_kb - kb0 < Cfg::SLABS ? p.num_kb - kb0 : Cfg::SLABS;
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
-          mbar_expect_tx(fb, (uint32_t)Cfg::STAGE_BYTES);
-          const uint32_t sa = base + (uint32_t)(stage * Cfg::STAGE_BYTES);
-          const uint32_t sb = sa + (uint32_t)Cfg::A_BYTES;
-          const int k0 = kb * TC_BK;
+          mbar_expect_tx(fb, (uint32_t)(nsl * (Cfg::A_BYTES + Cfg::B_BYTES)));
+          const uint32_t st = base + (uint32_t)(stage * Cfg::STAGE_BYTES);
+          for (int sl = 0; sl < nsl; ++sl) {
+          const uint32_t sa = st + (uint32_t)(sl * Cfg::A_BYTES);
+          const uint32_t sb = st + (uint32_t)(Cfg::SLABS * Cfg::A_BYTES + sl * Cfg::B_BYTES);
+          const int k0 = (kb0 + sl) * TC_BK;
           if (p.a_mn_major) {
 #pragma unroll
             for (int h = 0; h < TC_BM / MN_BOX; ++h)
@@ -166,6 +178,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
               tma_load_3d(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
           } else {
             tma_load_3d(sb, &p.tmB, k0, n0, zb, fb);
+          }
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -191,20 +204,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
           const int kb_begin = u * kb_per_unit;
           const int kb_end = min(p.num_kb, kb_begin + kb_per_unit);
-          for (int kb = kb_begin; kb < kb_end; ++kb) {
+          for (int kb = kb_begin; kb < kb_end; kb += Cfg::SLABS) {
+            const int nsl = kb_end - kb < Cfg::SLABS ? kb_end - kb : Cfg::SLABS;
             if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = base + (uint32_t)(stage * Cfg::STAGE_BYTES);
-            const uint32_t sb = sa + (uint32_t)Cfg::A_BYTES;
+            const uint32_t st = base + (uint32_t)(stage * Cfg::STAGE_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < TC_BK / 16; ++kk) {
-              // K-major: the 16-element K step is 32 bytes inside each 128-byte row.
-              // MN-major: it is 16 rows of 128 bytes; LBO steps between 64-wide MN boxes.
-              const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
-                                               : smem_desc_sw128(sa + kk * 32u, 16, 1024);
-              const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
-                                               : smem_desc_sw128(sb + kk * 32u, 16, 1024);
-              tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+            for (int sl = 0; sl < Cfg::SLABS; ++sl) {
+              if (sl >= nsl) break;
+              const uint32_t sa = st + (uint32_t)(sl * Cfg::A_BYTES);
+              const uint32_t sb = st + (uint32_t)(Cfg::SLABS * Cfg::A_BYTES + sl * Cfg::B_BYTES);
+#pragma unroll
+              for (int kk = 0; kk < TC_BK / 16; ++kk) {
+                // K-major: the 16-element K step is 32 bytes inside each 128-byte row.
+                // MN-major: it is 16 rows of 128 bytes; LBO steps between 64-wide MN boxes.
+                const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
+                                                 : smem_desc_sw128(sa + kk * 32u, 16, 1024);
+                const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
+                                                 : smem_desc_sw128(sb + kk * 32u, 16, 1024);
+                tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             tc_commit(empty_bar(stage));
             if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1u; }
@@ -320,6 +339,7 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
 }  // namespace
 
 int tc_stages(int bn) { return bn == 256 ? TcCfg<256>::STAGES : TcCfg<128>::STAGES; }
+int tc_k_per_stage(int bn) { return (bn == 256 ? TcCfg<256>::SLABS : TcCfg<128>::SLABS) * TC_BK; }
 size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>::SMEM; }
 
 cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream) {
