@@ -49,7 +49,9 @@ constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns 
 #endif
 constexpr int PAIR_STAGES = GEMM_PAIR_STAGES;
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
-constexpr size_t PAIR_SMEM = 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
+constexpr int PAIR_OUT_STAGE_BYTES = 4 * 4096;   // a 32 x 32 output turn-around buffer per floating epilogue warp
+constexpr size_t PAIR_SMEM =
+    1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_OUT_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
 
 // Producer warp, MMA warp, then 4 epilogue warps (floating) or 8 (exact integer).
 template <bool INT_MODE>
@@ -100,9 +102,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;   // same offset in both CTAs
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bar0 = base + (uint32_t)(PAIR_STAGES * PAIR_STAGE_BYTES);
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(base_ptr + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
+  const uint32_t out_stage0 = base + (uint32_t)(PAIR_STAGES * PAIR_STAGE_BYTES);
+  const uint32_t bar0 = out_stage0 + (uint32_t)PAIR_OUT_STAGE_BYTES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + PAIR_STAGES * PAIR_STAGE_BYTES +
+                                                    PAIR_OUT_STAGE_BYTES + PAIR_NUM_BARS * 8);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -406,7 +409,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] *= p.epi.alpha;
-            epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x);
+            epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x,
+                                   out_stage0 + (uint32_t)((warp - 2) * 4096), p.M);
           }
           tc_fence_before();
           __syncwarp();

@@ -50,7 +50,8 @@ struct TcCfg {
   static constexpr int STAGE_BYTES = SLABS * (A_BYTES + B_BYTES);   // [A slabs][B slabs]
   static constexpr int ACC_BUFS = 512 / BN;           // accumulators in the 512 TMEM columns
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr int OUT_STAGE_BYTES = 4 * 4096;   // a 32 x 32 output turn-around buffer per epilogue warp
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_STAGE_BYTES + NUM_BARS * 8 + 16;
 };
 
 constexpr int NUM_THREADS = 192;      // producer warp, MMA warp, 4 epilogue warps
@@ -99,9 +100,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;       // swizzle atoms need 1024-byte alignment
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bar0 = base + (uint32_t)(Cfg::STAGES * Cfg::STAGE_BYTES);
+  const uint32_t out_stage0 = base + (uint32_t)(Cfg::STAGES * Cfg::STAGE_BYTES);
+  const uint32_t bar0 = out_stage0 + (uint32_t)Cfg::OUT_STAGE_BYTES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES +
-                                                    Cfg::NUM_BARS * 8);
+                                                    Cfg::OUT_STAGE_BYTES + Cfg::NUM_BARS * 8);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -290,7 +292,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           float x[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
-          epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x);
+          epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x,
+                                 out_stage0 + (uint32_t)((warp - 2) * 4096), p.M);
         }
         tc_fence_before();
         __syncwarp();
