@@ -54,7 +54,7 @@ class gemm_epilogue_t(ctypes.Structure):
 class gemm_config_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kernel", "bm", "bn", "bk", "stages", "cta_group", "split_k", "raster", "grid",
-                 "k_chunk", "tiles", "sk_tiles", "cluster")]
+                 "k_chunk", "tiles", "sk_tiles", "cluster", "half_tiles")]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}

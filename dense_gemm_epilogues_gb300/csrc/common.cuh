@@ -614,21 +614,35 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 // cluster c takes the contiguous range [c*W/G, (c+1)*W/G).  A segment is one
 // tile's share of a range: K blocks [kb0, kb1).
 struct SegmentIter {
-  int G, T, t_dp, KB;
+  int G, T, t_dp, KB, t_half;
   int t;                 // next whole tile of this cluster
+  int u;                 // next half unit of this cluster
   int64_t L, L1;         // remaining linear range of this cluster
-  __device__ __forceinline__ SegmentIter(int cid, int G_, int T_, int t_dp_, int KB_)
-      : G(G_), T(T_), t_dp(t_dp_), KB(KB_), t(cid) {
+  // Tiles t_half ... T-1 (only without a stream-K tail, t_dp == T) run as two
+  // units of half their columns each, unit 2(t - t_half) + h being half h of
+  // tile t; with 2 (T - t_half) <= G each cluster runs at most one of them.
+  __device__ __forceinline__ SegmentIter(int cid, int G_, int T_, int t_dp_, int KB_, int t_half_)
+      : G(G_), T(T_), t_dp(t_dp_), KB(KB_), t_half(t_half_), t(cid), u(cid) {
     const int64_t W = (int64_t)(T - t_dp) * KB;
     L = (int64_t)cid * W / G;
     L1 = (int64_t)(cid + 1) * W / G;
   }
-  __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
-    if (t < t_dp) {
+  // half: -1 for a whole tile (or a stream-K segment), else the column half.
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1, int& half) {
+    half = -1;
+    if (t < t_dp && t < t_half) {
       tile = t;
       kb0 = 0;
       kb1 = KB;
       t += G;
+      return true;
+    }
+    if (u < 2 * (T - t_half)) {
+      tile = t_half + u / 2;
+      half = u & 1;
+      kb0 = 0;
+      kb1 = KB;
+      u += G;
       return true;
     }
     if (L < L1) {

@@ -133,6 +133,19 @@ double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 40
 // tile) bound tiles of small K; fixed costs ~8.3 us and ~6.6 us.  The stream-K
 // tail, when requested, spreads pair tiles over all pairs.
 // GEMM_TC_CTA_GROUP=1 never uses pairs; =2 uses them whenever both dimensions allow.
+// Tail halves of the CTA-pair kernel: T tiles over G pairs leave a last wave of
+// r = T mod G tiles.  When 2r <= G those r tiles run as 2r units of 256 x 128
+// (half the columns, half the MMA work each), one per pair, so the last wave
+// takes half a tile's time.  Returns the number of tiles so split (0: none).
+// GEMM_TC_TAIL_HALVES=0 turns it off.
+int64_t pair_tail_halves(int64_t T, int64_t G) {
+  if (G <= 0) return 0;
+  if (const char* env = std::getenv("GEMM_TC_TAIL_HALVES"))
+    if (std::atoi(env) == 0) return 0;
+  const int64_t r = T % G;
+  return (r > 0 && 2 * r <= G) ? r : 0;
+}
+
 bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters, int sm_count) {
   if (pair_clusters <= 0 || M <= 128 || N <= 128) return false;
   if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) {
@@ -144,8 +157,15 @@ bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters
     if (std::atoi(sk) != 0) return true;
   const double kb = (double)((K + 63) / 64);
   const int64_t pair_tiles = batch * ((M + 255) / 256) * ((N + 255) / 256);
+  // A split tail wave costs about half a tile; the estimate counts it only behind
+  // at least one whole wave (single partial waves are where the time model's
+  // fixed costs were calibrated, and the kernel's own choice between halves and
+  // whole tiles does not change which kernel is faster there).
+  const double tail = pair_tiles % pair_clusters == 0 ? 0.0
+                      : (pair_tiles >= pair_clusters && pair_tail_halves(pair_tiles, pair_clusters) > 0) ? 0.5
+                                                                                                          : 1.0;
   const double t_pair =
-      (double)((pair_tiles + pair_clusters - 1) / pair_clusters) * std::max(kb * 0.323, 4.4) + 8.3;
+      ((double)(pair_tiles / pair_clusters) + tail) * std::max(kb * 0.323, 4.4) + 8.3;
   double t_one = 1e300;
   for (int bn : {256, 128}) {
     const int64_t tiles = batch * ((M + 127) / 128) * ((N + bn - 1) / bn);
@@ -248,6 +268,10 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         else if (v == 4) quad = !sk && quad_clusters > 0 && tiles_m >= 2;
       }
       cfg.cluster = 2;
+      if (!sk && !quad) {
+        cfg.half_tiles = (int32_t)pair_tail_halves(T, G);
+        if (cfg.half_tiles > 0) cfg.grid = 2 * (int32_t)std::min<int64_t>(T + cfg.half_tiles, G);
+      }
       if (quad) {
         cfg.cluster = 4;
         const int64_t super_tiles = batch * ((tiles_m + 1) / 2) * tiles_n;
@@ -504,6 +528,15 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   if (!b_mn) ok = encode_3d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, quad ? 64 : 128);
   else ok = encode_3d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, bt.sb, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
+  // Half-tile units load 64 columns of B per CTA: K-major boxes of 64 rows (an
+  // MN-major box is already 64 columns wide).
+  const bool halves = cfg.half_tiles > 0 && chunk_kb == 0 && !quad && cfg.sk_tiles == 0;
+  if (halves && !b_mn) {
+    if (!encode_3d(&tp.tmBh, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, 64))
+      return GEMM_ERR_CUDA;
+  } else {
+    tp.tmBh = tp.tmB;
+  }
   tp.M = (int32_t)M;
   tp.N = (int32_t)N;
   tp.K = (int32_t)K;
@@ -519,11 +552,14 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   tp.a_mn_major = a_mn ? 1 : 0;
   tp.b_mn_major = b_mn ? 1 : 0;
   tp.idesc = make_idesc(bf16, 256, a_mn, b_mn, 256);
+  tp.idesc_half = make_idesc(bf16, 128, a_mn, b_mn, 256);
   tp.chunk_kb = chunk_kb;
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
   tp.sk_first_tile = tp.num_tiles;
+  tp.half_first_tile = tp.num_tiles;
+  if (halves && cfg.half_tiles <= tp.num_tiles) tp.half_first_tile = tp.num_tiles - cfg.half_tiles;
   if (cfg.sk_tiles > 0 && chunk_kb == 0) {
     const int clusters = cfg.grid / 2;
     const size_t part_bytes = (size_t)clusters * 2 * TC_BM * 256 * sizeof(float);
@@ -551,7 +587,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
 
 extern "C" {
 
-int gemm_abi_version(void) { return 106; }
+int gemm_abi_version(void) { return 107; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {

@@ -15,6 +15,7 @@ namespace gemmlib {
 struct TcParams {
   CUtensorMap tmA;        // A tiles (see tc_kernel.cu for the box shapes)
   CUtensorMap tmB;        // B tiles
+  CUtensorMap tmBh;       // CTA-pair kernel: B boxes of half the columns, for half-tile units
   int32_t M, N, K;
   int32_t num_kb;         // K blocks of 64 elements
   int32_t tiles_m, tiles_n, num_tiles;
@@ -25,6 +26,8 @@ struct TcParams {
   int32_t a_mn_major;     // A stored M-contiguous (layout N) rather than K-contiguous
   int32_t b_mn_major;     // B stored N-contiguous (layout T) rather than K-contiguous
   uint32_t idesc;         // tcgen05 instruction descriptor
+  uint32_t idesc_half;    // CTA-pair kernel: the same for half-tile units (N = 128)
+  int32_t half_first_tile;  // CTA-pair kernel: tiles from here on run as two column halves (num_tiles: none)
   int32_t chunk_kb;       // > 0: exact integer mode, K blocks per fp32 chunk
   EpiParams epi;
   int32_t* err;

@@ -158,23 +158,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
     if (lane == 0) {
       tma_prefetch_desc(&p.tmA);
       tma_prefetch_desc(&p.tmB);
+      if (p.half_first_tile < p.num_tiles) tma_prefetch_desc(&p.tmBh);
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
-      SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
-      int tile, kb0, kb1;
-      while (ok && it.next(tile, kb0, kb1)) {
+      SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb, p.half_first_tile);
+      int tile, kb0, kb1, half;
+      while (ok && it.next(tile, kb0, kb1, half)) {
         int bz, tm, tn;
         pair_tile_coords(tile, p, bz, tm, tn);
         if constexpr (CL == 4) tm = 2 * tm + pp;                    // this pair's half of the super-tile
         const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
-        const int n0 = tn * PAIR_BN + (int)rank * (PAIR_BN / 2);    // this CTA's half of B
+        // This CTA's half of B's columns: 128 of a whole tile, 64 of a half-tile unit.
+        const int n0 = half < 0 ? tn * PAIR_BN + (int)rank * (PAIR_BN / 2)
+                                : tn * PAIR_BN + half * (PAIR_BN / 2) + (int)rank * (PAIR_BN / 4);
+        const uint32_t slab_bytes = half < 0 ? (uint32_t)PAIR_SLAB_BYTES : (uint32_t)(PAIR_A_BYTES + PAIR_B_BYTES / 2);
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
         for (int kb = kb0; kb < kb1; kb += PAIR_SLABS) {
           const int nsl = kb1 - kb < PAIR_SLABS ? kb1 - kb : PAIR_SLABS;   // K blocks in this stage
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
-          if (leader) mbar_expect_tx(fb_local, 2u * (uint32_t)nsl * PAIR_SLAB_BYTES);
+          if (leader) mbar_expect_tx(fb_local, 2u * (uint32_t)nsl * slab_bytes);
           const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, pair_leader);
           const uint32_t st = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
           for (int sl = 0; sl < nsl; ++sl) {
@@ -196,6 +200,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
             else
               tma_load_3d_pair_multicast(sb + pp * (PAIR_B_BYTES / 2), &p.tmB, k0, n0 + pp * (PAIR_BN / 4), zb,
                                          fb, mask);
+          } else if (half >= 0) {
+            // 64 columns: one MN-major box, or a K-major box of 64 rows.
+            if (p.b_mn_major) tma_load_3d_pair(sb, &p.tmB, n0, k0, zb, fb);
+            else tma_load_3d_pair(sb, &p.tmBh, k0, n0, zb, fb);
           } else if (p.b_mn_major) {
 #pragma unroll
             for (int h = 0; h < (PAIR_BN / 2) / MN_BOX; ++h)
@@ -228,10 +236,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
       int stage = 0;
       uint32_t phase = 0, acc_it = 0;
       bool ok = true;
-      SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
-      int tile, kb0, kb1;
-      while (ok && it.next(tile, kb0, kb1)) {
+      SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb, p.half_first_tile);
+      int tile, kb0, kb1, half;
+      while (ok && it.next(tile, kb0, kb1, half)) {
         const int units = INT_MODE ? (kb1 - kb0 + kb_per_unit - 1) / kb_per_unit : 1;
+        const uint32_t idesc = half < 0 ? p.idesc : p.idesc_half;   // N = 256, or 128 for a half-tile unit
         for (int u = 0; ok && u < units; ++u) {
           const int buf = (int)(acc_it % PAIR_ACC_BUFS);
           const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
@@ -256,7 +265,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
                                                  : smem_desc_sw128(sa + kk * 32u, 16, 1024);
                 const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
                                                  : smem_desc_sw128(sb + kk * 32u, 16, 1024);
-                tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
               }
             }
             tc_commit_pair_multicast(empty_bar(stage), CL == 4 ? 0xF : 0x3);   // every CTA it feeds
@@ -276,19 +285,21 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t acc_it = 0;
     bool ok = true;
-    SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb);
-    int tile, kb0, kb1;
-    while (ok && it.next(tile, kb0, kb1)) {
+    SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb, p.half_first_tile);
+    int tile, kb0, kb1, half;
+    while (ok && it.next(tile, kb0, kb1, half)) {
       int bz, tm, tn;
       pair_tile_coords(tile, p, bz, tm, tn);
       if constexpr (CL == 4) tm = 2 * tm + pp;
       const int row_in_cta = q * 32 + lane;
       const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + row_in_cta;
-      const int64_t n0 = (int64_t)tn * PAIR_BN;
+      // A half-tile unit's columns start half a tile further and fill half the accumulator.
+      const int64_t n0 = (int64_t)tn * PAIR_BN + (half > 0 ? PAIR_BN / 2 : 0);
+      const int chunks = half < 0 ? PAIR_BN / 32 : PAIR_BN / 64;
       const bool row_ok = m < p.M;
       const EpiPtrs ptr = epi_ptrs(p.epi, bz);
       if constexpr (INT_MODE) {
-        const int half = (warp - 2) >> 2;                     // columns 128*half ... 128*half + 127
+        const int colh = (warp - 2) >> 2;                     // columns 128*colh ... 128*colh + 127
         const int units = (kb1 - kb0 + kb_per_unit - 1) / kb_per_unit;
         int32_t acc[128];
 #pragma unroll
@@ -298,7 +309,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
           const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
           if (!warp_wait_pair(tfull_bar(buf), apar, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN + half * 128);
+          const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * PAIR_BN + colh * 128);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
@@ -318,7 +329,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
         if (!ok) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          epi_finish_row32_int(p.epi, ptr, m, row_ok, n0 + half * 128 + c * 32, p.N, &acc[c * 32]);
+          epi_finish_row32_int(p.epi, ptr, m, row_ok, n0 + colh * 128 + c * 32, p.N, &acc[c * 32]);
       } else {
         const int buf = (int)(acc_it % PAIR_ACC_BUFS);
         const uint32_t apar = (acc_it / PAIR_ACC_BUFS) & 1u;
@@ -388,7 +399,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
             if (!good) cp_last = cp_first - 1;   // results are void; the error word says why
           }
 #pragma unroll 1
-          for (int c = 0; c < PAIR_BN / 32; ++c) {
+          for (int c = 0; c < chunks; ++c) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
             tmem_wait_ld();

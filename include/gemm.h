@@ -123,6 +123,9 @@ typedef struct {
                              all CTA pairs; 0 = every tile runs whole on one CTA pair) */
     int32_t cluster;      /* CTAs per thread-block cluster: 1, 2 (one CTA pair) or 4 (two CTA
                              pairs on vertically adjacent tiles sharing B by TMA multicast) */
+    int32_t half_tiles;   /* CTA-pair kernel: the last half_tiles tiles (a partial last wave
+                             of at most half the CTA pairs) each run as two units of 256 x 128,
+                             on two CTA pairs, so that the last wave takes half a tile's time */
 } gemm_config_t;
 
 /* ---------------------------------------------------------------------------
@@ -347,9 +350,9 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 106 (gemm_epilogue_t.c_act,
+/* ABI version of this header (major * 100 + minor): 107 (gemm_epilogue_t.c_act,
  * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex, gemm_config_t.cluster,
- * gemm_epilogue_t.out_scale and int8 D). */
+ * gemm_epilogue_t.out_scale and int8 D, gemm_config_t.half_tiles). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------

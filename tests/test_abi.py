@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings():
-    assert G.gemm_abi_version() == 106
+    assert G.gemm_abi_version() == 107
     for s in range(6):
         assert G.gemm_status_string(s).startswith("GEMM_")
     assert "unknown" in G.gemm_status_string(99)
@@ -102,6 +102,8 @@ def test_selector_large_square_uses_256x256_pair_tiles():
     assert cfg["kernel"] == G.GEMM_KERNEL_TC_PAIR and cfg["cta_group"] == 2
     assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (256, 256, 128)
     assert cfg["tiles"] == 32 * 32 and cfg["grid"] == 152 and cfg["raster"] == 8
+    # 1024 tiles over 76 pairs: the last 36 (at most half the pairs) run as 72 half tiles.
+    assert cfg["half_tiles"] == 36
 
 
 def test_selector_single_cta_when_one_dimension_fits_one_tile():
