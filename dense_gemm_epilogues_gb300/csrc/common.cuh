@@ -558,6 +558,16 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// The same with an L2 cache policy for the loaded lines (from createpolicy).
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
+                                                      int32_t z, uint32_t bar_cluster_addr, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr), "l"(policy)
+      : "memory");
+}
+
 // The same load delivered to every CTA of `cta_mask` (same shared-memory offset in
 // each); each destination's completion is signalled on the barrier at the same
 // offset in the leader CTA of that destination's pair.
