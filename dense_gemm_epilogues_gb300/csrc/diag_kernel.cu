@@ -40,6 +40,13 @@ __device__ __forceinline__ void ld_vec8(const T* p, T (&v)[8]) {
   } else if constexpr (sizeof(T) == 2) {
     const uint4 r = *reinterpret_cast<const uint4*>(p);
     memcpy(v, &r, 16);
+  } else if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+    // One 32-byte access per lane: a warp's request covers whole 32-byte sectors.
+    uint32_t w[8];
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+    memcpy(v, w, 32);
   } else {
     const uint4 r0 = reinterpret_cast<const uint4*>(p)[0];
     const uint4 r1 = reinterpret_cast<const uint4*>(p)[1];
@@ -54,6 +61,15 @@ __device__ __forceinline__ void st_vec8(T* p, const T (&v)[8]) {
     uint4 r;
     memcpy(&r, v, 16);
     *reinterpret_cast<uint4*>(p) = r;
+  } else if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+    // One 32-byte store per lane writes whole sectors; two 16-byte stores per lane
+    // leave every sector half written by each instruction, which halves the
+    // write bandwidth.
+    uint32_t w[8];
+    memcpy(w, v, 32);
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
   } else {
     uint4 r0, r1;
     memcpy(&r0, v, 16);
