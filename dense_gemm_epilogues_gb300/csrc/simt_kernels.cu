@@ -350,8 +350,12 @@ __global__ void s8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restr
         __half2 v = __halves2half2(__int2half_rn(b[2 * h]), __int2half_rn(b[2 * h + 1]));
         out[h] = *reinterpret_cast<uint32_t*>(&v);
       }
-      reinterpret_cast<uint4*>(d)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-      reinterpret_cast<uint4*>(d)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+      // One 32-byte store (d is 32-byte aligned on this path): each lane writes a
+      // whole sector, where two 16-byte stores would half-write every sector per
+      // warp request and halve the write bandwidth.
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d), "r"(out[0]), "r"(out[1]),
+                   "r"(out[2]), "r"(out[3]), "r"(out[4]), "r"(out[5]), "r"(out[6]), "r"(out[7])
+                   : "memory");
     } else {
       for (int j = 0; j < 16 && c + j < inner; ++j) d[j] = __int2half_rn(s[j]);
     }
