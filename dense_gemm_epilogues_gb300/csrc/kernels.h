@@ -71,8 +71,10 @@ struct FfmaParams {
   int32_t M, N, K;
   EpiParams epi;
 };
+// K slice per shared-memory buffer: 8 (measured 5 % faster than 16 at 4096^3 and
+// 8192^3: half the staging registers, the same one barrier per slice).
 #ifndef GEMM_FFMA_BK
-#define GEMM_FFMA_BK 16
+#define GEMM_FFMA_BK 8
 #endif
 constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = GEMM_FFMA_BK;
 cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, int batch, cudaStream_t stream);

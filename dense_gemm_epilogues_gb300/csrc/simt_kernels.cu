@@ -24,7 +24,7 @@ constexpr int SG_PAD = 4;                       // row padding: conflict-free tr
 constexpr int SG_LDS = FFMA_BM + SG_PAD;        // 132 floats per K row (BM == BN)
 
 // Loads one BK x 128 slice of op(A) (as A^T: [k][m]) or of op(B) ([k][n]) into
-// registers: NV = BK/8 groups of four values per thread.  `KMAJOR`: the operand
+// registers: NV = BK/8 groups of four values per thread (one at BK = 8).  `KMAJOR`: the operand
 // is K-contiguous in global memory (A row-major / B column-major), so a thread
 // loads 4 consecutive K values of one row/column per group; otherwise 4
 // consecutive M/N values of one K row.
