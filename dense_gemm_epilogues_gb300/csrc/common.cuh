@@ -287,6 +287,20 @@ __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, const
   }
 }
 
+// 32 bytes of one row from one thread: a single 32-byte store where the address
+// allows it (each lane of the warp then writes whole 32-byte sectors; two
+// 16-byte stores per lane half-write every sector per request), else two.
+__device__ __forceinline__ void st_row_32b(void* p, const uint32_t* w) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // x[j] holds the exact int32 product sums of columns n_base..n_base+31 of row m;
 // it is finished in place (alpha, beta*C, bias, ReLU) and stored.  Called by all
 // 32 lanes of a warp together, as the floating version.
@@ -341,11 +355,9 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, const E
 #pragma unroll
     for (int j = 0; j < 32; ++j) q[j] = requant_s8(x[j], e.out_scale);
     if (full && e.vec_d) {
-      uint4 w0, w1;
-      memcpy(&w0, q, 16);
-      memcpy(&w1, q + 16, 16);
-      reinterpret_cast<uint4*>(d8)[0] = w0;
-      reinterpret_cast<uint4*>(d8)[1] = w1;
+      uint32_t w[8];
+      memcpy(w, q, 32);
+      st_row_32b(d8, w);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -355,9 +367,8 @@ __device__ __forceinline__ void epi_finish_row32_int(const EpiParams& e, const E
   }
   int32_t* d = static_cast<int32_t*>(ptr.D) + m * e.ldd + n_base;
   if (full && e.vec_d) {
-    int4* d4 = reinterpret_cast<int4*>(d);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) d4[q] = make_int4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    for (int q = 0; q < 4; ++q) st_row_32b(d + 8 * q, reinterpret_cast<const uint32_t*>(x + 8 * q));
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
