@@ -32,6 +32,11 @@ struct gemm_plan {
   void* sk_ws = nullptr;             // stream-K partial accumulators and flags (per cluster and CTA)
   size_t sk_ws_bytes = 0;
   int32_t sk_epoch = 0;
+  // Stream-K of the single-CTA kernel: two fp32 partial slots per CTA, then one
+  // arrival counter per tile (zero between launches; each tile's last arriver
+  // resets its counter).
+  void* sk1_ws = nullptr;
+  size_t sk1_ws_bytes = 0;
   gemm_config_t last{};
   uint64_t timeout_ns = 4000000000ull;
   // gemm_run_host's row-panel pipeline: copy-in and copy-out streams and the
@@ -314,6 +319,27 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         if (std::atoi(env) == 512) chunk = 512;
       }
       cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? chunk : 0;
+      // Stream-K for a wave that leaves SMs idle (floating mode): all CTAs share
+      // the tiles' K blocks evenly and the last arrival on a tile finishes it.
+      // Publishing a partial, the fence and the last arrival's reads cost ~4 µs,
+      // about 20 K blocks of a 128 x 128 tile: taken when it saves at least 48 K
+      // blocks per CTA; GEMM_TC_SPLITK=0 turns it off, =1 forces it when every
+      // CTA gets a K block.
+      if (k == GEMM_KERNEL_TC) {
+        const int64_t T = cfg.tiles, KB = (K + TC_BK - 1) / TC_BK;
+        bool sk1 = T < sm_count && (double)KB * (1.0 - (double)T / sm_count) >= 48.0 && T * KB >= 4 * (int64_t)sm_count;
+        if (const char* env = std::getenv("GEMM_TC_SPLITK")) {
+          const int v = std::atoi(env);
+          if (v == 0) sk1 = false;
+          else if (v == 1) sk1 = T * KB >= sm_count;
+        }
+        if (sk1) {
+          cfg.sk_tiles = (int32_t)T;
+          cfg.grid = sm_count;
+          const int64_t per = std::max<int64_t>(1, T * KB / sm_count);
+          cfg.split_k = (int32_t)std::min<int64_t>((KB + per - 1) / per + 1, KB);
+        }
+      }
       const bool pair_int = k == GEMM_KERNEL_TC_INT8 && use_pairs(M, N, K, batch, pair_clusters, sm_count);
       if (pair_int) {   // exact integer mode on CTA pairs: 256 x 256 tiles
         cfg.bm = 2 * TC_BM;
@@ -504,6 +530,23 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
   tp.sk_first_tile = tp.num_tiles;
+  if (cfg.sk_tiles > 0 && chunk_kb == 0) {
+    // Stream-K over the last sk_tiles tiles: two 128 x bn fp32 partial slots per
+    // CTA, then one arrival counter per tile.
+    const size_t part_bytes = (size_t)cfg.grid * 2 * TC_BM * (size_t)bn * sizeof(float);
+    const size_t need = part_bytes + (size_t)tp.num_tiles * sizeof(int32_t);
+    if (plan->sk1_ws_bytes < need) {
+      if (plan->sk1_ws) cudaFreeAsync(plan->sk1_ws, stream);
+      plan->sk1_ws = nullptr;
+      plan->sk1_ws_bytes = 0;
+      if (cudaMallocAsync(&plan->sk1_ws, need, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+      if (cudaMemsetAsync(plan->sk1_ws, 0, need, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+      plan->sk1_ws_bytes = need;
+    }
+    tp.sk_first_tile = tp.num_tiles - std::min<int32_t>(cfg.sk_tiles, tp.num_tiles);
+    tp.sk_partials = static_cast<float*>(plan->sk1_ws);
+    tp.sk_flags = reinterpret_cast<int32_t*>(static_cast<char*>(plan->sk1_ws) + part_bytes);
+  }
   return launch_tc(tp, bn, cfg.grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -658,6 +701,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
   if (plan->ws) cudaFree(plan->ws);
   if (plan->stage) cudaFree(plan->stage);
   if (plan->sk_ws) cudaFree(plan->sk_ws);
+  if (plan->sk1_ws) cudaFree(plan->sk1_ws);
   if (plan->d_err) cudaFree(plan->d_err);
   if (plan->host_pipe) {
     for (cudaEvent_t e : plan->host_ev) cudaEventDestroy(e);
@@ -698,6 +742,8 @@ gemm_status_t gemm_plan_device_status(gemm_plan_t plan, gemm_stream_t stream, in
   if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
   if (cudaMemcpy(&v, plan->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
   if (cudaMemset(plan->d_err, 0, sizeof(int32_t)) != cudaSuccess) return GEMM_ERR_CUDA;
+  // A launch that gave up may have left stream-K arrival counters counted in.
+  if (v != 0 && plan->sk1_ws && cudaMemset(plan->sk1_ws, 0, plan->sk1_ws_bytes) != cudaSuccess) return GEMM_ERR_CUDA;
   *code = v;
   return GEMM_OK;
 }

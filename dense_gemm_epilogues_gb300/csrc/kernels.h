@@ -32,14 +32,18 @@ struct TcParams {
   EpiParams epi;
   int32_t* err;
   uint64_t timeout_ns;
-  // Stream-K tail (CTA-pair kernel, floating mode): tiles below sk_first_tile
-  // run whole, one per cluster in turn; the K blocks of the remaining tiles are
-  // split into equal contiguous ranges, one per cluster.  sk_first_tile ==
-  // num_tiles turns it off.
+  // Stream-K (floating mode, both tensor-core kernels): tiles below sk_first_tile
+  // run whole, one per cluster (CTA) in turn; the K blocks of the remaining tiles
+  // are split into equal contiguous ranges, one per cluster (CTA).
+  // sk_first_tile == num_tiles turns it off.
   int32_t sk_first_tile;
   int32_t sk_epoch;       // value published in sk_flags by this launch
-  float* sk_partials;     // per cluster and CTA: one 128 x 256 fp32 partial accumulator
-  int32_t* sk_flags;      // per cluster and CTA: epoch of its last published partial
+  // CTA-pair kernel: per cluster and CTA one 128 x 256 fp32 partial accumulator,
+  // and the epoch of its last published partial.  Single-CTA kernel: per CTA two
+  // 128 x BN fp32 partials (the tile its K range starts in, and the other), and
+  // per tile an arrival counter (0 between launches).
+  float* sk_partials;
+  int32_t* sk_flags;
 };
 
 constexpr int TC_BM = 128;

@@ -87,12 +87,41 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 // All lanes of a warp wait; the warp gives up together if any lane gave up.
+// CTA barrier of the four epilogue warps (named barrier 1; barrier 0 is __syncthreads).
+__device__ __forceinline__ void epi_warps_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
   const bool ok = mbar_wait(bar, parity, wc);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <int BN, bool INT_MODE>
+// The work of one CTA: whole tiles in turn (blockIdx.x, + gridDim.x, ...), or
+// with stream-K (SK) whole tiles below sk_first_tile and then its contiguous
+// share of the remaining tiles' K blocks, as (tile, K block range) segments.
+template <bool SK>
+struct TcWork {
+  int t, G, T, KB;
+  __device__ __forceinline__ TcWork(int cid, int G_, int T_, int KB_, int) : t(cid), G(G_), T(T_), KB(KB_) {}
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
+    if (t >= T) return false;
+    tile = t;
+    kb0 = 0;
+    kb1 = KB;
+    t += G;
+    return true;
+  }
+};
+template <>
+struct TcWork<true> {
+  SegmentIter it;
+  __device__ __forceinline__ TcWork(int cid, int G, int T, int KB, int t_dp) : it(cid, G, T, t_dp, KB, T) {}
+  __device__ __forceinline__ bool next(int& tile, int& kb0, int& kb1) {
+    int half;
+    return it.next(tile, kb0, kb1, half);
+  }
+};
+
+template <int BN, bool INT_MODE, bool SK>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   static_assert(!INT_MODE || BN == 128, "exact integer mode keeps 128 int32 accumulators per thread");
   using Cfg = TcCfg<BN>;
@@ -150,15 +179,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      TcWork<SK> it(blockIdx.x, gridDim.x, p.num_tiles, p.num_kb, p.sk_first_tile);
+      int t, kb_lo, kb_hi;
+      while (ok && it.next(t, kb_lo, kb_hi)) {
         int bz, tm, tn;
         tile_coords(t, p, bz, tm, tn);
         const int m0 = tm * TC_BM, n0 = tn * BN;
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-        for (int kb0 = 0; kb0 < p.num_kb; kb0 += Cfg::SLABS) {
+        for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += Cfg::SLABS) {
           // A unit of the exact integer mode spans an even number of K blocks, so
           // stages never straddle two units.
-          const int nsl = p.num_kb - kb0 < Cfg::SLABS ? p.num_kb - kb0 : Cfg::SLABS;
+          const int nsl = kb_hi - kb0 < Cfg::SLABS ? kb_hi - kb0 : Cfg::SLABS;
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
           mbar_expect_tx(fb, (uint32_t)(nsl * (Cfg::A_BYTES + Cfg::B_BYTES)));
@@ -197,15 +228,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       int stage = 0;
       uint32_t phase = 0, acc_it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        for (int u = 0; ok && u < units_per_tile; ++u) {
+      TcWork<SK> it(blockIdx.x, gridDim.x, p.num_tiles, p.num_kb, p.sk_first_tile);
+      int t, kb_lo, kb_hi;
+      while (ok && it.next(t, kb_lo, kb_hi)) {
+        // Integer mode: whole tiles in fp32 chunks of kb_per_unit K blocks.  Floating
+        // mode: one unit, the segment's K blocks (all of them unless stream-K split the tile).
+        const int units = INT_MODE ? units_per_tile : 1;
+        for (int u = 0; ok && u < units; ++u) {
           const int buf = (int)(acc_it % Cfg::ACC_BUFS);
           const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
           if (!mbar_wait(tempty_bar(buf), apar ^ 1u, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-          const int kb_begin = u * kb_per_unit;
-          const int kb_end = min(p.num_kb, kb_begin + kb_per_unit);
+          const int kb_begin = INT_MODE ? u * kb_per_unit : kb_lo;
+          const int kb_end = INT_MODE ? min(p.num_kb, kb_begin + kb_per_unit) : kb_hi;
           for (int kb = kb_begin; kb < kb_end; kb += Cfg::SLABS) {
             const int nsl = kb_end - kb < Cfg::SLABS ? kb_end - kb : Cfg::SLABS;
             if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
@@ -243,9 +279,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // -------------------------------- epilogue --------------------------------
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    volatile int32_t* sk_verdict = abort_flag + 1;   // stream-K: this CTA finishes the tile (1), aborted (2)
     uint32_t acc_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    TcWork<SK> it(blockIdx.x, gridDim.x, p.num_tiles, p.num_kb, p.sk_first_tile);
+    int t, kb_lo, kb_hi;
+    while (ok && it.next(t, kb_lo, kb_hi)) {
       int bz, tm, tn;
       tile_coords(t, p, bz, tm, tn);
       const int64_t m = (int64_t)tm * TC_BM + q * 32 + lane;
@@ -278,6 +317,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         if (!ok) break;
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) epi_finish_row32_int(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, &acc[c * 32]);
+      } else if (SK && (kb_lo > 0 || kb_hi < p.num_kb)) {
+        // Stream-K: this CTA holds K blocks [kb_lo, kb_hi) of tile t, which several
+        // CTAs share.  It publishes its raw fp32 partial, then counts itself in on
+        // the tile; the CTA that arrives last adds every part, in the order of the
+        // K blocks, and runs the epilogue.  No CTA waits for another.  Every
+        // epilogue warp reaches both CTA barriers below, whatever happened before.
+        const int buf = (int)(acc_it % Cfg::ACC_BUFS);
+        const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
+        const bool w_ok = warp_wait(tfull_bar(buf), apar, wc);
+        constexpr int SLOT_FLOATS = TC_BM * BN;
+        const int G = (int)gridDim.x;
+        const int64_t W = (int64_t)(p.num_tiles - p.sk_first_tile) * p.num_kb;
+        const int64_t tl = t - p.sk_first_tile;
+        const int row_in_cta = q * 32 + lane;
+        // Slot 0 of a CTA holds the part of the tile its K range starts in, slot 1 the other.
+        auto slot_of = [&](int cta) {
+          const int64_t start = (int64_t)cta * W / G;
+          return p.sk_partials + (size_t)(cta * 2 + (start / p.num_kb == tl ? 0 : 1)) * SLOT_FLOATS;
+        };
+        if (w_ok) {
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
+          float4* slot = reinterpret_cast<float4*>(slot_of((int)blockIdx.x));
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              __stcg(&slot[(c * 8 + v) * TC_BM + row_in_cta],
+                     make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+        }
+        __threadfence();
+        epi_warps_sync();
+        const int c_first = sk_cluster_of(tl * p.num_kb, W, G);
+        const int c_last = sk_cluster_of(tl * p.num_kb + p.num_kb - 1, W, G);
+        if (warp == 2 && lane == 0) {
+          if (*wc.abort) {
+            *sk_verdict = 2;
+          } else {
+            const int old = atomicAdd(&p.sk_flags[t], 1);
+            *sk_verdict = old == c_last - c_first ? 1 : 0;
+          }
+        }
+        epi_warps_sync();
+        const int verdict = *sk_verdict;
+        if (verdict == 2) { ok = false; break; }
+        if (verdict == 1) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = 0.0f;
+            // Two parts' loads in flight per round trip (the sum keeps the parts' order).
+#pragma unroll 1
+            for (int cc = c_first; cc <= c_last; cc += 2) {
+              const bool two = cc + 1 <= c_last;
+              const float4* s4a = reinterpret_cast<const float4*>(slot_of(cc));
+              const float4* s4b = reinterpret_cast<const float4*>(slot_of(two ? cc + 1 : cc));
+              float4 ya[8], yb[8];
+#pragma unroll
+              for (int v = 0; v < 8; ++v) ya[v] = __ldcg(&s4a[(c * 8 + v) * TC_BM + row_in_cta]);
+              if (two) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) yb[v] = __ldcg(&s4b[(c * 8 + v) * TC_BM + row_in_cta]);
+              }
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                x[4 * v] += ya[v].x;
+                x[4 * v + 1] += ya[v].y;
+                x[4 * v + 2] += ya[v].z;
+                x[4 * v + 3] += ya[v].w;
+              }
+              if (two) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  x[4 * v] += yb[v].x;
+                  x[4 * v + 1] += yb[v].y;
+                  x[4 * v + 2] += yb[v].z;
+                  x[4 * v + 3] += yb[v].w;
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= p.epi.alpha;
+            epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x,
+                                   out_stage0 + (uint32_t)((warp - 2) * 4096), p.M);
+          }
+          // Every part has been counted and read: the counter is ready for the next launch.
+          if (warp == 2 && lane == 0) p.sk_flags[t] = 0;
+        }
+        ++acc_it;
       } else {
         const int buf = (int)(acc_it % Cfg::ACC_BUFS);
         const uint32_t apar = (acc_it / Cfg::ACC_BUFS) & 1u;
@@ -310,7 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int BN, bool INT_MODE>
+template <int BN, bool INT_MODE, bool SK>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
   using Cfg = TcCfg<BN>;
   static_assert(Cfg::SMEM <= 232448, "shared memory budget");
@@ -319,7 +457,7 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, INT_MODE, SK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Cfg::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -336,7 +474,7 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, INT_MODE>, p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, INT_MODE, SK>, p);
 }
 
 }  // namespace
@@ -348,10 +486,11 @@ size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>:
 cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream) {
   if (p.chunk_kb > 0) {
     // exact integer mode keeps 128 int32 accumulators per thread: BN = 128 only
-    return bn == 128 ? launch_bn<128, true>(p, grid, stream) : cudaErrorInvalidValue;
+    return bn == 128 ? launch_bn<128, true, false>(p, grid, stream) : cudaErrorInvalidValue;
   }
-  if (bn == 256) return launch_bn<256, false>(p, grid, stream);
-  if (bn == 128) return launch_bn<128, false>(p, grid, stream);
+  const bool sk = p.sk_first_tile < p.num_tiles;   // stream-K: a separate instance, so whole tiles lose nothing
+  if (bn == 256) return sk ? launch_bn<256, false, true>(p, grid, stream) : launch_bn<256, false, false>(p, grid, stream);
+  if (bn == 128) return sk ? launch_bn<128, false, true>(p, grid, stream) : launch_bn<128, false, false>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 
