@@ -772,6 +772,17 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
   e.stride_c = bt.sc;
   e.stride_d = bt.sd;
   e.stride_bias = bt.sbias;
+  // The CTA-pair kernel's stream-K publishes partials under a per-launch epoch
+  // chosen here on the host; a CUDA graph would replay the same epoch, so while
+  // the stream is being captured the launch runs without stream-K.
+  if (cfg.kernel == GEMM_KERNEL_TC_PAIR && cfg.sk_tiles > 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) {
+      cfg.sk_tiles = 0;
+      cfg.split_k = 1;
+    }
+  }
 
   switch (cfg.kernel) {
     case GEMM_KERNEL_TC_PAIR:

@@ -339,6 +339,36 @@ def test_pair_stream_k_repeated_launches(layout, monkeypatch):
     dp.check_guards()
 
 
+def test_pair_stream_k_off_inside_cuda_graphs(monkeypatch):
+    """The pair kernel's stream-K uses a per-launch epoch chosen on the host, which
+    a graph would replay unchanged: a captured launch runs without stream-K, and
+    every replay is right."""
+    monkeypatch.setenv("GEMM_STREAM_K", "1")
+    p = H.tma_aligned(I.Problem("sk_graph", "f16", "T", "N", 1280, 1536, 1536, alpha=1.25, beta=1.0, c="f32"))
+    inp = I.generate(p, 132)
+    ref = H.oracle_full(inp)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.last_config()["sk_tiles"] > 0
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            dp.run(plan, stream=s.cuda_stream)
+    torch.cuda.synchronize()
+    assert plan.last_config()["sk_tiles"] == 0
+    for _ in range(3):
+        dp.D.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        H.check_close(dp.result(), ref, "f32", "stream-K under graph replay")
+    dp.check_guards()
+    plan.close()
+
+
 # ------------------------- transform of C as it is read ----------------------
 
 @pytest.mark.parametrize("kernel,ab", [(G.GEMM_KERNEL_TC_PAIR, "f16"), (G.GEMM_KERNEL_TC, "bf16"),
