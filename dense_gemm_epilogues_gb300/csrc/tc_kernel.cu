@@ -50,11 +50,18 @@ struct TcCfg {
   static constexpr int STAGE_BYTES = SLABS * (A_BYTES + B_BYTES);   // [A slabs][B slabs]
   static constexpr int ACC_BUFS = 512 / BN;           // accumulators in the 512 TMEM columns
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-  static constexpr int OUT_STAGE_BYTES = 4 * 4096;   // a 32 x 32 output turn-around buffer per epilogue warp
+  static constexpr int OUT_STAGE_BYTES = 8 * 4096;   // a 32 x 32 output turn-around buffer per epilogue warp
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_STAGE_BYTES + NUM_BARS * 8 + 16;
 };
 
-constexpr int NUM_THREADS = 192;      // producer warp, MMA warp, 4 epilogue warps
+// Producer warp, MMA warp, then the epilogue warps: 8 in floating mode (two per
+// tensor-memory lane quarter, each finishing half of the tile's columns), 4 in
+// exact integer mode (a thread keeps a whole row of int32 sums).
+template <bool INT_MODE>
+struct TcThreads {
+  static constexpr int EPI_WARPS = INT_MODE ? 4 : 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MN_BOX = 64;            // MN extent of one TMA box for MN-major operands
 constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;   // 8 KiB
@@ -88,7 +95,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 
 // All lanes of a warp wait; the warp gives up together if any lane gave up.
 // CTA barrier of the four epilogue warps (named barrier 1; barrier 0 is __syncthreads).
-__device__ __forceinline__ void epi_warps_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int THREADS>
+__device__ __forceinline__ void epi_warps_sync() { asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory"); }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
   const bool ok = mbar_wait(bar, parity, wc);
@@ -122,7 +130,9 @@ struct TcWork<true> {
 };
 
 template <int BN, bool INT_MODE, bool SK>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  constexpr int EPI_WARPS = TcThreads<INT_MODE>::EPI_WARPS;
+  constexpr int CHUNKS = BN / 32 / (EPI_WARPS / 4);   // 32-column chunks per epilogue warp
   static_assert(!INT_MODE || BN == 128, "exact integer mode keeps 128 int32 accumulators per thread");
   using Cfg = TcCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
     for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
       mbar_init(tfull_bar(b), 1);   // tcgen05.commit after a unit's last MMA
-      mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(b), EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(teardown_bar, 1);
     *abort_flag = 0;
@@ -278,6 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   } else {
     // -------------------------------- epilogue --------------------------------
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
+    const int c0 = ((warp - 2) >> 2) * CHUNKS;       // this warp's first 32-column chunk
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     volatile int32_t* sk_verdict = abort_flag + 1;   // stream-K: this CTA finishes the tile (1), aborted (2)
     uint32_t acc_it = 0;
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
           float4* slot = reinterpret_cast<float4*>(slot_of((int)blockIdx.x));
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = c0; c < c0 + CHUNKS; ++c) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
             tmem_wait_ld();
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
         __threadfence();
-        epi_warps_sync();
+        epi_warps_sync<32 * EPI_WARPS>();
         const int c_first = sk_cluster_of(tl * p.num_kb, W, G);
         const int c_last = sk_cluster_of(tl * p.num_kb + p.num_kb - 1, W, G);
         if (warp == 2 && lane == 0) {
@@ -367,13 +378,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             *sk_verdict = old == c_last - c_first ? 1 : 0;
           }
         }
-        epi_warps_sync();
+        epi_warps_sync<32 * EPI_WARPS>();
         const int verdict = *sk_verdict;
         if (verdict == 2) { ok = false; break; }
         if (verdict == 1) {
           __threadfence();
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = c0; c < c0 + CHUNKS; ++c) {
             float x[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = 0.0f;
@@ -423,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = c0; c < c0 + CHUNKS; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
           tmem_wait_ld();
@@ -466,7 +477,7 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
   // for another, so starting early on free SMs is safe (see pdl_wait).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(TcThreads<INT_MODE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
