@@ -135,7 +135,8 @@ double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 40
 // from 256^3 to 8192^3 and two batches: per 64-deep block 0.323 us for a
 // 256 x 256 pair tile and 0.397 us for a 128 x 256 single-CTA tile (0.77 of that
 // for 128 x 128); epilogues of ~4.4 us (pair tile) and ~3.3 us (single-CTA
-// tile) bound tiles of small K; fixed costs ~8.3 us and ~6.6 us.  The stream-K
+// tile) bound tiles of small K; fixed costs ~8.3 us and ~5.0 us (the single-CTA
+// kernel's eight-warp epilogue finishes its last tile sooner).  The stream-K
 // tail, when requested, spreads pair tiles over all pairs.
 // GEMM_TC_CTA_GROUP=1 never uses pairs; =2 uses them whenever both dimensions allow.
 // Tail halves of the CTA-pair kernel: T tiles over G pairs leave a last wave of
@@ -175,7 +176,7 @@ bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters
   for (int bn : {256, 128}) {
     const int64_t tiles = batch * ((M + 127) / 128) * ((N + bn - 1) / bn);
     const double per_tile = std::max(kb * 0.397 * tc_tile_cost(bn), 3.3 * (bn / 256.0));
-    t_one = std::min(t_one, (double)((tiles + sm_count - 1) / sm_count) * per_tile + 6.6);
+    t_one = std::min(t_one, (double)((tiles + sm_count - 1) / sm_count) * per_tile + 5.0);
   }
   return t_pair < t_one;
 }
