@@ -126,7 +126,9 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
 
 // Relative cost of one 128 x BN tile of the tensor-core kernel (a 128x128 tile
 // does half the MMA work of a 128x256 tile but keeps the fixed per-tile costs).
-double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : 0.77; }   // measured: 4096^3 and 1024^3 fp16
+// Relative time per K block of a 128 x bn single-CTA tile (measured: 4096^3 and
+// 1024^3 fp16 for 256 and 128; 64 from 1024^3 and the skinny 16384 x 64 x 16384).
+double tc_tile_cost(int bn) { return bn == 256 ? 1.0 : bn == 128 ? 0.77 : 0.6; }
 
 // Run a tensor-core problem on CTA pairs?  Both dimensions must exceed one
 // 128-wide tile.  Then the choice is the smaller estimated time:
@@ -152,6 +154,15 @@ int64_t pair_tail_halves(int64_t T, int64_t G) {
   return (r > 0 && 2 * r <= G) ? r : 0;
 }
 
+// Single-CTA stream-K (floating mode) for T tiles of KB K blocks on sm_count
+// SMs: publishing a partial, the fence and the last arrival's reads cost ~4 us,
+// about 20 K blocks of a 128 x 128 tile, so it is taken when the idle SMs of a
+// single partial wave would save at least 48 K blocks per CTA, and every CTA gets
+// at least 4.
+bool single_stream_k_pays(int64_t T, int64_t KB, int sm_count) {
+  return T < sm_count && (double)KB * (1.0 - (double)T / sm_count) >= 48.0 && T * KB >= 4 * (int64_t)sm_count;
+}
+
 bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters, int sm_count) {
   if (pair_clusters <= 0 || M <= 128 || N <= 128) return false;
   if (const char* env = std::getenv("GEMM_TC_CTA_GROUP")) {
@@ -173,7 +184,7 @@ bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters
   const double t_pair =
       ((double)(pair_tiles / pair_clusters) + tail) * std::max(kb * 0.323, 4.4) + 8.3;
   double t_one = 1e300;
-  for (int bn : {256, 128}) {
+  for (int bn : {256, 128, 64}) {
     const int64_t tiles = batch * ((M + 127) / 128) * ((N + bn - 1) / bn);
     const double per_tile = std::max(kb * 0.397 * tc_tile_cost(bn), 3.3 * (bn / 256.0));
     t_one = std::min(t_one, (double)((tiles + sm_count - 1) / sm_count) * per_tile + 5.0);
@@ -293,16 +304,27 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         // Pick the tile width with the smaller estimated makespan over the SMs
         // (the largest tile that fits, unless it leaves SMs idle).
         double best = 1e300;
-        for (int cand : {256, 128}) {
+        for (int cand : {256, 128, 64}) {
           const int64_t tiles = batch * ((M + 127) / 128) * ((N + cand - 1) / cand);
           const int64_t waves = (tiles + sm_count - 1) / sm_count;
           const double cost = (double)waves * tc_tile_cost(cand);
           if (cost < best - 1e-9) { best = cost; bn = cand; }
         }
-        // Tuning override: GEMM_TC_BN=128 or 256 fixes the tile width.
+        // A narrower tile fills more SMs, but a wider one that qualifies for stream-K
+        // (deep K on few tiles) keeps every SM busy with less operand traffic.
+        const int64_t KB = (K + TC_BK - 1) / TC_BK;
+        auto tiles_of = [&](int w) { return batch * ((M + 127) / 128) * ((N + w - 1) / w); };
+        if (!single_stream_k_pays(tiles_of(bn), KB, sm_count)) {
+          for (int cand : {128, 256})
+            if (cand > bn && single_stream_k_pays(tiles_of(cand), KB, sm_count)) {
+              bn = cand;
+              break;
+            }
+        }
+        // Tuning override: GEMM_TC_BN=64, 128 or 256 fixes the tile width.
         if (const char* env = std::getenv("GEMM_TC_BN")) {
           const int v = std::atoi(env);
-          if (v == 128 || v == 256) bn = v;
+          if (v == 64 || v == 128 || v == 256) bn = v;
         }
       }
       cfg.bm = TC_BM;
@@ -321,14 +343,12 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       }
       cfg.k_chunk = k == GEMM_KERNEL_TC_INT8 ? chunk : 0;
       // Stream-K for a wave that leaves SMs idle (floating mode): all CTAs share
-      // the tiles' K blocks evenly and the last arrival on a tile finishes it.
-      // Publishing a partial, the fence and the last arrival's reads cost ~4 µs,
-      // about 20 K blocks of a 128 x 128 tile: taken when it saves at least 48 K
-      // blocks per CTA; GEMM_TC_SPLITK=0 turns it off, =1 forces it when every
-      // CTA gets a K block.
+      // the tiles' K blocks evenly and the last arrival on a tile finishes it
+      // (single_stream_k_pays); GEMM_TC_SPLITK=0 turns it off, =1 forces it when
+      // every CTA gets a K block.
       if (k == GEMM_KERNEL_TC) {
         const int64_t T = cfg.tiles, KB = (K + TC_BK - 1) / TC_BK;
-        bool sk1 = T < sm_count && (double)KB * (1.0 - (double)T / sm_count) >= 48.0 && T * KB >= 4 * (int64_t)sm_count;
+        bool sk1 = single_stream_k_pays(T, KB, sm_count);
         if (const char* env = std::getenv("GEMM_TC_SPLITK")) {
           const int v = std::atoi(env);
           if (v == 0) sk1 = false;

@@ -44,9 +44,9 @@ namespace {
 template <int BN>
 struct TcCfg {
   static constexpr int SLABS = (BN == 256) ? 1 : 2;
-  static constexpr int STAGES = ((BN == 256) ? 4 : 6) / SLABS;
+  static constexpr int STAGES = ((BN == 256) ? 4 : (BN == 128) ? 6 : 8) / SLABS;
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;   // 16 KiB per slab
-  static constexpr int B_BYTES = BN * TC_BK * 2;      // 32 KiB (BN=256) / 16 KiB (BN=128) per slab
+  static constexpr int B_BYTES = BN * TC_BK * 2;      // 32 / 16 / 8 KiB per slab (BN = 256 / 128 / 64)
   static constexpr int STAGE_BYTES = SLABS * (A_BYTES + B_BYTES);   // [A slabs][B slabs]
   static constexpr int ACC_BUFS = 512 / BN;           // accumulators in the 512 TMEM columns
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
@@ -490,9 +490,11 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
 
 }  // namespace
 
-int tc_stages(int bn) { return bn == 256 ? TcCfg<256>::STAGES : TcCfg<128>::STAGES; }
-int tc_k_per_stage(int bn) { return (bn == 256 ? TcCfg<256>::SLABS : TcCfg<128>::SLABS) * TC_BK; }
-size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : TcCfg<128>::SMEM; }
+int tc_stages(int bn) { return bn == 256 ? TcCfg<256>::STAGES : bn == 128 ? TcCfg<128>::STAGES : TcCfg<64>::STAGES; }
+int tc_k_per_stage(int bn) {
+  return (bn == 256 ? TcCfg<256>::SLABS : bn == 128 ? TcCfg<128>::SLABS : TcCfg<64>::SLABS) * TC_BK;
+}
+size_t tc_smem_bytes(int bn) { return bn == 256 ? TcCfg<256>::SMEM : bn == 128 ? TcCfg<128>::SMEM : TcCfg<64>::SMEM; }
 
 cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream) {
   if (p.chunk_kb > 0) {
@@ -502,6 +504,7 @@ cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream) 
   const bool sk = p.sk_first_tile < p.num_tiles;   // stream-K: a separate instance, so whole tiles lose nothing
   if (bn == 256) return sk ? launch_bn<256, false, true>(p, grid, stream) : launch_bn<256, false, false>(p, grid, stream);
   if (bn == 128) return sk ? launch_bn<128, false, true>(p, grid, stream) : launch_bn<128, false, false>(p, grid, stream);
+  if (bn == 64) return sk ? launch_bn<64, false, true>(p, grid, stream) : launch_bn<64, false, false>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

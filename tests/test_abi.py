@@ -117,7 +117,7 @@ def test_selector_all_layouts_on_tensor_cores(la, lb):
 
 
 def test_selector_narrow_and_small_shapes():
-    assert _sel(N=64, M=16384, K=16384)["bn"] == 128
+    assert _sel(N=64, M=16384, K=16384)["bn"] == 64   # one 64-wide tile column
     cfg = _sel(M=512, N=512, K=512)   # 4 pair tiles: less than a wave of pairs
     assert cfg["kernel"] == G.GEMM_KERNEL_TC and cfg["bm"] == 128
     cfg = _sel(M=2560, N=2048, K=512)  # 80 pair tiles on 76 pairs: a second, nearly empty wave
