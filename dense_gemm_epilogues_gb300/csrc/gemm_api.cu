@@ -547,14 +547,6 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   tp.b_mn_major = b_mn ? 1 : 0;
   tp.idesc = make_idesc(bf16, bn, a_mn, b_mn);
   tp.chunk_kb = chunk_kb;
-  // One tile column: no two tiles share rows of A, so nothing is lost in L2 when
-  // the tiles walk K from different starting points, and the CTAs' concurrent
-  // reads of A spread over more of DRAM (skinny 16384 x 64 x 16384: 5.63 -> 5.95
-  // TB/s, measured).  GEMM_TC_KROT=0 keeps every tile in K order.
-  bool k_rotate = tp.tiles_n == 1 && chunk_kb == 0 && cfg.sk_tiles == 0;
-  if (const char* env = std::getenv("GEMM_TC_KROT"))
-    if (std::atoi(env) == 0) k_rotate = false;
-  tp.k_rotate = k_rotate ? 1 : 0;
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;

@@ -29,10 +29,6 @@ struct TcParams {
   uint32_t idesc_half;    // CTA-pair kernel: the same for half-tile units (N = 128)
   int32_t half_first_tile;  // CTA-pair kernel: tiles from here on run as two column halves (num_tiles: none)
   int32_t chunk_kb;       // > 0: exact integer mode, K blocks per fp32 chunk
-  // Single-CTA kernel, whole tiles in floating mode: each tile starts its K loop at
-  // stage (tile mod stages) and wraps around, so CTAs that stream disjoint rows of
-  // A read different K offsets at the same time.
-  int32_t k_rotate;
   EpiParams epi;
   int32_t* err;
   uint64_t timeout_ns;

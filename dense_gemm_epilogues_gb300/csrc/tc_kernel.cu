@@ -129,14 +129,6 @@ struct TcWork<true> {
   }
 };
 
-// First stage of a segment's K loop (see TcParams::k_rotate): only whole tiles in
-// floating mode rotate; integer units and stream-K segments run in K order.
-template <bool INT_MODE>
-__device__ __forceinline__ int k_rotation(const TcParams& p, int t, int kb_lo, int kb_hi, int nst) {
-  if (INT_MODE || !p.k_rotate || kb_lo != 0 || kb_hi != p.num_kb || nst <= 1) return 0;
-  return t % nst;
-}
-
 template <int BN, bool INT_MODE, bool SK>
 __global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   constexpr int EPI_WARPS = TcThreads<INT_MODE>::EPI_WARPS;
@@ -204,12 +196,9 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kerne
         tile_coords(t, p, bz, tm, tn);
         const int m0 = tm * TC_BM, n0 = tn * BN;
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
-        const int nst = (kb_hi - kb_lo + Cfg::SLABS - 1) / Cfg::SLABS;   // stages of this segment
-        const int rot = k_rotation<INT_MODE>(p, t, kb_lo, kb_hi, nst);
-        for (int s = 0; s < nst; ++s) {
+        for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += Cfg::SLABS) {
           // A unit of the exact integer mode spans an even number of K blocks, so
           // stages never straddle two units.
-          const int kb0 = kb_lo + (s + rot < nst ? s + rot : s + rot - nst) * Cfg::SLABS;
           const int nsl = kb_hi - kb0 < Cfg::SLABS ? kb_hi - kb0 : Cfg::SLABS;
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb = full_bar(stage);
@@ -263,10 +252,7 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kerne
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
           const int kb_begin = INT_MODE ? u * kb_per_unit : kb_lo;
           const int kb_end = INT_MODE ? min(p.num_kb, kb_begin + kb_per_unit) : kb_hi;
-          const int nst = (kb_end - kb_begin + Cfg::SLABS - 1) / Cfg::SLABS;
-          const int rot = k_rotation<INT_MODE>(p, t, kb_lo, kb_hi, nst);   // the producer's order
-          for (int s = 0; s < nst; ++s) {
-            const int kb = kb_begin + (s + rot < nst ? s + rot : s + rot - nst) * Cfg::SLABS;
+          for (int kb = kb_begin; kb < kb_end; kb += Cfg::SLABS) {
             const int nsl = kb_end - kb < Cfg::SLABS ? kb_end - kb : Cfg::SLABS;
             if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
             tc_fence_after();
@@ -284,7 +270,7 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kerne
                                                  : smem_desc_sw128(sa + kk * 32u, 16, 1024);
                 const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
                                                  : smem_desc_sw128(sb + kk * 32u, 16, 1024);
-                tc_mma_f16(d_tmem, ad, bd, p.idesc, (s > 0 || sl > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
               }
             }
             tc_commit(empty_bar(stage));

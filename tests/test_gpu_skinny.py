@@ -1,13 +1,11 @@
-"""One tile column (N <= the tile width): each tile starts its K loop at a
-different stage and wraps around (the single-CTA kernel's K rotation), so the
-CTAs read different K offsets of their rows of A at the same time.
+"""One tile column (N no wider than the single-CTA tile): every tile streams its
+own rows of A over the whole of K and shares only B with the others.
 
-Rotation changes only the order of the fp32 additions: checked element by
-element against the fp64 oracle with it on (the default) and off, including a
-last stage holding a single K block, ragged M and N, and the full epilogue.
+Checked element by element against the fp64 oracle: a full wave of 128 x 64
+tiles, a last stage holding a single K block, 128-wide tiles, ragged M and N,
+the full epilogue and all four layouts.
 """
 import pytest
-import torch
 
 import dense_gemm_epilogues_gb300 as G
 from dense_gemm_epilogues_gb300 import inputs as I
@@ -16,23 +14,21 @@ import parity_helpers as H
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("rotate", ["1", "0"])
 @pytest.mark.parametrize("mnk_bn", [(16384, 64, 2048, 64), (3000, 40, 1064, 64), (1200, 128, 2112, 128)],
                          ids=lambda s: "x".join(map(str, s[:3])))
-def test_single_tile_column(mnk_bn, rotate, monkeypatch):
+def test_single_tile_column(mnk_bn, monkeypatch):
     """128 tiles of 128 x 64 (a full wave, no stream-K); K = 1064: 17 K blocks, so
     the last stage of two slabs holds one; 128-wide tiles over K = 2112."""
-    monkeypatch.setenv("GEMM_TC_KROT", rotate)
     M, N, K, bn = mnk_bn
     monkeypatch.setenv("GEMM_TC_BN", str(bn))
-    p = H.tma_aligned(I.Problem("skinny_rot", "f16", "T", "N", M, N, K, alpha=1.25, beta=0.5, c="f32",
+    p = H.tma_aligned(I.Problem("skinny", "f16", "T", "N", M, N, K, alpha=1.25, beta=0.5, c="f32",
                                 d="f32", bias="f32", bias_mode="col", act="relu"))
     cfg = H.run_and_check_full(p, 170, expect_kernel=G.GEMM_KERNEL_TC)
     assert cfg["sk_tiles"] == 0 and cfg["bn"] == bn and (p.N + bn - 1) // bn == 1, cfg
 
 
 @pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
-def test_rotation_all_layouts(layout):
+def test_single_tile_column_all_layouts(layout):
     p = H.tma_aligned(I.Problem("skinny_lay", "bf16", layout[0], layout[1], 2000, 64, 2000, beta=-1.0,
                                 c="bf16", d="bf16"))
     H.run_and_check_full(p, 171, expect_kernel=G.GEMM_KERNEL_TC)
