@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kerne
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int c0 = ((warp - 2) >> 2) * CHUNKS;       // this warp's first 32-column chunk
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    volatile int32_t* sk_verdict = abort_flag + 1;   // stream-K: this CTA finishes the tile (1), aborted (2)
+    volatile int32_t* sk_role = abort_flag + 1;   // stream-K: this CTA finishes the tile (1), aborted (2)
     uint32_t acc_it = 0;
     bool ok = true;
     TcWork<SK> it(blockIdx.x, gridDim.x, p.num_tiles, p.num_kb, p.sk_first_tile);
@@ -372,16 +372,16 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE>::THREADS, 1) tc_gemm_kerne
         const int c_last = sk_cluster_of(tl * p.num_kb + p.num_kb - 1, W, G);
         if (warp == 2 && lane == 0) {
           if (*wc.abort) {
-            *sk_verdict = 2;
+            *sk_role = 2;
           } else {
             const int old = atomicAdd(&p.sk_flags[t], 1);
-            *sk_verdict = old == c_last - c_first ? 1 : 0;
+            *sk_role = old == c_last - c_first ? 1 : 0;
           }
         }
         epi_warps_sync<32 * EPI_WARPS>();
-        const int verdict = *sk_verdict;
-        if (verdict == 2) { ok = false; break; }
-        if (verdict == 1) {
+        const int role = *sk_role;
+        if (role == 2) { ok = false; break; }
+        if (role == 1) {
           __threadfence();
 #pragma unroll 1
           for (int c = c0; c < c0 + CHUNKS; ++c) {
