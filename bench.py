@@ -73,6 +73,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest of the ranks' values of x (each rank's elapsed time -> the
+    job's); x itself when there is one rank (dist None)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return flops_per_rank * world / seconds / 1e12
+
+
 def workload_config(world: int) -> dict:
     return {"workload": "gemm_f16_8192x8192x8192_alpha1.5_beta0.5_fp32_C_D_layouts_NN_NT_TN_TT",
             "M": MAIN_N, "N": MAIN_N, "K": MAIN_N, "layouts": LAYOUTS, "ab": "f16",
@@ -260,14 +276,11 @@ def bench_ours(args, rank, world, local_rank):
     status = plan.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, device)
 
     flops_per_gemm = 2.0 * MAIN_N ** 3
     flops_step = flops_per_gemm * len(ins)
-    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+    value = job_tflops(flops_step * args.steps, world, total_ms / 1e3)
     peaks = load_peaks()
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     per_layout_ms = {l: round(statistics.mean(st[li][0].elapsed_time(st[li][1]) for st in evs), 4)
@@ -337,11 +350,7 @@ def bench_e2e(G, plan, ins, device, steps, dist):
     for _ in range(steps):
         step()
     torch.cuda.synchronize()
-    el = time.perf_counter() - t
-    if dist:
-        tt = torch.tensor([el], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el = float(tt.item())
+    el = max_over_ranks(time.perf_counter() - t, dist, device)
     world = dist.get_world_size() if dist else 1
     flops = 2.0 * MAIN_N ** 3 * len(hosts) * steps * world
     h2d = sum(A.numel() * A.element_size() + B.numel() * B.element_size() for _, A, B in hosts)
