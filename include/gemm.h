@@ -119,8 +119,9 @@ typedef struct {
     int32_t grid;         /* CTAs launched */
     int32_t k_chunk;      /* int8 path: K elements per exact fp32 chunk; 0 otherwise */
     int32_t tiles;        /* output tiles */
-    int32_t sk_tiles;     /* tiles in the stream-K tail (their K blocks are shared out over
-                             all CTA pairs; 0 = every tile runs whole on one CTA pair) */
+    int32_t sk_tiles;     /* stream-K tiles: their K blocks are shared out over all CTAs
+                             (single-CTA kernel) or CTA pairs of the launch; 0 = every tile
+                             runs whole on one CTA or CTA pair */
     int32_t cluster;      /* CTAs per thread-block cluster: 1, 2 (one CTA pair) or 4 (two CTA
                              pairs on vertically adjacent tiles sharing B by TMA multicast) */
     int32_t half_tiles;   /* CTA-pair kernel: the last half_tiles tiles (a partial last wave
