@@ -579,19 +579,6 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtens
       : "memory");
 }
 
-// The same load delivered to every CTA of `cta_mask` (same shared-memory offset in
-// each); each destination's completion is signalled on the barrier at the same
-// offset in the leader CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_3d_pair_multicast(uint32_t dst, const CUtensorMap* tm, int32_t x,
-                                                           int32_t y, int32_t z, uint32_t bar_cluster_addr,
-                                                           uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr), "h"(cta_mask)
-      : "memory");
-}
-
 // D(tmem, both CTAs) (+)= A(smem, both CTAs) * B(smem, N split over both CTAs).
 __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                 uint32_t idesc, uint32_t accumulate) {
@@ -605,9 +592,10 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc,
       : "memory");
 }
 
-// Arrive once on the mbarrier at this offset in every CTA of `cta_mask` when the
-// pair MMAs issued so far by this thread have completed.
-__device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
+// Arrive once on the mbarrier at this offset in every CTA of `cta_mask` (bit r:
+// CTA r of the pair) when the pair MMAs issued so far by this thread have
+// completed.  This signals barriers only; it moves no operand data.
+__device__ __forceinline__ void tc_commit_pair_mask(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(cta_mask)

@@ -28,7 +28,6 @@ struct gemm_plan {
   size_t stage_bytes = 0;
   gemm_kernel_t forced = GEMM_KERNEL_AUTO;
   int pair_clusters = 0;             // co-resident CTA-pair clusters (0: pair kernel unavailable)
-  int quad_clusters = 0;             // co-resident clusters of two CTA pairs (B shared by multicast)
   void* sk_ws = nullptr;             // stream-K partial accumulators and flags (per cluster and CTA)
   size_t sk_ws_bytes = 0;
   int32_t sk_epoch = 0;
@@ -197,7 +196,7 @@ bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters
 gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
                             int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                             int sm_count, gemm_kernel_t forced, gemm_config_t* out, int pair_clusters = 0,
-                            int64_t batch = 1, int quad_clusters = 0) {
+                            int64_t batch = 1) {
   (void)c;
   gemm_config_t cfg{};
   cfg.split_k = 1;
@@ -273,27 +272,10 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         const int64_t per = std::max<int64_t>(1, sk_tiles * KB / G);
         cfg.split_k = (int32_t)std::min<int64_t>((KB + per - 1) / per + 1, KB);
       }
-      // Two CTA pairs per cluster on vertically adjacent tiles, B shared by TMA
-      // multicast: a quarter fewer operand bytes per SM from L2.  Taken when the
-      // tile rows pair up (an odd last row wastes one pair's work) and clusters of
-      // four cover as many SMs as pairs would.  GEMM_TC_CLUSTER=2 or 4 forces it.
-      bool quad = !sk && quad_clusters > 0 && tiles_m >= 2 && (tiles_m % 2 == 0 || tiles_m >= 8) &&
-                  2 * quad_clusters >= pair_clusters;
-      if (const char* env = std::getenv("GEMM_TC_CLUSTER")) {
-        const int v = std::atoi(env);
-        if (v == 2) quad = false;
-        else if (v == 4) quad = !sk && quad_clusters > 0 && tiles_m >= 2;
-      }
       cfg.cluster = 2;
-      if (!sk && !quad) {
+      if (!sk) {
         cfg.half_tiles = (int32_t)pair_tail_halves(T, G);
         if (cfg.half_tiles > 0) cfg.grid = 2 * (int32_t)std::min<int64_t>(T + cfg.half_tiles, G);
-      }
-      if (quad) {
-        cfg.cluster = 4;
-        const int64_t super_tiles = batch * ((tiles_m + 1) / 2) * tiles_n;
-        cfg.grid = 4 * (int32_t)std::min<int64_t>(super_tiles, quad_clusters);
-        cfg.raster = std::max<int32_t>(2, cfg.raster / 2 * 2);
       }
       break;
     }
@@ -582,19 +564,18 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   std::memset(&tp, 0, sizeof(tp));
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const bool a_mn = la == GEMM_OP_N, b_mn = lb == GEMM_OP_T;
-  const bool quad = cfg.cluster == 4 && chunk_kb == 0;   // two CTA pairs per cluster
   const uint64_t na = (bt.count > 1 && bt.sa != 0) ? (uint64_t)bt.count : 1;
   const uint64_t nb = (bt.count > 1 && bt.sb != 0) ? (uint64_t)bt.count : 1;
   bool ok;
   if (!a_mn) ok = encode_3d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, na, bt.sa, TC_BK, TC_BM);
   else ok = encode_3d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, na, bt.sa, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
-  if (!b_mn) ok = encode_3d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, quad ? 64 : 128);
+  if (!b_mn) ok = encode_3d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, 128);
   else ok = encode_3d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, bt.sb, 64, TC_BK);
   if (!ok) return GEMM_ERR_CUDA;
   // Half-tile units load 64 columns of B per CTA: K-major boxes of 64 rows (an
   // MN-major box is already 64 columns wide).
-  const bool halves = cfg.half_tiles > 0 && chunk_kb == 0 && !quad && cfg.sk_tiles == 0;
+  const bool halves = cfg.half_tiles > 0 && chunk_kb == 0 && cfg.sk_tiles == 0;
   if (halves && !b_mn) {
     if (!encode_3d(&tp.tmBh, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, 64))
       return GEMM_ERR_CUDA;
@@ -606,13 +587,12 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   tp.K = (int32_t)K;
   tp.num_kb = (int32_t)((K + TC_BK - 1) / TC_BK);
   tp.tiles_m = (int32_t)((M + 255) / 256);
-  if (quad) tp.tiles_m = (tp.tiles_m + 1) / 2;     // super-tile rows of 512
   tp.tiles_n = (int32_t)((N + 255) / 256);
   tp.tiles_per_batch = tp.tiles_m * tp.tiles_n;
   tp.num_tiles = tp.tiles_per_batch * (int32_t)bt.count;
   tp.a_batched = na > 1;
   tp.b_batched = nb > 1;
-  tp.raster = quad ? std::max<int32_t>(1, cfg.raster / 2) : (cfg.raster > 0 ? cfg.raster : 1);
+  tp.raster = cfg.raster > 0 ? cfg.raster : 1;
   tp.a_mn_major = a_mn ? 1 : 0;
   tp.b_mn_major = b_mn ? 1 : 0;
   tp.idesc = make_idesc(bf16, 256, a_mn, b_mn, 256);
@@ -643,8 +623,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
     if (++plan->sk_epoch <= 0) plan->sk_epoch = 1;
     tp.sk_epoch = plan->sk_epoch;
   }
-  const int csize = quad ? 4 : 2;
-  return launch_tc_pair(tp, cfg.grid / csize, csize, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  return launch_tc_pair(tp, cfg.grid / 2, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 }  // namespace
@@ -680,8 +659,7 @@ gemm_status_t gemm_select(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gem
   const double alpha_probe = ab == GEMM_S8 ? 1.0 : 1.0;
   gemm_status_t s = validate(ab, c, la, lb, M, N, K, alpha_probe, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
-  // Host-only: a device whose SMs all pair up; clusters of four are not assumed
-  // (whether they fit is a property of the device's GPC layout).
+  // Host-only: a device whose SMs all pair up.
   return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out, sm_count / 2);
 }
 
@@ -710,7 +688,6 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab, gemm_dtype_t 
     return GEMM_ERR_CUDA;
   }
   p->pair_clusters = tc_pair_max_clusters(device);
-  p->quad_clusters = tc_quad_max_clusters(device);
   *plan = p;
   return GEMM_OK;
 }
@@ -780,7 +757,7 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
                        gemm_stream_t stream_, const Batch& bt) {
   gemm_config_t cfg{};
   gemm_status_t s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count,
-                                  plan->forced, &cfg, plan->pair_clusters, bt.count, plan->quad_clusters);
+                                  plan->forced, &cfg, plan->pair_clusters, bt.count);
   if (s != GEMM_OK) return s;
   if (cfg.kernel == GEMM_KERNEL_NONE) {
     plan->last = cfg;

@@ -59,12 +59,8 @@ cudaError_t launch_tc(const TcParams& p, int bn, int grid, cudaStream_t stream);
 int tc_pair_stages();
 int tc_pair_k_per_stage();              // K depth of one pipeline stage (64-deep slabs per stage x 64)
 size_t tc_pair_smem_bytes();
-// cluster_size 4 (floating mode only): two CTA pairs per cluster on a 512 x 256
-// super-tile sharing B by multicast; then tiles_m / num_tiles count super-tiles
-// and B's K-major box is 64 columns wide.
 int tc_pair_max_clusters(int device);   // co-resident clusters of two (0 if unknown)
-int tc_quad_max_clusters(int device);   // co-resident clusters of four (0 if unknown)
-cudaError_t launch_tc_pair(const TcParams& p, int clusters, int cluster_size, cudaStream_t stream);
+cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream);
 
 // FFMA SGEMM (fp32, CUDA cores).
 struct FfmaParams {

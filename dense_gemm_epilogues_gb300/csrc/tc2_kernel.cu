@@ -4,16 +4,17 @@
 // 256 (M) x 256 (N) per cluster of two CTAs on two SMs:
 //   - CTA r of the pair stages, per 64-deep K block, its own 128 rows of A
 //     (rows m0 + 128r ...) and its own half of B (columns n0 + 128r ...) --
-//     32 KiB per stage, six stages -- so each SM moves 2/3 of the operand bytes
-//     of a 128 x 256 single-CTA tile for the same MMA work;
+//     32 KiB per K block; a pipeline stage holds two K blocks (64 KiB) and the
+//     ring has three stages -- so each SM moves 2/3 of the operand bytes of a
+//     128 x 256 single-CTA tile for the same MMA work;
 //   - both CTAs' TMA loads complete on the leader CTA's (rank 0) full barrier;
 //   - one thread of the leader issues tcgen05.mma.cta_group::2 (M = 256,
 //     N = 256, K = 16): the hardware takes A's rows from both CTAs and B's halves
 //     from both CTAs, and writes each CTA's 128 rows of D into that CTA's tensor
 //     memory (two 256-column fp32 accumulators per CTA, double buffered);
-//   - its commits arrive on both CTAs' barriers (multicast): the stage-free
-//     barriers that the two producers wait on and the accumulator-full barriers
-//     the two epilogues wait on;
+//   - its commits arrive on both CTAs' barriers (the commit's CTA mask): the
+//     stage-free barriers that the two producers wait on and the
+//     accumulator-full barriers the two epilogues wait on;
 //   - the epilogue warps of both CTAs finish their 128 rows (alpha, beta*C,
 //     bias, ReLU, cast, 16-byte stores) and release the accumulator on the
 //     leader's barrier (the peer's four warps arrive remotely).
@@ -22,7 +23,8 @@
 // epilogue warps per CTA -- two per tensor-memory lane quarter, one per half of
 // the 256 columns -- convert each finished chunk to int32 and add it into 128
 // registers per thread, then apply the integer epilogue after the last chunk.
-// No TMA multicast is used: every CTA loads only its own data.
+// Every TMA load brings one CTA's own operand data into that CTA's shared
+// memory; no load is delivered to more than one CTA.
 // Every mbarrier wait is bounded, as in tc_kernel.cu.
 #include "kernels.h"
 
@@ -89,14 +91,10 @@ __device__ __forceinline__ bool warp_wait_pair(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// CL = 2: one CTA pair per cluster.  CL = 4 (floating mode): two CTA pairs per
-// cluster on vertically adjacent tiles of one 512 x 256 super-tile; both pairs
-// need the same B columns, so each CTA loads one quarter of its B half and
-// multicasts it to the CTA in the same position of the other pair.
-template <bool INT_MODE, int CL>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
+// One CTA pair per cluster of two.
+template <bool INT_MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
-  static_assert(CL == 2 || (CL == 4 && !INT_MODE), "two-pair clusters serve the floating mode");
   constexpr int EPI_WARPS = PairThreads<INT_MODE>::EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -117,21 +115,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;                // position in the CTA pair
-  const int pp = (int)(crank >> 1);                // pair of the cluster (0 unless CL == 4)
-  const uint32_t pair_leader = crank & ~1u;        // cluster rank of this pair's leader
+  const uint32_t rank = cluster_ctarank() & 1u;    // position in the CTA pair
+  const uint32_t pair_leader = 0;                  // cluster rank of the pair's leader
   const bool leader = rank == 0;
-  const int cluster_id = (int)(blockIdx.x / CL);
-  const int num_clusters = (int)(gridDim.x / CL);
+  const int cluster_id = (int)(blockIdx.x / 2);
+  const int num_clusters = (int)(gridDim.x / 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PAIR_STAGES; ++s) {
       mbar_init(full_bar(s), 1);    // leader: its expect_tx arrival + both CTAs' TMA bytes
-      mbar_init(empty_bar(s), CL / 2);   // the multicast commit of each pair's leader
+      mbar_init(empty_bar(s), 1);   // the leader's commit (CTA mask: both CTAs)
     }
     for (int b = 0; b < PAIR_ACC_BUFS; ++b) {
-      mbar_init(tfull_bar(b), 1);   // the leader's multicast commit
+      mbar_init(tfull_bar(b), 1);   // the leader's commit (CTA mask: both CTAs)
       mbar_init(tempty_bar(b), 2 * EPI_WARPS);  // leader: every epilogue warp of both CTAs
     }
     mbar_init(teardown_bar, 1);
@@ -172,7 +168,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
       while (ok && it.next(tile, kb0, kb1, half)) {
         int bz, tm, tn;
         pair_tile_coords(tile, p, bz, tm, tn);
-        if constexpr (CL == 4) tm = 2 * tm + pp;                    // this pair's half of the super-tile
         const int m0 = tm * (2 * TC_BM) + (int)rank * TC_BM;        // this CTA's rows of A
         // This CTA's half of B's columns: 128 of a whole tile, 64 of a half-tile unit.
         const int n0 = half < 0 ? tn * PAIR_BN + (int)rank * (PAIR_BN / 2)
@@ -197,15 +192,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
           } else {
             tma_load_3d_pair_hint(sa, &p.tmA, k0, m0, za, fb, a_policy);
           }
-          if constexpr (CL == 4) {
-            // Quarter pp of this CTA's B half, into this CTA and its counterpart in the other pair.
-            const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-            if (p.b_mn_major)
-              tma_load_3d_pair_multicast(sb + pp * MN_BOX_BYTES, &p.tmB, n0 + pp * MN_BOX, k0, zb, fb, mask);
-            else
-              tma_load_3d_pair_multicast(sb + pp * (PAIR_B_BYTES / 2), &p.tmB, k0, n0 + pp * (PAIR_BN / 4), zb,
-                                         fb, mask);
-          } else if (half >= 0) {
+          if (half >= 0) {
             // 64 columns: one MN-major box, or a K-major box of 64 rows.
             if (p.b_mn_major) tma_load_3d_pair(sb, &p.tmB, n0, k0, zb, fb);
             else tma_load_3d_pair(sb, &p.tmBh, k0, n0, zb, fb);
@@ -273,11 +260,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
                 tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
               }
             }
-            tc_commit_pair_multicast(empty_bar(stage), CL == 4 ? 0xF : 0x3);   // every CTA it feeds
+            tc_commit_pair_mask(empty_bar(stage), 0x3);   // both CTAs' producers
             if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          tc_commit_pair_multicast(tfull_bar(buf), (uint16_t)(0x3u << pair_leader));
+          tc_commit_pair_mask(tfull_bar(buf), (uint16_t)(0x3u << pair_leader));
           ++acc_it;
         }
       }
@@ -295,7 +282,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
     while (ok && it.next(tile, kb0, kb1, half)) {
       int bz, tm, tn;
       pair_tile_coords(tile, p, bz, tm, tn);
-      if constexpr (CL == 4) tm = 2 * tm + pp;
       const int row_in_cta = q * 32 + lane;
       const int64_t m = (int64_t)tm * (2 * TC_BM) + (int64_t)rank * TC_BM + row_in_cta;
       // A half-tile unit's columns start half a tile further and fill half the accumulator.
@@ -447,27 +433,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(PairThreads<INT_MOD
   if (warp == 1) tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
 }
 
-template <bool INT_MODE, int CL>
+template <bool INT_MODE>
 int max_clusters_for(int device) {
   static int cached[64] = {};
   if (device < 0 || device >= 64) return 0;
   if (cached[device] > 0) return cached[device];
-  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)PAIR_SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL * 256, 1, 1);
+  cfg.gridDim = dim3(2 * 256, 1, 1);
   cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE, CL>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -475,7 +461,7 @@ int max_clusters_for(int device) {
   return n;
 }
 
-template <bool INT_MODE, int CL>
+template <bool INT_MODE>
 cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   static_assert(PAIR_SMEM <= 232448, "shared memory budget");
   int dev = 0;
@@ -483,7 +469,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PAIR_SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -493,7 +479,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   // kernel's end) -- unless the stream-K tail is on: its CTA pairs wait for each
   // other, so they must all start together on an otherwise free GPU.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL * clusters, 1, 1);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM;
   cfg.stream = stream;
@@ -502,7 +488,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = p.sk_first_tile == p.num_tiles ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE, CL>, p);
+  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE>, p);
 }
 
 }  // namespace
@@ -512,16 +498,13 @@ int tc_pair_k_per_stage() { return PAIR_SLABS * TC_BK; }
 size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
 
 int tc_pair_max_clusters(int device) {
-  const int a = max_clusters_for<false, 2>(device);
-  const int b = max_clusters_for<true, 2>(device);
+  const int a = max_clusters_for<false>(device);
+  const int b = max_clusters_for<true>(device);
   return a < b ? a : b;
 }
 
-int tc_quad_max_clusters(int device) { return max_clusters_for<false, 4>(device); }
-
-cudaError_t launch_tc_pair(const TcParams& p, int clusters, int cluster_size, cudaStream_t stream) {
-  if (p.chunk_kb > 0) return cluster_size == 2 ? launch_mode<true, 2>(p, clusters, stream) : cudaErrorInvalidValue;
-  return cluster_size == 4 ? launch_mode<false, 4>(p, clusters, stream) : launch_mode<false, 2>(p, clusters, stream);
+cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
+  return p.chunk_kb > 0 ? launch_mode<true>(p, clusters, stream) : launch_mode<false>(p, clusters, stream);
 }
 
 }  // namespace gemmlib

@@ -122,8 +122,7 @@ typedef struct {
     int32_t sk_tiles;     /* stream-K tiles: their K blocks are shared out over all CTAs
                              (single-CTA kernel) or CTA pairs of the launch; 0 = every tile
                              runs whole on one CTA or CTA pair */
-    int32_t cluster;      /* CTAs per thread-block cluster: 1, 2 (one CTA pair) or 4 (two CTA
-                             pairs on vertically adjacent tiles sharing B by TMA multicast) */
+    int32_t cluster;      /* CTAs per thread-block cluster: 1, or 2 (one CTA pair) */
     int32_t half_tiles;   /* CTA-pair kernel: the last half_tiles tiles (a partial last wave
                              of at most half the CTA pairs) each run as two units of 256 x 128,
                              on two CTA pairs, so that the last wave takes half a tile's time */
