@@ -41,8 +41,8 @@ LAYOUT_CODES = {"N": GEMM_OP_N, "T": GEMM_OP_T}
 EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host", "gemm_validate",
             "gemm_select", "gemm_plan_set_kernel", "gemm_plan_last_config", "gemm_plan_device_status",
             "gemm_plan_set_timeout", "gemm_status_string", "gemm_abi_version",
-            "gemm_run_s8_noalloc", "gemm_run_strided_batched", "gemm_run_diag",
-            "gemm_run_complex"]
+            "gemm_run_s8_noalloc", "gemm_noalloc_device_status", "gemm_noalloc_set_timeout",
+            "gemm_run_strided_batched", "gemm_run_diag", "gemm_run_complex"]
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -104,6 +104,8 @@ def load_library(path: str = LIB_PATH):
                                              ctypes.POINTER(gemm_epilogue_t), i64, vp]
     lib.gemm_run_s8_noalloc.argtypes = [ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64,
                                         vp, i64, ctypes.POINTER(gemm_epilogue_t), vp, vp]
+    lib.gemm_noalloc_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+    lib.gemm_noalloc_set_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_run_diag.argtypes = [vp, ci, ci, i64, i64, dbl, vp, vp, i64, dbl, vp, i64, vp, i64,
                                   ctypes.POINTER(gemm_epilogue_t), vp]
     lib.gemm_run_complex.argtypes = [vp, ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64, dbl, vp, i64,
@@ -196,6 +198,19 @@ def gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta
     _check(load_library().gemm_run_s8_noalloc(layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
                                               beta, C, ldc, D, ldd, _epi_ptr(epi), status, stream),
            "gemm_run_s8_noalloc")
+
+
+def gemm_noalloc_device_status(stream: int = 0) -> int:
+    """Read and clear the library's error word of gemm_run_s8_noalloc on the
+    current device (after synchronising `stream`)."""
+    code = ctypes.c_int32(0)
+    _check(load_library().gemm_noalloc_device_status(ctypes.byref(code), stream),
+           "gemm_noalloc_device_status")
+    return code.value
+
+
+def gemm_noalloc_set_timeout(timeout_ns: int) -> None:
+    _check(load_library().gemm_noalloc_set_timeout(timeout_ns), "gemm_noalloc_set_timeout")
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -630,7 +631,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
 
 extern "C" {
 
-int gemm_abi_version(void) { return 107; }
+int gemm_abi_version(void) { return 108; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
@@ -1185,6 +1186,8 @@ struct NoallocDevice {
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
+// Bound of the in-kernel waits of gemm_run_s8_noalloc (gemm_noalloc_set_timeout).
+std::atomic<uint64_t> g_noalloc_timeout_ns{4000000000ull};
 
 // Once per device, with that device current: look up the arrays' device addresses.
 gemm_status_t noalloc_device(int dev, NoallocDevice** out) {
@@ -1229,8 +1232,8 @@ extern "C" gemm_status_t gemm_run_s8_noalloc(gemm_layout_t la, gemm_layout_t lb,
   s = noalloc_device(dev, &nd);
   if (s != GEMM_OK) return s;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // The library's word keeps the first failure until gemm_noalloc_device_status reads it.
   int32_t* err = status ? status : nd->status;
-  if (!status && cudaMemsetAsync(err, 0, sizeof(int32_t), stream) != cudaSuccess) return GEMM_ERR_CUDA;
 
   // A plan-shaped record on the stack (no device memory behind it) so that the
   // launch helpers of gemm_run serve this entry point unchanged.
@@ -1240,11 +1243,16 @@ extern "C" gemm_status_t gemm_run_s8_noalloc(gemm_layout_t la, gemm_layout_t lb,
   local.c = GEMM_S32;
   local.sm_count = nd->sm_count;
   local.d_err = err;
+  local.timeout_ns = g_noalloc_timeout_ns.load();
   gemm_config_t cfg{};
   s = select_config(GEMM_S8, GEMM_S32, la, lb, M, N, K, A, lda, B, ldb, local.sm_count, GEMM_KERNEL_AUTO, &cfg);
   if (s != GEMM_OK) return s;
   const EpiParams e = make_epi(&local, alpha, beta, C, ldc, D, ldd, epi);
-  if (cfg.kernel != GEMM_KERNEL_TC_INT8) {   // K == 0: epilogue of beta*C only, no staging
+  // With K > 0 the leading dimensions were checked above, so the selector picks
+  // the single-CTA int8 kernel (no CTA-pair plan data exists here); K == 0 leaves
+  // the epilogue of beta*C alone, which the generic kernel runs without staging.
+  if (cfg.kernel != GEMM_KERNEL_TC_INT8) {
+    if (K != 0) return GEMM_ERR_UNSUPPORTED;
     SimtParams sp{};
     sp.A = A;
     sp.B = B;
@@ -1271,5 +1279,26 @@ extern "C" gemm_status_t gemm_run_s8_noalloc(gemm_layout_t la, gemm_layout_t lb,
   if (ce != cudaSuccess) return GEMM_ERR_CUDA;
   return launch_tc_problem(&local, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                            false, e, cfg.k_chunk / TC_BK, stream);
+}
+
+extern "C" gemm_status_t gemm_noalloc_device_status(int32_t* code, gemm_stream_t stream_) {
+  if (!code) return GEMM_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  NoallocDevice* nd = nullptr;
+  gemm_status_t s = noalloc_device(dev, &nd);
+  if (s != GEMM_OK) return s;
+  int32_t v = 0;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemcpy(&v, nd->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemset(nd->status, 0, sizeof(int32_t)) != cudaSuccess) return GEMM_ERR_CUDA;
+  *code = v;
+  return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_noalloc_set_timeout(uint64_t timeout_ns) {
+  if (timeout_ns == 0) return GEMM_ERR_INVALID_ARG;
+  g_noalloc_timeout_ns.store(timeout_ns);
+  return GEMM_OK;
 }
 

@@ -350,14 +350,18 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 107 (gemm_epilogue_t.c_act,
+/* ABI version of this header (major * 100 + minor): 108 (gemm_epilogue_t.c_act,
  * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex, gemm_config_t.cluster,
- * gemm_epilogue_t.out_scale and int8 D, gemm_config_t.half_tiles). */
+ * gemm_epilogue_t.out_scale and int8 D, gemm_config_t.half_tiles,
+ * gemm_noalloc_device_status and gemm_noalloc_set_timeout). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------
- * gemm_run_s8_noalloc -- the exact int8 GEMM (int32 accumulation, the same
- * kernels as gemm_run on an S8 plan) without allocating any device memory.
+ * gemm_run_s8_noalloc -- the exact int8 GEMM (int32 accumulation) without
+ * allocating any device memory.  It runs the int8 -> fp16 staging pass and the
+ * single-CTA tensor-core int8 kernel (gemm_run on an S8 plan may take the
+ * CTA-pair int8 kernel for large shapes instead; both give the same exact
+ * result); with K == 0 it runs the generic CUDA-core kernel on beta*C alone.
  * The paper has no counterpart: this is a service of the library.
  *
  * Why: some callers cannot allocate device memory when they call the GEMM --
@@ -397,6 +401,21 @@ gemm_status_t gemm_run_s8_noalloc(gemm_layout_t layoutA, gemm_layout_t layoutB,
                                   double beta, const void* C, int64_t ldc, void* D, int64_t ldd,
                                   const gemm_epilogue_t* epi, int32_t* status,
                                   gemm_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the library's own error word of
+ * gemm_run_s8_noalloc on the current device (the word its calls with
+ * status == NULL report to).  *code is 0 when no such call reported a failure
+ * since the last read, else the status of the first one (GEMM_ERR_TIMEOUT).
+ * Allocates nothing.  Like gemm_run_s8_noalloc, its first use on a device
+ * looks up the word's device address; make that first call before any stream
+ * capture.  The paper has no counterpart. */
+gemm_status_t gemm_noalloc_device_status(int32_t* code, gemm_stream_t stream);
+
+/* Set the bound, in nanoseconds (> 0; default 4e9), of the in-kernel waits of
+ * every later gemm_run_s8_noalloc call in this process (all devices).  A wait
+ * that runs past it records GEMM_ERR_TIMEOUT and its CTA winds down, as for
+ * gemm_plan_set_timeout.  The paper has no counterpart. */
+gemm_status_t gemm_noalloc_set_timeout(uint64_t timeout_ns);
 
 #ifdef __cplusplus
 }

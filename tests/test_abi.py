@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings():
-    assert G.gemm_abi_version() == 107
+    assert G.gemm_abi_version() == 108
     for s in range(6):
         assert G.gemm_status_string(s).startswith("GEMM_")
     assert "unknown" in G.gemm_status_string(99)

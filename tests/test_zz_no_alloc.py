@@ -1,15 +1,18 @@
-"""The allocation-free int8 entry point, gemm_run_s8_noalloc, against gemm_run.
+"""The allocation-free int8 entry point, gemm_run_s8_noalloc.
 
 Some callers cannot allocate device memory when they call the GEMM: their
 device memory was reserved up front by a framework's memory pool, or their loop
 cannot afford cudaMalloc/cudaFree and the synchronisation those imply.
 gemm_run_s8_noalloc serves them from a fixed staging array that the library
-holds on each device.  This test calls it through the C ABI and checks its
-output against the plan-based entry point (gemm_run) on the same inputs --
-bit for bit, the tolerance every int8 test here uses -- on two calls in a row
-(the second call reuses the array the first one left filled, with other shapes
-and layouts), and checks that a problem too large for the array is refused
-before anything is launched.
+holds on each device.  These tests call it through the C ABI and check its
+output against the plan-based entry point (gemm_run) and against the oracle on
+the same inputs -- bit for bit, the tolerance every int8 test here uses -- on
+two calls in a row (the second call reuses the array the first one left
+filled, with other shapes and layouts); check that a problem too large for the
+array is refused before anything is launched; and check that an in-kernel wait
+that runs out is reported through the library's own error word
+(gemm_noalloc_device_status), after which the same context computes the next
+call correctly.
 
 The file name makes pytest collect it last, so a run that stops at the first
 failure has already run every other test.  It needs no state from them.
@@ -51,8 +54,9 @@ PROBLEMS = [
 ]
 
 
-def test_noalloc_matches_gemm_run_on_two_calls_in_a_row():
+def test_noalloc_matches_gemm_run_and_oracle_on_two_calls_in_a_row():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert G.gemm_noalloc_device_status() == 0      # also clears what an earlier test left
     for call, p in enumerate(PROBLEMS):
         inp = I.generate(p, 300 + call)
         ref = H.DeviceProblem(inp)
@@ -68,7 +72,9 @@ def test_noalloc_matches_gemm_run_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         got.check_guards()
         H.check_close(got.result(), ref.result().cpu().numpy(), "s32", f"no-alloc call {call + 1}")
+        H.check_close(got.result(), H.oracle_full(inp), "s32", f"no-alloc call {call + 1} vs oracle")
     assert int(status.item()) == 0
+    assert G.gemm_noalloc_device_status() == 0
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
@@ -84,3 +90,27 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
                               G.make_epilogue(G.GEMM_S32), None,
                               torch.cuda.current_stream().cuda_stream)
     assert e.value.status == G.GEMM_ERR_UNSUPPORTED
+
+
+def test_noalloc_expired_wait_is_reported_and_context_survives():
+    """A wait bound far below a tile's run time makes the kernel's bounded waits
+    expire: the kernel records GEMM_ERR_TIMEOUT in the library's word and winds
+    down; gemm_noalloc_device_status reports it once, and with the default bound
+    restored the next call is exact again."""
+    p = PROBLEMS[0]
+    inp = I.generate(p, 310)
+    dp = H.DeviceProblem(inp)
+    assert G.gemm_noalloc_device_status() == 0
+    try:
+        G.gemm_noalloc_set_timeout(200)              # 200 ns
+        _noalloc_run(dp)
+        torch.cuda.synchronize()
+    finally:
+        G.gemm_noalloc_set_timeout(4_000_000_000)
+    assert G.gemm_noalloc_device_status() == G.GEMM_ERR_TIMEOUT
+    assert G.gemm_noalloc_device_status() == 0       # read once, then cleared
+    _noalloc_run(dp)
+    torch.cuda.synchronize()
+    assert G.gemm_noalloc_device_status() == 0
+    dp.check_guards()
+    H.check_close(dp.result(), H.oracle_full(inp), "s32", "no-alloc after an expired wait")
