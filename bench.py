@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--suite", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload measurements of the other BASELINE configs")
     ap.add_argument("--case", default=None,
                     help="run one named workload --iters times (profiling driver); see CASES")
     ap.add_argument("--iters", type=int, default=3)
@@ -328,6 +330,8 @@ def bench_ours(args, rank, world, local_rank):
             "data": "synthetic", "config": workload_config(world), "roofline": roofline,
             "clocks": clocks, "e2e": e2e, "gpu_launches": len(ins) * args.steps,
             "kernel_config": cfg_used}
+    if rank == 0 and not args.no_configs:
+        line["configs"] = measure_configs(G, device, gpu_id)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(budget_s=15.0)
     if rank == 0:
@@ -557,6 +561,143 @@ def run_suite(G, device, warmup=3, iters=20):
         plan.close()
         del A, B, C, D, bias, flush
         torch.cuda.empty_cache()
+
+
+# Every workload BASELINE names beside the contract's, measured in the default
+# run: (problem constructor, seed offset, bound of its roofline).
+def config_workloads():
+    from dense_gemm_epilogues_gb300 import inputs as I
+    out = [("cfg1_gemm_f16_tn_256", I.square_fp16_256(), 0, "tensor"),
+           ("cfg3_fc_bf16_8192x4096x11008_bias_relu", I.fc_bf16_8192x4096x11008(), 2, "tensor"),
+           ("cfg4_gemm_s8_tn_8192", I.int8_8192(), 3, "tensor"),
+           ("cfg5a_sgemm_f32_tn_4096_bias_relu", I.sgemm_4096_bias_relu(), 4, "alu")]
+    out += [(f"cfg5b_gemm_f16_tn_{n}", I.square_fp16(n), 5, "tensor") for n in (512, 1024, 2048, 4096, 16384)]
+    out += [("cfg5c_gemm_f16_tn_skinny_16384x64x16384", I.skinny_fp16_16384x64x16384(), 6, "hbm")]
+    return out
+
+
+def algorithmic_bytes(p, eb) -> int:
+    """Bytes a GEMM must move at least once: A, B, C (when read), bias, D."""
+    n = p.M * p.K * eb[p.ab] + p.K * p.N * eb[p.ab] + p.M * p.N * eb[p.d]
+    if p.c:
+        n += p.M * p.N * eb[p.c]
+    if p.bias:
+        n += (p.N if p.bias_mode == "col" else p.M) * eb[p.bias]
+    return n
+
+
+def ffma_peak_tflops(sm_count: int, sm_mhz: float) -> float:
+    """FP32 FFMA issue peak: 128 FP32 lanes per SM, 2 flops per FMA."""
+    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def measure_configs(G, device, gpu_id, min_region_s=0.4, max_iters=3000):
+    """One record per BASELINE workload: per-call device time by CUDA events on
+    the launching stream, L2 flushed before each call unless the inputs and
+    output exceed L2, with its own clock record and roofline."""
+    import torch
+    from dense_gemm_epilogues_gb300 import inputs as I
+    peaks = load_peaks()
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    eb = I.ELEM_BYTES
+    records = []
+    for name, p, k, bound in config_workloads():
+        inp = I.generate(p, I.BASE_SEED + k)
+        A, B = inp.A.to(device), inp.B.to(device)
+        C = inp.C.to(device) if inp.C is not None else None
+        bias = inp.bias.to(device) if inp.bias is not None else None
+        D = torch.empty((p.M, p.ldd), dtype=I.TORCH_DTYPES[p.d], device=device)
+        cc = p.c or ("s32" if p.ab == "s8" else "f32")
+        plan = G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[cc], device.index or 0)
+        bm = {"none": G.GEMM_BIAS_NONE, "col": G.GEMM_BIAS_COL, "row": G.GEMM_BIAS_ROW}[p.bias_mode]
+        epi = G.make_epilogue(G.DTYPE_CODES[p.d], bias.data_ptr() if bias is not None else 0,
+                              G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32, bm,
+                              G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE)
+
+        def call():
+            G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M,
+                       p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                       C.data_ptr() if C is not None else None, p.ldc if C is not None else 0,
+                       D.data_ptr(), p.ldd, epi, stream.cuda_stream)
+        abytes = algorithmic_bytes(p, eb)
+        flush_each = abytes < 2 * 129e6
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        call()
+        torch.cuda.synchronize()
+        est = max(time.perf_counter() - t0, 1e-6) + (1e-4 if flush_each else 0.0)
+        iters = int(min(max_iters, max(10, min_region_s / est)))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        sampler = ClockSampler(gpu_id)
+        sampler.start()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for e0, e1 in evs:
+            if flush_each:
+                flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        region_s = r0.elapsed_time(r1) / 1e3
+        per = [a.elapsed_time(b) / 1e3 for a, b in evs]
+        t_mean, t_med = statistics.mean(per), statistics.median(per)
+        cfg = plan.last_config()
+        status = plan.device_status()
+        flops = p.flops
+        rec = {"name": name, "M": p.M, "N": p.N, "K": p.K, "layout": p.layout_a + p.layout_b,
+               "ab": p.ab, "d": p.d, "alpha": p.alpha, "beta": p.beta,
+               "epilogue": (f"bias[{p.bias_mode}] " if p.bias else "") + (p.act if p.act != "none" else ""),
+               "kernel": cfg["kernel_name"], "tile": f"{cfg['bm']}x{cfg['bn']}", "grid": cfg["grid"],
+               "stream_k_tiles": cfg["sk_tiles"], "half_tiles": cfg["half_tiles"],
+               "iters": iters, "mean_us": round(t_mean * 1e6, 2), "median_us": round(t_med * 1e6, 2),
+               "l2": "flushed before each call (512 MB write)" if flush_each
+                     else "inputs and output exceed L2; no flush",
+               "algorithmic_bytes": abytes, "flops": flops, "status": status, "clocks": clocks}
+        if bound == "hbm":
+            ach = abytes / t_mean / 1e9
+            rec.update(value=round(ach, 1), unit="GB/s",
+                       roofline={"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                                 "peak_source": f"{peaks['source']} HBM copy bandwidth"},
+                       tflops=round(flops / t_mean / 1e12, 2))
+        elif bound == "alu":
+            mhz = clocks.get("sm_max_mhz") or 2070.0
+            pk = ffma_peak_tflops(sm_count, mhz)
+            ach = flops / t_mean / 1e12
+            rec.update(value=round(ach, 2), unit="TFLOP/s",
+                       roofline={"bound": "alu", "achieved": round(ach, 2), "peak": round(pk, 2),
+                                 "unit": "TFLOP/s", "frac": round(ach / pk, 4),
+                                 "peak_source": f"FFMA issue rate: {sm_count} SMs x 128 FP32 lanes x 2 flops "
+                                                f"x {mhz:.0f} MHz (maximum SM clock)"})
+            med = clocks.get("sm_mhz")
+            if med:
+                rec["roofline"]["frac_at_median_clock"] = round(ach / ffma_peak_tflops(sm_count, med), 4)
+        else:
+            pk, src = choose_tensor_peak(peaks, clocks, region_s)
+            ach = flops / t_mean / 1e12
+            unit = "TOP/s" if p.ab == "s8" else "TFLOP/s"
+            if p.ab == "s8":
+                src += "; int8 runs on the fp16 tensor-core kind (exact chunks), so its unit's peak is fp16's"
+            rec.update(value=round(ach, 2), unit=unit,
+                       roofline={"bound": "tensor", "achieved": round(ach, 2), "peak": pk, "unit": unit,
+                                 "frac": round(ach / pk, 4), "peak_source": src},
+                       gbs=round(abytes / t_mean / 1e9, 1))
+        records.append(rec)
+        plan.close()
+        del A, B, C, D, bias, inp
+        torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return records
 
 
 def run_batched_suite(G, device, warmup=3, iters=20):
