@@ -64,6 +64,10 @@ class Problem:
     act: str = "none"            # 'none' | 'relu'
     c_act: str = "none"          # transform of C as it is read: 'none' | 'relu'
     out_scale: float = 1.0       # int8 output of an int8 problem: requantisation scale
+    a_act: str = "none"          # transform of A as it is read: 'none' | 'relu' (after a_scale)
+    a_scale: float = 1.0         # multiplier of A's elements as they are read
+    b_act: str = "none"          # the same for B
+    b_scale: float = 1.0
     dist_a: Dist = U11
     dist_b: Dist = U11
     dist_c: Dist = Dist("normal", std=1.0)

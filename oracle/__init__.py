@@ -68,11 +68,12 @@ def _load_from(path: str):
     i64, dbl, vp, ci = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
     lib.oracle_gemm.restype = i64
     lib.oracle_gemm.argtypes = [ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
-                                dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, vp, i64, ci, ci, dbl]
+                                dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, vp, i64, ci, ci, dbl,
+                                ci, dbl, ci, dbl]
     lib.oracle_gemm_entries.restype = i64
     lib.oracle_gemm_entries.argtypes = [ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
                                         dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, i64, vp, vp,
-                                        vp, ci, dbl]
+                                        vp, ci, dbl, ci, dbl, ci, dbl]
     lib.oracle_gemm_pairs.restype = i64
     lib.oracle_gemm_pairs.argtypes = [ci, ci, ci, ci, i64, i64, i64, dbl, vp, i64, vp, i64,
                                       dbl, ci, vp, i64, ci, vp, ci, ci, ci, ci, vp, i64, ci]
@@ -116,9 +117,11 @@ def max_threads() -> int:
 def gemm(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
          beta=0.0, c_dtype=F32, C=None, ldc=0, bias_dtype=F32, bias=None,
          bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, ldd=None,
-         loop_order=0, nthreads=None, c_act=ACT_NONE, out_scale=1.0):
+         loop_order=0, nthreads=None, c_act=ACT_NONE, out_scale=1.0,
+         a_act=ACT_NONE, a_scale=1.0, b_act=ACT_NONE, b_scale=1.0):
     """Full D (row-major M x ldd, raw bits for 16-bit outputs) and the int32
-    overflow count.  Buffers are raw storage: numpy arrays or CPU tensors."""
+    overflow count.  Buffers are raw storage: numpy arrays or CPU tensors.
+    a_act/a_scale, b_act/b_scale: the transforms of A and B after load."""
     if ldd is None:
         ldd = N
     if nthreads is None:
@@ -127,7 +130,8 @@ def gemm(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
     n = _load().oracle_gemm(ab_dtype, layout_a, layout_b, M, N, K, float(alpha),
                             _ptr(A), lda, _ptr(B), ldb, float(beta), c_dtype, _ptr(C), ldc,
                             bias_dtype, _ptr(bias), bias_mode, act, c_act, d_dtype,
-                            D.ctypes.data, ldd, loop_order, nthreads, float(out_scale))
+                            D.ctypes.data, ldd, loop_order, nthreads, float(out_scale),
+                            a_act, float(a_scale), b_act, float(b_scale))
     if n < 0:
         raise ValueError("oracle_gemm: invalid arguments")
     return D, int(n)
@@ -136,7 +140,8 @@ def gemm(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
 def gemm_entries(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
                  rows, cols, beta=0.0, c_dtype=F32, C=None, ldc=0, bias_dtype=F32,
                  bias=None, bias_mode=BIAS_NONE, act=ACT_NONE, d_dtype=F32, nthreads=None,
-                 c_act=ACT_NONE, out_scale=1.0):
+                 c_act=ACT_NONE, out_scale=1.0, a_act=ACT_NONE, a_scale=1.0, b_act=ACT_NONE,
+                 b_scale=1.0):
     """D at the listed (rows[e], cols[e]) entries, in d_dtype (raw bits for 16-bit)."""
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     cols = np.ascontiguousarray(cols, dtype=np.int64)
@@ -147,7 +152,8 @@ def gemm_entries(ab_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
                                     _ptr(A), lda, _ptr(B), ldb, float(beta), c_dtype, _ptr(C),
                                     ldc, bias_dtype, _ptr(bias), bias_mode, act, c_act, d_dtype,
                                     rows.shape[0], rows.ctypes.data, cols.ctypes.data,
-                                    out.ctypes.data, nthreads, float(out_scale))
+                                    out.ctypes.data, nthreads, float(out_scale),
+                                    a_act, float(a_scale), b_act, float(b_scale))
     if n < 0:
         raise ValueError("oracle_gemm_entries: invalid arguments")
     return out, int(n)

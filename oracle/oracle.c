@@ -45,6 +45,16 @@
  *     the fp64 value in one step; fp32 output uses C's double->float conversion,
  *     which is the same rounding.  int32 output keeps the low 32 bits of the
  *     int64 value and counts every value outside the int32 range.
+ *   - Optional elementwise transforms of A and B as they are read (the
+ *     transforms applied after every load of "Flexible Performant GEMM Kernels
+ *     on GPUs", section 4.2, Figure 10: a simple scaling, an activation):
+ *     t(x) = act(scale * x) with act = none or ReLU (threshold 0), the scale
+ *     applied first.  The tensor cores multiply 16-bit operands, so for fp16 and
+ *     bf16 operands the transformed value is taken as the product in fp32
+ *     (rounded to nearest even), then the activation, then rounded to nearest
+ *     even back to the operand's own type; fp32 operands keep the fp32 value;
+ *     int8 operands admit the activation only (any scale would leave the
+ *     integers).  The sum then runs over t_A(a(i,k)) * t_B(b(k,j)).
  *   - int8 output of an int8 problem (the requantising cast): the int32 result v
  *     (low 32 bits, as above) is converted to fp32, multiplied by the fp32 scale
  *     out_scale, rounded to the nearest integer with ties to even, and saturated
@@ -199,6 +209,10 @@ typedef struct {
     int c_dtype, bias_dtype, bias_mode, act, d_dtype;
     int c_act;   /* transform applied to each C element as it is read */
     double out_scale;   /* int8 output: requantisation scale (applied in fp32) */
+    int a_act;          /* transforms applied to each A and B element as it is read */
+    double a_scale;
+    int b_act;
+    double b_scale;
 } problem_t;
 
 static int is_int_problem(const problem_t* p) { return p->ab_dtype == OR_S8; }
@@ -260,6 +274,21 @@ static int store_int_out(const problem_t* p, void* D, int64_t idx, int64_t v) {
     return (v < INT32_MIN || v > INT32_MAX) ? 1 : 0;
 }
 
+/* The transform of one operand element after it is read (see the header):
+ * act(scale * x), the product in fp32, rounded back to the operand's type. */
+static double transform_operand(int dtype, double x, int act, double scale) {
+    if (dtype == OR_S8) return (act == OR_ACT_RELU && x < 0.0) ? 0.0 : x;
+    double v = (double)((float)scale * (float)x);
+    if (act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;
+    if (dtype == OR_F16) return oracle_f16_to_double(oracle_f16_from_double(v));
+    if (dtype == OR_BF16) return oracle_bf16_to_double(oracle_bf16_from_double(v));
+    return v;   /* fp32: already an fp32 value */
+}
+
+static int has_transform(const problem_t* p) {
+    return p->a_act != OR_ACT_NONE || p->b_act != OR_ACT_NONE || p->a_scale != 1.0 || p->b_scale != 1.0;
+}
+
 /* Decoding tables for the 16-bit formats: entry b is the value of bit pattern
  * b, filled once from the decoders above. */
 static double f16_table[65536], bf16_table[65536];
@@ -289,6 +318,12 @@ static double dot_float(const problem_t* p, int64_t i, int64_t j) {
     const int64_t db = p->K > 1 ? b_offset(p->layout_b, 1, j, p->ldb) - b0 : 0;
     double acc = 0.0;
     int64_t ia = a0, ib = b0;
+    if (has_transform(p)) {
+        for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db)
+            acc += transform_operand(p->ab_dtype, load_float(p->ab_dtype, p->A, ia), p->a_act, p->a_scale) *
+                   transform_operand(p->ab_dtype, load_float(p->ab_dtype, p->B, ib), p->b_act, p->b_scale);
+        return acc;
+    }
     switch (p->ab_dtype) {
     case OR_F32: {
         const float *A = (const float*)p->A, *B = (const float*)p->B;
@@ -319,6 +354,14 @@ static int64_t dot_int(const problem_t* p, int64_t i, int64_t j) {
     const int64_t db = p->K > 1 ? b_offset(p->layout_b, 1, j, p->ldb) - b0 : 0;
     const int8_t *A = (const int8_t*)p->A, *B = (const int8_t*)p->B;
     int64_t acc = 0, ia = a0, ib = b0;
+    if (has_transform(p)) {
+        for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) {
+            const int64_t a = (p->a_act == OR_ACT_RELU && A[ia] < 0) ? 0 : A[ia];
+            const int64_t b = (p->b_act == OR_ACT_RELU && B[ib] < 0) ? 0 : B[ib];
+            acc += a * b;
+        }
+        return acc;
+    }
     for (int64_t k = 0; k < p->K; ++k, ia += da, ib += db) acc += (int64_t)A[ia] * (int64_t)B[ib];
     return acc;
 }
@@ -341,6 +384,10 @@ static int valid_problem(const problem_t* p) {
     if (p->beta != 0.0 && (p->C == NULL || p->ldc < p->N)) return 0;
     if (p->bias_mode != OR_BIAS_NONE && p->bias == NULL) return 0;
     if (p->c_act != OR_ACT_NONE && p->c_act != OR_ACT_RELU) return 0;
+    if (p->a_act != OR_ACT_NONE && p->a_act != OR_ACT_RELU) return 0;
+    if (p->b_act != OR_ACT_NONE && p->b_act != OR_ACT_RELU) return 0;
+    if (!isfinite(p->a_scale) || !isfinite(p->b_scale)) return 0;
+    if (is_int_problem(p) && (p->a_scale != 1.0 || p->b_scale != 1.0)) return 0;
     if (is_int_problem(p)) {
         if (p->d_dtype != OR_S32 && p->d_dtype != OR_S8) return 0;
         if (p->d_dtype == OR_S8 && !isfinite(p->out_scale)) return 0;
@@ -365,9 +412,11 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
                     double beta, int c_dtype, const void* C, int64_t ldc,
                     int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                     int d_dtype, void* D, int64_t ldd,
-                    int loop_order, int nthreads, double out_scale) {
+                    int loop_order, int nthreads, double out_scale,
+                    int a_act, double a_scale, int b_act, double b_scale) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, out_scale};
+                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, out_scale,
+                   a_act, a_scale, b_act, b_scale};
     if (!valid_problem(&p)) return -1;
     if (M == 0 || N == 0) return 0;
     init_tables();
@@ -387,8 +436,8 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
         for (int64_t k = 0; k < K; ++k)
             for (int64_t i = 0; i < M; ++i)
                 for (int64_t j = 0; j < N; ++j)
-                    acc[i * N + j] += load_int(ab_dtype, A, a_offset(layout_a, i, k, lda)) *
-                                      load_int(ab_dtype, B, b_offset(layout_b, k, j, ldb));
+                    acc[i * N + j] += (int64_t)transform_operand(OR_S8, (double)load_int(ab_dtype, A, a_offset(layout_a, i, k, lda)), a_act, 1.0) *
+                                      (int64_t)transform_operand(OR_S8, (double)load_int(ab_dtype, B, b_offset(layout_b, k, j, ldb)), b_act, 1.0);
         for (int64_t i = 0; i < M; ++i)
             for (int64_t j = 0; j < N; ++j)
                 overflow += store_int_out(&p, D, i * ldd + j, epilogue_int(&p, i, j, acc[i * N + j]));
@@ -400,8 +449,8 @@ int64_t oracle_gemm(int ab_dtype, int layout_a, int layout_b,
     for (int64_t k = 0; k < K; ++k)
         for (int64_t i = 0; i < M; ++i)
             for (int64_t j = 0; j < N; ++j)
-                acc[i * N + j] += load_float(ab_dtype, A, a_offset(layout_a, i, k, lda)) *
-                                  load_float(ab_dtype, B, b_offset(layout_b, k, j, ldb));
+                acc[i * N + j] += transform_operand(ab_dtype, load_float(ab_dtype, A, a_offset(layout_a, i, k, lda)), a_act, a_scale) *
+                                  transform_operand(ab_dtype, load_float(ab_dtype, B, b_offset(layout_b, k, j, ldb)), b_act, b_scale);
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j)
             store_float(d_dtype, D, i * ldd + j, epilogue_float(&p, i, j, acc[i * N + j]));
@@ -420,9 +469,11 @@ int64_t oracle_gemm_entries(int ab_dtype, int layout_a, int layout_b,
                             double beta, int c_dtype, const void* C, int64_t ldc,
                             int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                             int d_dtype, int64_t n_entries, const int64_t* rows, const int64_t* cols,
-                            void* out, int nthreads, double out_scale) {
+                            void* out, int nthreads, double out_scale,
+                            int a_act, double a_scale, int b_act, double b_scale) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, out_scale};
+                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, out_scale,
+                   a_act, a_scale, b_act, b_scale};
     if (!valid_problem(&p)) return -1;
     for (int64_t e = 0; e < n_entries; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
@@ -501,7 +552,8 @@ int64_t oracle_gemm_pairs(int unit, int ab_dtype, int layout_a, int layout_b,
                           int bias_dtype, const void* bias, int bias_mode, int act, int c_act,
                           int d_dtype, void* D, int64_t ldd, int nthreads) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, 1.0};
+                   lda, ldb, ldc, ldd, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, 1.0,
+                   OR_ACT_NONE, 1.0, OR_ACT_NONE, 1.0};
     if (!valid_pair_problem(&p, unit)) return -1;
     if (M == 0 || N == 0) return 0;
     init_tables();
@@ -522,7 +574,8 @@ int64_t oracle_gemm_pairs_entries(int unit, int ab_dtype, int layout_a, int layo
                                   int d_dtype, int64_t n_entries, const int64_t* rows,
                                   const int64_t* cols, void* out, int nthreads) {
     problem_t p = {ab_dtype, layout_a, layout_b, M, N, K, alpha, beta, A, B, C, bias,
-                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, 1.0};
+                   lda, ldb, ldc, N, c_dtype, bias_dtype, bias_mode, act, d_dtype, c_act, 1.0,
+                   OR_ACT_NONE, 1.0, OR_ACT_NONE, 1.0};
     if (!valid_pair_problem(&p, unit)) return -1;
     for (int64_t e = 0; e < n_entries; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;

@@ -31,7 +31,8 @@ def _oracle_kwargs(p: I.Problem, inp: I.Inputs) -> dict:
     return dict(beta=p.beta, c_dtype=OR_DT[p.c] if p.c else O.F32, C=inp.C,
                 ldc=p.ldc if p.c else 0, bias_dtype=OR_DT[p.bias] if p.bias else O.F32,
                 bias=inp.bias, bias_mode=OR_BIAS[p.bias_mode], act=OR_ACT[p.act],
-                d_dtype=OR_DT[p.d], c_act=OR_ACT[p.c_act], out_scale=p.out_scale)
+                d_dtype=OR_DT[p.d], c_act=OR_ACT[p.c_act], out_scale=p.out_scale,
+                a_act=OR_ACT[p.a_act], a_scale=p.a_scale, b_act=OR_ACT[p.b_act], b_scale=p.b_scale)
 
 
 def oracle_full(inp: I.Inputs) -> np.ndarray:
@@ -164,6 +165,21 @@ def sample_entries(M: int, N: int, n: int, seed: int, tile_m=128, tile_n=256):
             rows.append(r)
             cols.append(c)
     return np.array(rows, dtype=np.int64), np.array(cols, dtype=np.int64)
+
+
+def boundary_entries(M: int, N: int, row_block: int = 128, col_block: int = 64):
+    """Whole rows at both edges of every row block of D (the first and last row
+    each CTA of a tile owns) and whole columns at both edges of every column
+    block (the first and last column of each epilogue chunk), as (rows, cols)
+    entry lists.  Every tile then has at least one whole row and one whole
+    column of its outputs checked."""
+    rs = sorted({r for t in range(0, M, row_block) for r in (t, min(t + row_block - 1, M - 1))})
+    cs = sorted({c for t in range(0, N, col_block) for c in (t, min(t + col_block - 1, N - 1))})
+    rows = np.concatenate([np.repeat(np.asarray(rs, dtype=np.int64), N),
+                           np.tile(np.arange(M, dtype=np.int64), len(cs))])
+    cols = np.concatenate([np.tile(np.arange(N, dtype=np.int64), len(rs)),
+                           np.repeat(np.asarray(cs, dtype=np.int64), M)])
+    return rows, cols
 
 
 def tma_aligned(p: I.Problem, mult: int = 8) -> I.Problem:

@@ -32,7 +32,8 @@ def run_oracle(inp: I.Inputs, loop_order=0, nthreads=None):
                     bias_dtype=DT[p.bias] if p.bias else O.F32, bias=inp.bias,
                     bias_mode=BIAS[p.bias_mode], act=ACT[p.act], d_dtype=DT[p.d], ldd=p.ldd,
                     loop_order=loop_order, nthreads=nthreads, c_act=ACT[p.c_act],
-                    out_scale=p.out_scale)
+                    out_scale=p.out_scale, a_act=ACT[p.a_act], a_scale=p.a_scale,
+                    b_act=ACT[p.b_act], b_scale=p.b_scale)
     return D[:, :p.N], ovf
 
 
@@ -80,7 +81,9 @@ def test_hand_worked_examples(case, layout):
                     ldb, beta=case["beta"], c_dtype=DT[case["c"]], C=C, ldc=N,
                     bias_dtype=DT[case.get("bias_dtype", "f32")], bias=bias,
                     bias_mode=BIAS[case["bias_mode"]], act=ACT[case["act"]],
-                    d_dtype=DT[case["d"]], c_act=ACT[case.get("c_act", "none")])
+                    d_dtype=DT[case["d"]], c_act=ACT[case.get("c_act", "none")],
+                    a_act=ACT[case.get("a_act", "none")], a_scale=case.get("a_scale", 1.0),
+                    b_act=ACT[case.get("b_act", "none")], b_scale=case.get("b_scale", 1.0))
     assert ovf == 0
     if "D_bits" in case:
         assert D.tolist() == case["D_bits"]
@@ -469,3 +472,118 @@ def test_requant_matches_numpy_closed_form():
     v32 = v.astype(np.int32)
     q = np.clip(np.rint(v32.astype(np.float32) * np.float32(0.0123)), -128, 127).astype(np.int8)
     np.testing.assert_array_equal(D, q)
+
+
+# --------------------------------------------------------------------------
+# Transforms of A and B after load ("Flexible Performant GEMM Kernels on GPUs",
+# section 4.2, Figure 10): t(x) = act(scale * x), product in fp32, rounded
+# back to a 16-bit operand's type.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("ab", ["f16", "bf16", "f32", "s8"])
+@pytest.mark.parametrize("acts", [("relu", "none"), ("none", "relu"), ("relu", "relu")])
+def test_transform_relu_matches_numpy_on_small_integers(layout, ab, acts):
+    """Small integers stay exact through every step, so the oracle must equal
+    numpy's int64 product of the rectified logical matrices."""
+    M, N, K = 11, 13, 17
+    cd = "s32" if ab == "s8" else "f32"
+    p = I.Problem("t_relu", ab, layout[0], layout[1], M, N, K, d=cd, a_act=acts[0], b_act=acts[1],
+                  alpha=2.0, beta=-1.0, c=cd, dist_c=I.Dist("small", -9, 9),
+                  dist_a=I.Dist("small", -4, 4), dist_b=I.Dist("small", -4, 4), pad_a=1, pad_b=3)
+    inp = I.generate(p, 41, keep_logical=True)
+    a = inp.logical["a"].to(torch.float64).numpy().astype(np.int64)
+    b = inp.logical["b"].to(torch.float64).numpy().astype(np.int64)
+    c = inp.logical["c"].to(torch.float64).numpy().astype(np.int64)
+    if acts[0] == "relu":
+        a = np.maximum(a, 0)
+    if acts[1] == "relu":
+        b = np.maximum(b, 0)
+    D, ovf = run_oracle(inp)
+    assert ovf == 0
+    np.testing.assert_array_equal(D.astype(np.int64), 2 * (a @ b) - c)
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("scales", [(2.0, 1.0), (1.0, 0.25), (-4.0, 0.5)])
+def test_transform_power_of_two_scales_factor_out(ab, scales):
+    """Scaling by powers of two is exact in every format, so the product of
+    scaled operands is the product times sa * sb, bit for bit."""
+    p = I.Problem("t_scale", ab, "N", "T", 9, 12, 21, dist_a=I.Dist("small", -8, 8),
+                  dist_b=I.Dist("small", -8, 8))
+    inp = I.generate(p, 42)
+    base, _ = run_oracle(inp)
+    scaled, _ = run_oracle(I.Inputs(inp.A, inp.B, inp.C, inp.bias,
+                                    p.with_(a_scale=scales[0], b_scale=scales[1])))
+    np.testing.assert_array_equal(scaled.astype(np.float64),
+                                  base.astype(np.float64) * scales[0] * scales[1])
+
+
+# Scales for which, on some fp16 x in [1, 2), rounding fp32(s) * x to fp32 first
+# and then to fp16 differs from rounding the exact product to fp16 once (found by
+# a search over random fp32 scales; the test below re-checks that they do).
+DOUBLE_ROUNDING_SCALES = [0.9447439312934875, 0.7901661992073059]
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16"])
+def test_transform_takes_the_scale_in_fp32_then_rounds_to_the_operand_type(ab):
+    """For every fp16 (bf16) value in [1, 2), a grid of other values, and several
+    scales, the transformed element the sum uses is round_type(fp32(s) * fp32(x)),
+    computed here with numpy's float32 product and numpy's float16 (torch's
+    bfloat16) rounding.  A = the values as one column, B = 1, so D[i, 0] is t(A[i]).
+    For fp16 the scales include ones where taking the product exactly (in fp64)
+    and rounding once gives a different element, so the fp32 step is pinned."""
+    mant = 1024 if ab == "f16" else 128
+    grid = torch.cat([torch.arange(mant, 2 * mant, dtype=torch.float64) / mant,
+                      torch.linspace(-7.3, 7.9, 211, dtype=torch.float64)])
+    vals = grid.to(I.TORCH_DTYPES[ab])
+    M = vals.numel()
+    x32 = vals.to(torch.float32).numpy()
+    differs = 0
+    for s in [0.1, 1.0 / 3.0, -2.7182817, 0.7071068] + DOUBLE_ROUNDING_SCALES:
+        p = I.Problem("t_round", ab, "T", "N", M, 1, 1, a_scale=s, a_act="relu")
+        inp = I.Inputs(A=vals.reshape(M, 1).contiguous(), B=torch.ones(1, 1, dtype=vals.dtype),
+                       C=None, bias=None, problem=p)
+        D, _ = run_oracle(inp)
+        prod = np.maximum(np.float32(s) * x32, np.float32(0.0))
+        if ab == "f16":
+            want = prod.astype(np.float16).astype(np.float64)
+            once = np.maximum(np.float64(np.float32(s)) * x32.astype(np.float64), 0.0).astype(np.float16)
+            differs += int(np.count_nonzero(once.astype(np.float64) != want))
+        else:
+            want = torch.from_numpy(prod).to(torch.bfloat16).to(torch.float64).numpy()
+        np.testing.assert_array_equal(D[:, 0].astype(np.float64), want)
+    if ab == "f16":
+        assert differs > 0, "the scale grid no longer tells one rounding from two"
+
+
+def test_transform_fp32_operand_keeps_the_fp32_product():
+    """An fp32 operand is not narrowed: t(x) = fp32(s * x)."""
+    x = np.array([[1.0], [3.0], [-0.1]], dtype=np.float32)
+    s = 0.1
+    p = I.Problem("t_f32", "f32", "T", "N", 3, 1, 1, a_scale=s)
+    inp = I.Inputs(A=torch.from_numpy(x), B=torch.ones(1, 1), C=None, bias=None, problem=p)
+    D, _ = run_oracle(inp)
+    np.testing.assert_array_equal(D[:, 0], (np.float32(s) * x[:, 0]).astype(np.float32))
+
+
+def test_transform_loop_orders_agree():
+    p = I.Problem("t_lo", "bf16", "T", "N", 13, 11, 19, a_scale=0.3, a_act="relu", b_scale=-1.7,
+                  alpha=1.5, beta=0.5, c="f32")
+    inp = I.generate(p, 43)
+    np.testing.assert_array_equal(run_oracle(inp, 0)[0], run_oracle(inp, 1)[0])
+    pi = I.Problem("t_lo8", "s8", "N", "T", 9, 10, 33, d="s32", dist_a=I.I8, dist_b=I.I8,
+                   a_act="relu", b_act="relu")
+    inp = I.generate(pi, 44)
+    np.testing.assert_array_equal(run_oracle(inp, 0)[0], run_oracle(inp, 1)[0])
+
+
+def test_transform_arguments_rejected():
+    A = np.zeros(4, np.int8)
+    with pytest.raises(ValueError):   # a scale on int8 operands leaves the integers
+        O.gemm(O.S8, O.LAYOUT_T, O.LAYOUT_N, 2, 2, 2, 1.0, A, 2, A, 2, d_dtype=O.S32, a_scale=2.0)
+    Af = np.zeros(4, np.float32)
+    with pytest.raises(ValueError):
+        O.gemm(O.F32, O.LAYOUT_T, O.LAYOUT_N, 2, 2, 2, 1.0, Af, 2, Af, 2, b_scale=float("inf"))
+    with pytest.raises(ValueError):
+        O.gemm(O.F32, O.LAYOUT_T, O.LAYOUT_N, 2, 2, 2, 1.0, Af, 2, Af, 2, a_act=5)

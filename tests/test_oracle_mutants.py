@@ -42,6 +42,18 @@ MUTANTS = {
     "requant_no_saturation": ("if (r > 127.0f) r = 127.0f;", ""),
     "requant_round_half_away": ("float r = nearbyintf(prod);                             /* ties", "float r = roundf(prod);                             /* ties"),
     "requant_scale_ignored": ("(float)v32 * (float)p->out_scale;", "(float)v32 * 1.0f;"),
+    # transforms of A and B after load
+    "transform_A_dropped": ("acc += transform_operand(p->ab_dtype, load_float(p->ab_dtype, p->A, ia), p->a_act, p->a_scale) *",
+                            "acc += load_float(p->ab_dtype, p->A, ia) *"),
+    "transform_B_takes_A_parameters": ("load_float(p->ab_dtype, p->B, ib), p->b_act, p->b_scale);",
+                                       "load_float(p->ab_dtype, p->B, ib), p->a_act, p->a_scale);"),
+    "transform_relu_before_scale": ("    double v = (double)((float)scale * (float)x);\n    if (act == OR_ACT_RELU) v = (v > 0.0) ? v : 0.0;",
+                                    "    double v = (act == OR_ACT_RELU && x < 0.0) ? 0.0 : x;\n    v = (double)((float)scale * (float)v);"),
+    "transform_scale_in_fp64": ("double v = (double)((float)scale * (float)x);", "double v = scale * x;"),
+    "transform_not_rounded_to_f16": ("if (dtype == OR_F16) return oracle_f16_to_double(oracle_f16_from_double(v));",
+                                     "if (dtype == OR_F16) return v;"),
+    "transform_int8_relu_dropped": ("const int64_t b = (p->b_act == OR_ACT_RELU && B[ib] < 0) ? 0 : B[ib];",
+                                    "const int64_t b = B[ib];"),
     # complex / dual-number GEMM
     "pair_unit_square_sign": ("re += a * c + u2 * (b * d);", "re += a * c - u2 * (b * d);"),
     "pair_dual_as_complex": ("unit == OR_UNIT_IMAGINARY ? -1.0 : 0.0;", "unit == OR_UNIT_IMAGINARY ? -1.0 : -1.0;"),
@@ -70,6 +82,10 @@ PINS = [
     lambda: T.test_requant_ties_round_to_even_and_saturate(),
     lambda: T.test_requant_product_is_taken_in_fp32(),
     lambda: T.test_requant_matches_numpy_closed_form(),
+    lambda: [T.test_transform_relu_matches_numpy_on_small_integers(lay, ab, acts) for lay in T.LAYOUTS
+             for ab in ["f16", "s8"] for acts in [("relu", "none"), ("none", "relu")]],
+    lambda: [T.test_transform_takes_the_scale_in_fp32_then_rounds_to_the_operand_type(ab)
+             for ab in ["f16", "bf16"]],
     lambda: [TP.test_hand_worked_pairs(c, lay) for c in TP._golden() for lay in TP.LAYOUTS],
     lambda: [TP.test_block_matrix_representation(u, lay) for u in ("complex", "dual")
              for lay in TP.LAYOUTS],
