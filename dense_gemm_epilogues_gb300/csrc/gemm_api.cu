@@ -568,11 +568,13 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   const uint64_t na = (bt.count > 1 && bt.sa != 0) ? (uint64_t)bt.count : 1;
   const uint64_t nb = (bt.count > 1 && bt.sb != 0) ? (uint64_t)bt.count : 1;
   bool ok;
+  // MN-major operands: boxes of 64 (MN) x one pipeline stage of K, one per stage.
+  const uint32_t kstage = (uint32_t)tc_pair_k_per_stage();
   if (!a_mn) ok = encode_3d(&tp.tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, na, bt.sa, TC_BK, TC_BM);
-  else ok = encode_3d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, na, bt.sa, 64, TC_BK);
+  else ok = encode_3d(&tp.tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, na, bt.sa, 64, kstage);
   if (!ok) return GEMM_ERR_CUDA;
   if (!b_mn) ok = encode_3d(&tp.tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, nb, bt.sb, TC_BK, 128);
-  else ok = encode_3d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, bt.sb, 64, TC_BK);
+  else ok = encode_3d(&tp.tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, nb, bt.sb, 64, kstage);
   if (!ok) return GEMM_ERR_CUDA;
   // Half-tile units load 64 columns of B per CTA: K-major boxes of 64 rows (an
   // MN-major box is already 64 columns wide).

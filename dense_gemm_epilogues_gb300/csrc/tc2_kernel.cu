@@ -62,8 +62,10 @@ struct PairThreads {
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 constexpr uint32_t PAIR_TMEM_COLS = 512;
-constexpr int MN_BOX = 64;
-constexpr uint32_t MN_BOX_BYTES = MN_BOX * TC_BK * 2;
+constexpr int MN_BOX = 64;   // MN extent of one TMA box of an MN-major operand (128 bytes)
+// An MN-major operand is loaded in boxes of 64 (MN) x PAIR_SLABS * 64 (K): one
+// box per 64-wide MN group per stage (fewer, larger copies than one per K block).
+constexpr uint32_t MN_STAGE_BYTES = MN_BOX * 2 * PAIR_SLABS * TC_BK;
 
 __device__ __forceinline__ void pair_tile_coords(int t, const TcParams& p, int& bz, int& tm, int& tn) {
   bz = t / p.tiles_per_batch;                     // problem of the batch
@@ -91,8 +93,9 @@ __device__ __forceinline__ bool warp_wait_pair(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// One CTA pair per cluster of two.
-template <bool INT_MODE>
+// One CTA pair per cluster of two.  A_MN / B_MN: the operand is stored
+// MN-contiguous (A column-major, B row-major) rather than K-contiguous.
+template <bool INT_MODE, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
   constexpr int EPI_WARPS = PairThreads<INT_MODE>::EPI_WARPS;
@@ -172,37 +175,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
         // This CTA's half of B's columns: 128 of a whole tile, 64 of a half-tile unit.
         const int n0 = half < 0 ? tn * PAIR_BN + (int)rank * (PAIR_BN / 2)
                                 : tn * PAIR_BN + half * (PAIR_BN / 2) + (int)rank * (PAIR_BN / 4);
-        const uint32_t slab_bytes = half < 0 ? (uint32_t)PAIR_SLAB_BYTES : (uint32_t)(PAIR_A_BYTES + PAIR_B_BYTES / 2);
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
+        // B bytes of one K block for this CTA: 128 columns of a whole tile, 64 of a half-tile unit.
+        const uint32_t b_slab_bytes = half < 0 ? (uint32_t)PAIR_B_BYTES : (uint32_t)(PAIR_B_BYTES / 2);
         for (int kb = kb0; kb < kb1; kb += PAIR_SLABS) {
           const int nsl = kb1 - kb < PAIR_SLABS ? kb1 - kb : PAIR_SLABS;   // K blocks in this stage
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
-          if (leader) mbar_expect_tx(fb_local, 2u * (uint32_t)nsl * slab_bytes);
+          // An MN-major operand arrives in stage-deep boxes, which always carry the
+          // whole stage (zero-filled past K); a K-major one in one box per K block.
+          const uint32_t a_bytes = (uint32_t)(A_MN ? PAIR_SLABS : nsl) * (uint32_t)PAIR_A_BYTES;
+          const uint32_t b_bytes = (uint32_t)(B_MN ? PAIR_SLABS : nsl) * b_slab_bytes;
+          if (leader) mbar_expect_tx(fb_local, 2u * (a_bytes + b_bytes));
           const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, pair_leader);
-          const uint32_t st = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
-          for (int sl = 0; sl < nsl; ++sl) {
-          const uint32_t sa = st + (uint32_t)(sl * PAIR_A_BYTES);
-          const uint32_t sb = st + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES + sl * PAIR_B_BYTES);
-          const int k0 = (kb + sl) * TC_BK;
-          if (p.a_mn_major) {
+          const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+          const uint32_t sb = sa + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES);
+          const int k0 = kb * TC_BK;
+          if constexpr (A_MN) {
 #pragma unroll
             for (int h = 0; h < TC_BM / MN_BOX; ++h)
-              tma_load_3d_pair_hint(sa + h * MN_BOX_BYTES, &p.tmA, m0 + h * MN_BOX, k0, za, fb, a_policy);
+              tma_load_3d_pair_hint(sa + h * MN_STAGE_BYTES, &p.tmA, m0 + h * MN_BOX, k0, za, fb, a_policy);
           } else {
-            tma_load_3d_pair_hint(sa, &p.tmA, k0, m0, za, fb, a_policy);
+            for (int sl = 0; sl < nsl; ++sl)
+              tma_load_3d_pair_hint(sa + sl * PAIR_A_BYTES, &p.tmA, k0 + sl * TC_BK, m0, za, fb, a_policy);
           }
-          if (half >= 0) {
-            // 64 columns: one MN-major box, or a K-major box of 64 rows.
-            if (p.b_mn_major) tma_load_3d_pair(sb, &p.tmB, n0, k0, zb, fb);
-            else tma_load_3d_pair(sb, &p.tmBh, k0, n0, zb, fb);
-          } else if (p.b_mn_major) {
-#pragma unroll
-            for (int h = 0; h < (PAIR_BN / 2) / MN_BOX; ++h)
-              tma_load_3d_pair(sb + h * MN_BOX_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
+          if constexpr (B_MN) {
+            // 128 columns: two stage-deep boxes of 64; a half-tile unit's 64 columns: one.
+            const int nh = half < 0 ? (PAIR_BN / 2) / MN_BOX : 1;
+            for (int h = 0; h < nh; ++h)
+              tma_load_3d_pair(sb + h * MN_STAGE_BYTES, &p.tmB, n0 + h * MN_BOX, k0, zb, fb);
           } else {
-            tma_load_3d_pair(sb, &p.tmB, k0, n0, zb, fb);
-          }
+            // One box per K block: 128 rows (tmB), or 64 rows for a half-tile unit (tmBh).
+            const CUtensorMap* tb = half < 0 ? &p.tmB : &p.tmBh;
+            for (int sl = 0; sl < nsl; ++sl) tma_load_3d_pair(sb + sl * PAIR_B_BYTES, tb, k0 + sl * TC_BK, n0, zb, fb);
           }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -245,18 +250,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
             const int nsl = kb_end - kb < PAIR_SLABS ? kb_end - kb : PAIR_SLABS;
             if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t st = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+            const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+            const uint32_t sb = sa + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES);
 #pragma unroll
             for (int sl = 0; sl < PAIR_SLABS; ++sl) {
               if (sl >= nsl) break;
-              const uint32_t sa = st + (uint32_t)(sl * PAIR_A_BYTES);
-              const uint32_t sb = st + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES + sl * PAIR_B_BYTES);
 #pragma unroll
               for (int kk = 0; kk < TC_BK / 16; ++kk) {
-                const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + kk * 2048u, MN_BOX_BYTES, 1024)
-                                                 : smem_desc_sw128(sa + kk * 32u, 16, 1024);
-                const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048u, MN_BOX_BYTES, 1024)
-                                                 : smem_desc_sw128(sb + kk * 32u, 16, 1024);
+                // K-major: one 128-byte-wide box per K block; the 16-element K step is
+                // 32 bytes inside each row.  MN-major: stage-deep boxes of 64 MN; the K
+                // step is 16 rows of 128 bytes, LBO steps from one 64-wide box to the next.
+                const uint64_t ad = A_MN ? smem_desc_sw128(sa + sl * (TC_BK * 128u) + kk * 2048u, MN_STAGE_BYTES, 1024)
+                                         : smem_desc_sw128(sa + sl * PAIR_A_BYTES + kk * 32u, 16, 1024);
+                const uint64_t bd = B_MN ? smem_desc_sw128(sb + sl * (TC_BK * 128u) + kk * 2048u, MN_STAGE_BYTES, 1024)
+                                         : smem_desc_sw128(sb + sl * PAIR_B_BYTES + kk * 32u, 16, 1024);
                 tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb > kb_begin || sl > 0 || kk > 0) ? 1u : 0u);
               }
             }
@@ -433,12 +440,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
   if (warp == 1) tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
 }
 
-template <bool INT_MODE>
+template <bool INT_MODE, bool A_MN, bool B_MN>
 int max_clusters_for(int device) {
   static int cached[64] = {};
   if (device < 0 || device >= 64) return 0;
   if (cached[device] > 0) return cached[device];
-  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)PAIR_SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -453,7 +460,7 @@ int max_clusters_for(int device) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -461,7 +468,7 @@ int max_clusters_for(int device) {
   return n;
 }
 
-template <bool INT_MODE>
+template <bool INT_MODE, bool A_MN, bool B_MN>
 cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   static_assert(PAIR_SMEM <= 232448, "shared memory budget");
   int dev = 0;
@@ -469,7 +476,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PAIR_SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -488,7 +495,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = p.sk_first_tile == p.num_tiles ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE>, p);
+  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, p);
 }
 
 }  // namespace
@@ -498,13 +505,23 @@ int tc_pair_k_per_stage() { return PAIR_SLABS * TC_BK; }
 size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
 
 int tc_pair_max_clusters(int device) {
-  const int a = max_clusters_for<false>(device);
-  const int b = max_clusters_for<true>(device);
+  // Every instantiation has the same threads per mode and shared memory.
+  const int a = max_clusters_for<false, false, false>(device);
+  const int b = max_clusters_for<true, false, false>(device);
   return a < b ? a : b;
 }
 
+template <bool INT_MODE>
+cudaError_t launch_layouts(const TcParams& p, int clusters, cudaStream_t stream) {
+  if (p.a_mn_major)
+    return p.b_mn_major ? launch_mode<INT_MODE, true, true>(p, clusters, stream)
+                        : launch_mode<INT_MODE, true, false>(p, clusters, stream);
+  return p.b_mn_major ? launch_mode<INT_MODE, false, true>(p, clusters, stream)
+                      : launch_mode<INT_MODE, false, false>(p, clusters, stream);
+}
+
 cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
-  return p.chunk_kb > 0 ? launch_mode<true>(p, clusters, stream) : launch_mode<false>(p, clusters, stream);
+  return p.chunk_kb > 0 ? launch_layouts<true>(p, clusters, stream) : launch_layouts<false>(p, clusters, stream);
 }
 
 }  // namespace gemmlib

@@ -1,9 +1,13 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark
 times (default selector, same problem definitions and seeds).
 
-The oracle recomputes sampled outputs one by one (random entries, corners and
-tile-boundary rows/columns); the int8 workload is also checked on whole rows.
-Guard bands around D must be untouched.
+The 8192^3 fp16 TN GEMM and the 8192^3 int8 GEMM are compared with the oracle
+on the whole output matrix.  The other layouts of the 8192^3 GEMM, the FC layer
+and the square sweep are compared on whole rows at both edges of every
+128-row block and whole columns at both edges of every 64-column block (every
+CTA's rows of every tile, every epilogue chunk's columns, every half-tile unit
+of a tail), plus random entries and corners.  Guard bands around D must be
+untouched.
 """
 import numpy as np
 import pytest
@@ -28,32 +32,13 @@ def _cuda():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("kernel", [G.GEMM_KERNEL_TC, G.GEMM_KERNEL_TC_PAIR], ids=["cta1", "pair"])
-@pytest.mark.parametrize("layout", ["NN", "TT"])
-def test_square_fp16_8192_each_tensor_core_kernel(layout, kernel):
-    """Both tensor-core kernels at the full size (the selector runs the pair kernel)."""
-    p = I.square_fp16_8192(layout)
-    inp = I.generate(p, I.BASE_SEED + 1)
-    dp = H.DeviceProblem(inp)
-    plan = H.make_plan(p, kernel)
-    dp.run(plan)
-    torch.cuda.synchronize()
-    assert plan.device_status() == 0 and plan.last_config()["kernel"] == kernel
-    dp.check_guards()
-    rows, cols = H.sample_entries(p.M, p.N, 600, 7, 256, 256)
-    ref = H.oracle_entries(inp, rows, cols)
-    got = dp.result()[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
-    H.check_close(got, ref, p.d, p.name)
-    plan.close()
-
-
 TC_ANY = (G.GEMM_KERNEL_TC, G.GEMM_KERNEL_TC_PAIR)
 
 
-def _check_sampled(p: I.Problem, seed: int, expect_kernel, extra_rows=()):
+def _run(p: I.Problem, seed: int, expect_kernel, kernel=None):
     inp = I.generate(p, seed)
     dp = H.DeviceProblem(inp)
-    plan = H.make_plan(p)
+    plan = H.make_plan(p, kernel)
     dp.run(plan)
     torch.cuda.synchronize()
     assert plan.device_status() == 0
@@ -61,15 +46,52 @@ def _check_sampled(p: I.Problem, seed: int, expect_kernel, extra_rows=()):
     allowed = expect_kernel if isinstance(expect_kernel, tuple) else (expect_kernel,)
     assert cfg["kernel"] in allowed, cfg
     dp.check_guards()
-    rows, cols = H.sample_entries(p.M, p.N, N_SAMPLES, seed, cfg["bm"] or 128, cfg["bn"] or 128)
-    for r in extra_rows:
-        rows = np.concatenate([rows, np.full(p.N, r, dtype=np.int64)])
-        cols = np.concatenate([cols, np.arange(p.N, dtype=np.int64)])
+    plan.close()
+    return inp, dp, cfg
+
+
+def _check_whole(p: I.Problem, seed: int, expect_kernel):
+    inp, dp, cfg = _run(p, seed, expect_kernel)
+    got = dp.result().cpu()
+    del dp
+    torch.cuda.empty_cache()
+    H.check_close(got, H.oracle_full(inp), p.d, p.name + " (whole matrix)")
+    return cfg
+
+
+def _check_boundaries(p: I.Problem, seed: int, expect_kernel, kernel=None):
+    inp, dp, cfg = _run(p, seed, expect_kernel, kernel)
+    rows, cols = H.boundary_entries(p.M, p.N, 128, 64)
+    r2, c2 = H.sample_entries(p.M, p.N, N_SAMPLES, seed, cfg["bm"] or 128, cfg["bn"] or 128)
+    rows, cols = np.concatenate([rows, r2]), np.concatenate([cols, c2])
     ref = H.oracle_entries(inp, rows, cols)
     got = dp.result()[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
-    H.check_close(got, ref, p.d, p.name)
-    plan.close()
+    H.check_close(got, ref, p.d, p.name + " (block-edge rows and columns)")
     return cfg
+
+
+def test_square_fp16_8192_tn_whole_matrix():
+    cfg = _check_whole(I.square_fp16_8192("TN"), I.BASE_SEED + 1, G.GEMM_KERNEL_TC_PAIR)
+    assert cfg["half_tiles"] > 0          # the tail's half-tile units are inside the checked matrix
+
+
+def test_int8_8192_whole_matrix_exact():
+    _check_whole(I.int8_8192(), I.BASE_SEED + 3, G.GEMM_KERNEL_TC_INT8)
+
+
+@pytest.mark.parametrize("layout", ["NN", "NT", "TT"])
+def test_square_fp16_8192_alpha_beta(layout):
+    _check_boundaries(I.square_fp16_8192(layout), I.BASE_SEED + 1, G.GEMM_KERNEL_TC_PAIR)
+
+
+@pytest.mark.parametrize("layout", ["NN", "TT"])
+def test_square_fp16_8192_single_cta_kernel(layout):
+    """The single-CTA tensor-core kernel at the full size (the selector runs pairs)."""
+    _check_boundaries(I.square_fp16_8192(layout), I.BASE_SEED + 1, G.GEMM_KERNEL_TC, G.GEMM_KERNEL_TC)
+
+
+def test_fc_bf16_bias_relu():
+    _check_boundaries(I.fc_bf16_8192x4096x11008(), I.BASE_SEED + 2, G.GEMM_KERNEL_TC_PAIR)
 
 
 def test_square_fp16_256_full():
@@ -78,27 +100,22 @@ def test_square_fp16_256_full():
     assert cfg["kernel"] in TC_ANY
 
 
-@pytest.mark.parametrize("layout", ["NN", "NT", "TN", "TT"])
-def test_square_fp16_8192_alpha_beta(layout):
-    _check_sampled(I.square_fp16_8192(layout), I.BASE_SEED + 1, G.GEMM_KERNEL_TC_PAIR)
-
-
-def test_fc_bf16_bias_relu():
-    _check_sampled(I.fc_bf16_8192x4096x11008(), I.BASE_SEED + 2, G.GEMM_KERNEL_TC_PAIR)
-
-
-def test_int8_8192_exact():
-    _check_sampled(I.int8_8192(), I.BASE_SEED + 3, G.GEMM_KERNEL_TC_INT8, extra_rows=(0, 8191))
-
-
 def test_sgemm_4096_bias_relu():
-    _check_sampled(I.sgemm_4096_bias_relu(), I.BASE_SEED + 4, G.GEMM_KERNEL_FFMA)
+    _check_boundaries(I.sgemm_4096_bias_relu(), I.BASE_SEED + 4, G.GEMM_KERNEL_FFMA)
 
 
-@pytest.mark.parametrize("n", [512, 1024, 2048, 4096, 16384])
-def test_square_fp16_sweep(n):
-    _check_sampled(I.square_fp16(n), I.BASE_SEED + 5, TC_ANY)
+@pytest.mark.parametrize("n", [512, 1024, 2048, 4096])
+def test_square_fp16_sweep_whole(n):
+    p = I.square_fp16(n)
+    cfg = H.run_and_check_full(p, I.BASE_SEED + 5)
+    assert cfg["kernel"] in TC_ANY
 
 
-def test_skinny_fp16():
-    _check_sampled(I.skinny_fp16_16384x64x16384(), I.BASE_SEED + 6, TC_ANY)
+def test_square_fp16_16384():
+    _check_boundaries(I.square_fp16(16384), I.BASE_SEED + 5, TC_ANY)
+
+
+def test_skinny_fp16_whole():
+    p = I.skinny_fp16_16384x64x16384()
+    cfg = H.run_and_check_full(p, I.BASE_SEED + 6)
+    assert cfg["kernel"] in TC_ANY
