@@ -45,16 +45,21 @@ EXPORTED = ["gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_host"
             "gemm_run_strided_batched", "gemm_run_diag", "gemm_run_complex"]
 
 
+GEMM_XF_A, GEMM_XF_B = 1, 2
+
+
 class gemm_epilogue_t(ctypes.Structure):
     _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int), ("bias_mode", ctypes.c_int),
                 ("act", ctypes.c_int), ("out_dtype", ctypes.c_int), ("c_act", ctypes.c_int),
-                ("out_scale", ctypes.c_float)]
+                ("out_scale", ctypes.c_float), ("load_xf", ctypes.c_uint32),
+                ("a_act", ctypes.c_int), ("a_scale", ctypes.c_float),
+                ("b_act", ctypes.c_int), ("b_scale", ctypes.c_float)]
 
 
 class gemm_config_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kernel", "bm", "bn", "bk", "stages", "cta_group", "split_k", "raster", "grid",
-                 "k_chunk", "tiles", "sk_tiles", "cluster", "half_tiles")]
+                 "k_chunk", "tiles", "sk_tiles", "cluster", "half_tiles", "xf_staged")]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -129,8 +134,17 @@ def _epi_ptr(epi: Optional[gemm_epilogue_t]):
 
 def make_epilogue(out_dtype: int, bias: int = 0, bias_dtype: int = GEMM_F32,
                   bias_mode: int = GEMM_BIAS_NONE, act: int = GEMM_ACT_NONE,
-                  c_act: int = GEMM_ACT_NONE, out_scale: float = 1.0) -> gemm_epilogue_t:
-    return gemm_epilogue_t(bias or None, bias_dtype, bias_mode, act, out_dtype, c_act, out_scale)
+                  c_act: int = GEMM_ACT_NONE, out_scale: float = 1.0,
+                  a_act: int = GEMM_ACT_NONE, a_scale: float = 1.0,
+                  b_act: int = GEMM_ACT_NONE, b_scale: float = 1.0,
+                  load_xf: Optional[int] = None) -> gemm_epilogue_t:
+    """The C struct.  load_xf defaults to the operands whose transform is not
+    the identity (act none, scale 1); pass it to force a transform on or off."""
+    if load_xf is None:
+        load_xf = ((GEMM_XF_A if (a_act != GEMM_ACT_NONE or a_scale != 1.0) else 0) |
+                   (GEMM_XF_B if (b_act != GEMM_ACT_NONE or b_scale != 1.0) else 0))
+    return gemm_epilogue_t(bias or None, bias_dtype, bias_mode, act, out_dtype, c_act, out_scale,
+                           load_xf, a_act, a_scale, b_act, b_scale)
 
 
 # ---- C entry points, same names ----

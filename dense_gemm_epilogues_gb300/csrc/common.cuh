@@ -47,6 +47,25 @@ struct EpiParams {
   int64_t stride_bias;
 };
 
+// ---------------------------------------------------------------------------
+// Operand transforms after load ("Flexible Performant GEMM Kernels on GPUs",
+// section 4.2, "Transforms", Figure 10): every element x of A (of B) enters the
+// product as t(x) = act(scale * x) -- the product rounded to nearest even in
+// fp32, then ReLU (threshold 0) if asked, then, for 16-bit operands, rounded to
+// nearest even back to the operand's type.  t(0) = 0 for every finite scale,
+// so zero fill past the matrix edges stays zero after the transform.
+// ---------------------------------------------------------------------------
+struct LoadXf {
+  int32_t a_on, b_on;         // transform A / B
+  int32_t a_relu, b_relu;
+  float a_scale, b_scale;
+  // Tensor-core kernels, 16-bit operands: how a packed pair is transformed
+  // (XF_F16_PACKED, XF_BF16 or XF_F16_F32, below), and for XF_F16_PACKED the
+  // scale as an fp16 pair.
+  int32_t a_kind, b_kind;
+  uint32_t a_scale2, b_scale2;
+};
+
 // The C, D and bias of one problem of a (strided) batch.
 struct EpiPtrs {
   const void* C;
@@ -99,6 +118,103 @@ __device__ __forceinline__ int8_t requant_s8(int32_t v, float scale) {
   float r = rintf(__fmul_rn(__int2float_rn(v), scale));
   r = fminf(fmaxf(r, -128.0f), 127.0f);
   return (int8_t)__float2int_rn(r);
+}
+
+// t(x) = act(scale * x) in fp32 (the transform of one operand element).
+__device__ __forceinline__ float xf_f32(float x, float scale, int relu) {
+  const float v = __fmul_rn(scale, x);
+  return relu ? fmaxf(v, 0.0f) : v;
+}
+
+// How the tensor-core kernels transform a 32-bit word of two 16-bit elements
+// (a per-operand choice made on the host, LoadXf::a_kind / b_kind):
+//   XF_F16_PACKED  fp16 with a scale that fp16 holds exactly: the product of two
+//                  fp16 values is exact in fp32, so rounding it once to fp16
+//                  (mul.rn.f16x2) is the fp32 product rounded back to fp16;
+//   XF_BF16        bf16: widen each half to fp32 (a shift), multiply in fp32,
+//                  round both to bf16 with one cvt;
+//   XF_F16_F32     fp16 with any other scale: widen, multiply in fp32, round.
+// ReLU is applied to the rounded pair (max with +0): rounding to nearest even
+// is monotone and keeps the sign, so it commutes with the ReLU.
+enum { XF_F16_PACKED = 0, XF_BF16 = 1, XF_F16_F32 = 2 };
+
+template <int KIND>
+__device__ __forceinline__ uint32_t xf_word(uint32_t w, float scale, uint32_t scale2, bool mul, bool relu) {
+  if (mul) {
+    if constexpr (KIND == XF_F16_PACKED) {
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(w) : "r"(w), "r"(scale2));
+    } else if constexpr (KIND == XF_BF16) {
+      const float lo = __fmul_rn(__uint_as_float(w << 16), scale);
+      const float hi = __fmul_rn(__uint_as_float(w & 0xffff0000u), scale);
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w);
+      const float2 f = __half22float2(h);
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(__fmul_rn(f.y, scale)), "f"(__fmul_rn(f.x, scale)));
+    }
+  }
+  if (relu) {
+    if constexpr (KIND == XF_BF16) asm("max.bf16x2 %0, %1, %2;" : "=r"(w) : "r"(w), "r"(0u));
+    else asm("max.f16x2 %0, %1, %2;" : "=r"(w) : "r"(w), "r"(0u));
+  }
+  return w;
+}
+
+// Transform, in place, `bytes` (a multiple of 16) of 16-bit operand elements in
+// shared memory starting at `saddr`, shared by `nthr` threads (this one is `tid`).
+// Elementwise, so the layout of the staged tile (swizzle, K- or MN-major) does
+// not matter.  Eight 16-byte vectors per thread are in flight at a time.
+template <int KIND>
+__device__ __forceinline__ void xf_smem_k(uint32_t saddr, uint32_t bytes, float scale, uint32_t scale2, bool mul,
+                                          bool relu, int tid, int nthr) {
+  constexpr int U = 8;
+  const uint32_t step = (uint32_t)nthr * 16u;
+  uint32_t off = (uint32_t)tid * 16u;
+  for (; off + (U - 1) * step < bytes; off += U * step) {
+    uint32_t w[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[u][0]), "=r"(w[u][1]), "=r"(w[u][2]), "=r"(w[u][3])
+                   : "r"(saddr + off + (uint32_t)u * step));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[u][q] = xf_word<KIND>(w[u][q], scale, scale2, mul, relu);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr + off + (uint32_t)u * step),
+                   "r"(w[u][0]), "r"(w[u][1]), "r"(w[u][2]), "r"(w[u][3])
+                   : "memory");
+    }
+  }
+  for (; off < bytes; off += step) {
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(saddr + off));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = xf_word<KIND>(w[q], scale, scale2, mul, relu);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr + off), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3])
+                 : "memory");
+  }
+}
+
+// The transform of operand A (op = 0) or B (op = 1) of a staged tile region.
+__device__ __forceinline__ void xf_smem(uint32_t saddr, uint32_t bytes, const LoadXf& x, int op, int tid, int nthr) {
+  const int kind = op ? x.b_kind : x.a_kind;
+  const float scale = op ? x.b_scale : x.a_scale;
+  const uint32_t scale2 = op ? x.b_scale2 : x.a_scale2;
+  const bool relu = (op ? x.b_relu : x.a_relu) != 0;
+  const bool mul = scale != 1.0f;
+  if (kind == XF_F16_PACKED) xf_smem_k<XF_F16_PACKED>(saddr, bytes, scale, scale2, mul, relu, tid, nthr);
+  else if (kind == XF_BF16) xf_smem_k<XF_BF16>(saddr, bytes, scale, scale2, mul, relu, tid, nthr);
+  else xf_smem_k<XF_F16_F32>(saddr, bytes, scale, scale2, mul, relu, tid, nthr);
+}
+
+// Make this thread's generic-proxy writes to its CTA's shared memory visible to
+// the async proxy (the tensor cores read the transformed tiles through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async;" ::: "memory");
 }
 
 // Integer epilogue arithmetic wraps modulo 2^32 (done in unsigned to keep it defined).
@@ -415,6 +531,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with acquire semantics at cluster scope: for barriers that threads of
+// the other CTA of a pair arrive on (release.cluster) after writing shared
+// memory that this thread's later tensor-core operations read.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel of the
 // stream (if it was launched as a programmatic dependent) start its prologue on
 // free SMs; wait blocks until every prerequisite grid has completed and its
@@ -438,6 +571,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;   // try_wait itself suspends for a while
+    if (*ctx.abort) return false;
+    if (globaltimer_ns() - t0 > ctx.timeout_ns) {
+      atomicCAS(ctx.err, 0, (int32_t)GEMM_ERR_TIMEOUT);
+      *ctx.abort = 1;
+      __threadfence_block();
+      return false;
+    }
+  }
+}
+
+// mbar_wait with the cluster-scope acquire of mbar_try_wait_cluster.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtx& ctx) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if (*ctx.abort) return false;
     if (globaltimer_ns() - t0 > ctx.timeout_ns) {
       atomicCAS(ctx.err, 0, (int32_t)GEMM_ERR_TIMEOUT);

@@ -108,6 +108,17 @@ gemm_status_t validate(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_l
       if (ab == GEMM_S8 ? epi->bias_dtype != GEMM_S32 : !is_float_out(epi->bias_dtype))
         return GEMM_ERR_INVALID_ARG;
     }
+    // Operand transforms: only the two operand bits, known activations, finite
+    // scales; int8 operands take the activation alone.
+    if (epi->load_xf & ~(GEMM_XF_A | GEMM_XF_B)) return GEMM_ERR_INVALID_ARG;
+    const struct { uint32_t bit; gemm_act_t act; float scale; } ops[2] = {
+        {GEMM_XF_A, epi->a_act, epi->a_scale}, {GEMM_XF_B, epi->b_act, epi->b_scale}};
+    for (const auto& o : ops) {
+      if (!(epi->load_xf & o.bit)) continue;
+      if (o.act != GEMM_ACT_NONE && o.act != GEMM_ACT_RELU) return GEMM_ERR_INVALID_ARG;
+      if (!std::isfinite(o.scale)) return GEMM_ERR_INVALID_ARG;
+      if (ab == GEMM_S8 && o.scale != 1.0f) return GEMM_ERR_UNSUPPORTED;
+    }
   }
   if (ab == GEMM_S8 && (!integral_int32(alpha) || !integral_int32(beta))) return GEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -197,7 +208,9 @@ bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t batch, int pair_clusters
 gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
                             int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                             int sm_count, gemm_kernel_t forced, gemm_config_t* out, int pair_clusters = 0,
-                            int64_t batch = 1) {
+                            int64_t batch = 1, bool xf = false) {
+  // xf: operand transforms are requested; their kernel instances run whole tiles
+  // (no stream-K).
   (void)c;
   gemm_config_t cfg{};
   cfg.split_k = 1;
@@ -266,7 +279,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       int64_t sk_tiles = q >= 1 ? G + r : T;
       if (sk_tiles * KB < 8 * G) sk = false;          // too little K work per pair
       const char* sk_env = std::getenv("GEMM_STREAM_K");
-      sk = sk && sk_env != nullptr && std::atoi(sk_env) != 0;
+      sk = sk && sk_env != nullptr && std::atoi(sk_env) != 0 && !xf;
       if (sk) {
         cfg.sk_tiles = (int32_t)sk_tiles;
         cfg.grid = 2 * (int32_t)G;
@@ -297,7 +310,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
         // (deep K on few tiles) keeps every SM busy with less operand traffic.
         const int64_t KB = (K + TC_BK - 1) / TC_BK;
         auto tiles_of = [&](int w) { return batch * ((M + 127) / 128) * ((N + w - 1) / w); };
-        if (!single_stream_k_pays(tiles_of(bn), KB, sm_count)) {
+        if (!xf && !single_stream_k_pays(tiles_of(bn), KB, sm_count)) {
           for (int cand : {128, 256})
             if (cand > bn && single_stream_k_pays(tiles_of(cand), KB, sm_count)) {
               bn = cand;
@@ -337,6 +350,7 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
           if (v == 0) sk1 = false;
           else if (v == 1) sk1 = T * KB >= sm_count;
         }
+        if (xf) sk1 = false;
         if (sk1) {
           cfg.sk_tiles = (int32_t)T;
           cfg.grid = sm_count;
@@ -480,6 +494,46 @@ EpiParams make_epi(const gemm_plan* plan, double alpha, double beta, const void*
   return e;
 }
 
+// The kernels' view of the operand transforms; an identity transform (no
+// activation, scale 1) is dropped, so it costs nothing.
+// How the tensor-core kernels transform a pair of 16-bit elements: bf16 through
+// fp32; fp16 with a scale that fp16 holds exactly in fp16 arithmetic (the
+// product of two fp16 values is exact in fp32, so one fp16 rounding equals the
+// fp32 product rounded to fp16); any other fp16 scale through fp32.
+int xf_kind(gemm_dtype_t ab, float scale, uint32_t* scale2) {
+  *scale2 = 0;
+  if (ab == GEMM_BF16) return XF_BF16;
+  const __half h = __float2half_rn(scale);
+  if (__half2float(h) != scale) return XF_F16_F32;
+  const uint16_t bits = *reinterpret_cast<const uint16_t*>(&h);
+  *scale2 = (uint32_t)bits | ((uint32_t)bits << 16);
+  return XF_F16_PACKED;
+}
+
+LoadXf make_xf(gemm_dtype_t ab, const gemm_epilogue_t* epi) {
+  LoadXf x{};
+  x.a_scale = x.b_scale = 1.0f;
+  if (!epi) return x;
+  if ((epi->load_xf & GEMM_XF_A) && (epi->a_act == GEMM_ACT_RELU || epi->a_scale != 1.0f)) {
+    x.a_on = 1;
+    x.a_relu = epi->a_act == GEMM_ACT_RELU ? 1 : 0;
+    x.a_scale = epi->a_scale;
+  }
+  if ((epi->load_xf & GEMM_XF_B) && (epi->b_act == GEMM_ACT_RELU || epi->b_scale != 1.0f)) {
+    x.b_on = 1;
+    x.b_relu = epi->b_act == GEMM_ACT_RELU ? 1 : 0;
+    x.b_scale = epi->b_scale;
+  }
+  x.a_kind = xf_kind(ab, x.a_scale, &x.a_scale2);
+  x.b_kind = xf_kind(ab, x.b_scale, &x.b_scale2);
+  return x;
+}
+
+bool xf_any(const gemm_epilogue_t* epi) {
+  const LoadXf x = make_xf(GEMM_F16, epi);
+  return x.a_on || x.b_on;
+}
+
 gemm_status_t ensure_ws(gemm_plan* plan, size_t bytes, cudaStream_t stream) {
   if (plan->ws_bytes >= bytes) return GEMM_OK;
   if (plan->ws) {
@@ -499,7 +553,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
                                 int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                                 int64_t ldb, CUtensorMapDataType dt, bool bf16, const EpiParams& epi,
-                                int chunk_kb, cudaStream_t stream, const Batch& bt = Batch()) {
+                                int chunk_kb, cudaStream_t stream, const Batch& bt = Batch(),
+                                const LoadXf& xf = LoadXf{}) {
   TcParams tp;
   std::memset(&tp, 0, sizeof(tp));
   const int bn = cfg.bn;
@@ -530,6 +585,7 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   tp.b_mn_major = b_mn ? 1 : 0;
   tp.idesc = make_idesc(bf16, bn, a_mn, b_mn);
   tp.chunk_kb = chunk_kb;
+  tp.xf = xf;
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
@@ -560,7 +616,7 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
 gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_layout_t la, gemm_layout_t lb,
                                   int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                                   int64_t ldb, bool bf16, const EpiParams& epi, cudaStream_t stream,
-                                  int chunk_kb = 0, const Batch& bt = Batch()) {
+                                  int chunk_kb = 0, const Batch& bt = Batch(), const LoadXf& xf = LoadXf{}) {
   TcParams tp;
   std::memset(&tp, 0, sizeof(tp));
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -601,6 +657,7 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   tp.idesc = make_idesc(bf16, 256, a_mn, b_mn, 256);
   tp.idesc_half = make_idesc(bf16, 128, a_mn, b_mn, 256);
   tp.chunk_kb = chunk_kb;
+  tp.xf = xf;
   tp.epi = epi;
   tp.err = plan->d_err;
   tp.timeout_ns = plan->timeout_ns;
@@ -629,11 +686,67 @@ gemm_status_t launch_pair_problem(gemm_plan* plan, const gemm_config_t& cfg, gem
   return launch_tc_pair(tp, cfg.grid / 2, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Operand transforms of 16-bit operands on the tensor-core kernels: which
+// operands are transformed by a staging pass into plan scratch before the GEMM
+// (GEMM_XF_A / GEMM_XF_B bits) rather than in place on the staged tiles inside
+// the kernel.  Inside the kernel every tile that reads an element transforms it
+// again -- an A element once per tile column, a B element once per tile row --
+// and each pass costs shared-memory bandwidth the MMAs need; measured on an
+// 8192^3 fp16 GEMM it took the kernel from 0.63 ms to 1.3-1.6 ms, where a
+// staging pass costs one read and one write of the operand at HBM speed (~40 us
+// for 134 MB).  An operand that only one tile reads (a skinny GEMM's A) is
+// transformed inside the kernel (once, and overlapped with its streaming), and
+// so is one under 4 MiB, where the extra launch would dominate.
+// GEMM_XF_STAGE=0 / 1: never / always stage.
+uint32_t xf_stage_mask(gemm_dtype_t ab, const LoadXf& x, const gemm_config_t& cfg, gemm_layout_t la,
+                       gemm_layout_t lb, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, const Batch& bt) {
+  if (!is_f16ish(ab) || (cfg.kernel != GEMM_KERNEL_TC && cfg.kernel != GEMM_KERNEL_TC_PAIR)) return 0;
+  const uint32_t want = (x.a_on ? GEMM_XF_A : 0u) | (x.b_on ? GEMM_XF_B : 0u);
+  if (const char* env = std::getenv("GEMM_XF_STAGE")) {
+    const int v = std::atoi(env);
+    if (v == 0) return 0;
+    if (v == 1) return want;
+  }
+  const int64_t tiles_m = (M + cfg.bm - 1) / cfg.bm, tiles_n = (N + cfg.bn - 1) / cfg.bn;
+  const int64_t na = (bt.count > 1 && bt.sa != 0) ? bt.count : 1;
+  const int64_t nb = (bt.count > 1 && bt.sb != 0) ? bt.count : 1;
+  const int64_t a_bytes = ((na - 1) * bt.sa + storage_elems(la, M, K, lda)) * 2;
+  const int64_t b_bytes = ((nb - 1) * bt.sb + storage_elems(lb, K, N, ldb)) * 2;
+  constexpr int64_t kMinStage = 4ll << 20;
+  uint32_t m = 0;
+  if (x.a_on && tiles_n >= 2 && a_bytes >= kMinStage) m |= GEMM_XF_A;
+  if (x.b_on && tiles_m >= 2 && b_bytes >= kMinStage) m |= GEMM_XF_B;
+  return m;
+}
+
+// The selector's configuration for a request with operand transforms `x`: the
+// kernel and tile first (as without transforms), then which operands are
+// staged; if some transform stays inside the kernel the configuration is
+// chosen again for the transform instances (whole tiles, no stream-K).
+gemm_status_t select_with_transforms(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gemm_layout_t lb, int64_t M,
+                                     int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                                     int sm_count, gemm_kernel_t forced, int pair_clusters, const Batch& bt,
+                                     const LoadXf& x, gemm_config_t* cfg, LoadXf* in_kernel) {
+  gemm_status_t s = select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, forced, cfg, pair_clusters,
+                                  bt.count, false);
+  *in_kernel = x;
+  if (s != GEMM_OK || !(x.a_on || x.b_on)) return s;
+  const uint32_t staged = xf_stage_mask(ab, x, *cfg, la, lb, M, N, K, lda, ldb, bt);
+  if (staged & GEMM_XF_A) in_kernel->a_on = 0;
+  if (staged & GEMM_XF_B) in_kernel->b_on = 0;
+  if (in_kernel->a_on || in_kernel->b_on) {
+    s = select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, forced, cfg, pair_clusters, bt.count, true);
+    if (s != GEMM_OK) return s;
+  }
+  cfg->xf_staged = (int32_t)staged;
+  return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int gemm_abi_version(void) { return 108; }
+int gemm_abi_version(void) { return 109; }
 
 const char* gemm_status_string(gemm_status_t s) {
   switch (s) {
@@ -663,7 +776,9 @@ gemm_status_t gemm_select(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, gem
   gemm_status_t s = validate(ab, c, la, lb, M, N, K, alpha_probe, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
   // Host-only: a device whose SMs all pair up.
-  return select_config(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, out, sm_count / 2);
+  LoadXf in_kernel{};
+  return select_with_transforms(ab, c, la, lb, M, N, K, A, lda, B, ldb, sm_count, GEMM_KERNEL_AUTO, sm_count / 2,
+                                Batch(), make_xf(ab, epi), out, &in_kernel);
 }
 
 gemm_status_t gemm_plan_create(gemm_plan_t* plan, gemm_dtype_t ab, gemm_dtype_t c, int device) {
@@ -759,8 +874,10 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
                        const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
                        gemm_stream_t stream_, const Batch& bt) {
   gemm_config_t cfg{};
-  gemm_status_t s = select_config(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count,
-                                  plan->forced, &cfg, plan->pair_clusters, bt.count);
+  const LoadXf xf_req = make_xf(plan->ab, epi);
+  LoadXf xf{};
+  gemm_status_t s = select_with_transforms(plan->ab, plan->c, la, lb, M, N, K, A, lda, B, ldb, plan->sm_count,
+                                           plan->forced, plan->pair_clusters, bt, xf_req, &cfg, &xf);
   if (s != GEMM_OK) return s;
   if (cfg.kernel == GEMM_KERNEL_NONE) {
     plan->last = cfg;
@@ -785,15 +902,48 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
     }
   }
 
+  // Staged operand transforms: each transformed operand (every problem of a
+  // batch, a shared one once) is written to plan scratch with its own layout,
+  // leading dimension and batch stride, and the GEMM reads the copy.
+  if (cfg.xf_staged != 0) {
+    const int64_t na = (bt.count > 1 && bt.sa != 0) ? bt.count : 1;
+    const int64_t nb = (bt.count > 1 && bt.sb != 0) ? bt.count : 1;
+    const int64_t a_el = (na - 1) * bt.sa + storage_elems(la, M, K, lda);
+    const int64_t b_el = (nb - 1) * bt.sb + storage_elems(lb, K, N, ldb);
+    const size_t a_bytes = (cfg.xf_staged & GEMM_XF_A) ? align_up((size_t)a_el * 2, 256) : 0;
+    const size_t b_bytes = (cfg.xf_staged & GEMM_XF_B) ? (size_t)b_el * 2 : 0;
+    s = ensure_ws(plan, a_bytes + b_bytes, stream);
+    if (s != GEMM_OK) return s;
+    cudaError_t ce = cudaSuccess;
+    if (cfg.xf_staged & GEMM_XF_A) {
+      uint16_t* As = static_cast<uint16_t*>(plan->ws);
+      const uint16_t* Ao = static_cast<const uint16_t*>(A);
+      for (int64_t z = 0; z < na && ce == cudaSuccess; ++z)
+        ce = la == GEMM_OP_T ? launch_xf_stage(Ao + z * bt.sa, As + z * bt.sa, M, K, lda, xf_req, 0, stream)
+                             : launch_xf_stage(Ao + z * bt.sa, As + z * bt.sa, K, M, lda, xf_req, 0, stream);
+      A = As;
+    }
+    if (cfg.xf_staged & GEMM_XF_B) {
+      uint16_t* Bs = reinterpret_cast<uint16_t*>(static_cast<char*>(plan->ws) + a_bytes);
+      const uint16_t* Bo = static_cast<const uint16_t*>(B);
+      for (int64_t z = 0; z < nb && ce == cudaSuccess; ++z)
+        ce = lb == GEMM_OP_N ? launch_xf_stage(Bo + z * bt.sb, Bs + z * bt.sb, N, K, ldb, xf_req, 1, stream)
+                             : launch_xf_stage(Bo + z * bt.sb, Bs + z * bt.sb, K, N, ldb, xf_req, 1, stream);
+      B = Bs;
+    }
+    if (ce != cudaSuccess) return GEMM_ERR_CUDA;
+  }
+
   switch (cfg.kernel) {
     case GEMM_KERNEL_TC_PAIR:
-      s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb, plan->ab == GEMM_BF16, e, stream, 0, bt);
+      s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb, plan->ab == GEMM_BF16, e, stream, 0, bt,
+                              xf);
       break;
     case GEMM_KERNEL_TC: {
       const bool bf16 = plan->ab == GEMM_BF16;
       s = launch_tc_problem(plan, cfg, la, lb, M, N, K, A, lda, B, ldb,
                             bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bf16,
-                            e, 0, stream, bt);
+                            e, 0, stream, bt, xf);
       break;
     }
     case GEMM_KERNEL_TC_INT8: {
@@ -811,12 +961,13 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       const int8_t* A8 = static_cast<const int8_t*>(A);
       const int8_t* B8 = static_cast<const int8_t*>(B);
       cudaError_t ce = cudaSuccess;
+      // The int8 operand transform (ReLU) is applied as the operands are staged.
       for (int64_t z = 0; z < na && ce == cudaSuccess; ++z)
-        ce = la == GEMM_OP_T ? launch_s8_to_f16(A8 + z * bt.sa, A16 + z * bt.sa, M, K, lda, stream)
-                             : launch_s8_to_f16(A8 + z * bt.sa, A16 + z * bt.sa, K, M, lda, stream);
+        ce = la == GEMM_OP_T ? launch_s8_to_f16(A8 + z * bt.sa, A16 + z * bt.sa, M, K, lda, stream, xf.a_relu)
+                             : launch_s8_to_f16(A8 + z * bt.sa, A16 + z * bt.sa, K, M, lda, stream, xf.a_relu);
       for (int64_t z = 0; z < nb && ce == cudaSuccess; ++z)
-        ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8 + z * bt.sb, B16 + z * bt.sb, N, K, ldb, stream)
-                             : launch_s8_to_f16(B8 + z * bt.sb, B16 + z * bt.sb, K, N, ldb, stream);
+        ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8 + z * bt.sb, B16 + z * bt.sb, N, K, ldb, stream, xf.b_relu)
+                             : launch_s8_to_f16(B8 + z * bt.sb, B16 + z * bt.sb, K, N, ldb, stream, xf.b_relu);
       if (ce != cudaSuccess) { s = GEMM_ERR_CUDA; break; }
       if (cfg.cta_group == 2)
         s = launch_pair_problem(plan, cfg, la, lb, M, N, K, A16, lda, B16, ldb, false, e, stream,
@@ -837,6 +988,7 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       fp.K = (int32_t)K;
       fp.stride_a = bt.sa;
       fp.stride_b = bt.sb;
+      fp.xf = xf;
       fp.epi = e;
       s = launch_ffma(fp, la == GEMM_OP_T, lb == GEMM_OP_T, (int)bt.count, stream) == cudaSuccess ? GEMM_OK
                                                                                      : GEMM_ERR_CUDA;
@@ -856,6 +1008,7 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       sp.K = K;
       sp.stride_a = bt.sa;
       sp.stride_b = bt.sb;
+      sp.xf = xf;
       sp.epi = e;
       s = launch_simt(sp, (int)bt.count, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
       break;
@@ -949,6 +1102,7 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx
            : validate(plan->ab, plan->c, lx, GEMM_OP_N, M, N, N, alpha, X, ldx, diag, std::max<int64_t>(1, N),
                       beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
+  if (epi && epi->load_xf != 0) return GEMM_ERR_UNSUPPORTED;   // no operand transforms on this path
   gemm_config_t cfg{};
   cfg.split_k = 1;
   cfg.cta_group = 1;
@@ -998,6 +1152,7 @@ gemm_status_t gemm_run_complex(gemm_plan_t plan, gemm_unit_t unit, gemm_layout_t
   if (s != GEMM_OK) return s;
   if (plan->ab == GEMM_S8) return GEMM_ERR_UNSUPPORTED;
   if (epi && epi->bias_mode == GEMM_BIAS_ROW) return GEMM_ERR_UNSUPPORTED;
+  if (epi && epi->load_xf != 0) return GEMM_ERR_UNSUPPORTED;   // no operand transforms on this path
   if (2 * N > kMaxDim || 2 * K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) {
     gemm_config_t none{};
@@ -1273,11 +1428,13 @@ extern "C" gemm_status_t gemm_run_s8_noalloc(gemm_layout_t la, gemm_layout_t lb,
   __half* B16 = reinterpret_cast<__half*>(static_cast<char*>(nd->scratch) + a_bytes);
   const int8_t* A8 = static_cast<const int8_t*>(A);
   const int8_t* B8 = static_cast<const int8_t*>(B);
-  cudaError_t ce = la == GEMM_OP_T ? launch_s8_to_f16(A8, A16, M, K, lda, stream)
-                                   : launch_s8_to_f16(A8, A16, K, M, lda, stream);
+  // The int8 operand transform (ReLU), if any, is applied as the operands are staged.
+  const LoadXf xf = make_xf(GEMM_S8, epi);
+  cudaError_t ce = la == GEMM_OP_T ? launch_s8_to_f16(A8, A16, M, K, lda, stream, xf.a_relu)
+                                   : launch_s8_to_f16(A8, A16, K, M, lda, stream, xf.a_relu);
   if (ce == cudaSuccess)
-    ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8, B16, N, K, ldb, stream)
-                         : launch_s8_to_f16(B8, B16, K, N, ldb, stream);
+    ce = lb == GEMM_OP_N ? launch_s8_to_f16(B8, B16, N, K, ldb, stream, xf.b_relu)
+                         : launch_s8_to_f16(B8, B16, K, N, ldb, stream, xf.b_relu);
   if (ce != cudaSuccess) return GEMM_ERR_CUDA;
   return launch_tc_problem(&local, cfg, la, lb, M, N, K, A16, lda, B16, ldb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                            false, e, cfg.k_chunk / TC_BK, stream);

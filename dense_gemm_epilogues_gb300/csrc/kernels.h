@@ -29,6 +29,7 @@ struct TcParams {
   uint32_t idesc_half;    // CTA-pair kernel: the same for half-tile units (N = 128)
   int32_t half_first_tile;  // CTA-pair kernel: tiles from here on run as two column halves (num_tiles: none)
   int32_t chunk_kb;       // > 0: exact integer mode, K blocks per fp32 chunk
+  LoadXf xf;              // transforms of the staged A / B tiles (launched as a separate kernel instance)
   EpiParams epi;
   int32_t* err;
   uint64_t timeout_ns;
@@ -69,6 +70,7 @@ struct FfmaParams {
   int64_t lda, ldb;
   int64_t stride_a, stride_b;   // batched problems (elements); one problem per grid row
   int32_t M, N, K;
+  LoadXf xf;                    // transforms of A / B elements as they are loaded
   EpiParams epi;
 };
 // K slice per shared-memory buffer: 8 (measured 5 % faster than 16 at 4096^3 and
@@ -88,6 +90,7 @@ struct SimtParams {
   int32_t a_row_major, b_row_major;
   int64_t M, N, K;
   int64_t stride_a, stride_b;   // batched problems (elements); one problem per grid row
+  LoadXf xf;                    // transforms of A / B elements as they are loaded
   EpiParams epi;
 };
 cudaError_t launch_simt(const SimtParams& p, int batch, cudaStream_t stream);
@@ -121,9 +124,15 @@ cudaError_t launch_pair_stage_b(const void* B, int64_t ldb, int b_row_major, int
 cudaError_t launch_pair_stage_a(const void* A, int64_t lda, int a_row_major, int64_t M, int64_t K, int elem_bytes,
                                 void* out, int64_t lds, cudaStream_t stream);
 
+// Transform staging of a 16-bit operand: dst[r*ld + c] = t(src[r*ld + c]) for
+// r < outer, c < inner, with the operand transform of op (0: A, 1: B) of x.
+cudaError_t launch_xf_stage(const void* src, void* dst, int64_t outer, int64_t inner, int64_t ld, const LoadXf& x,
+                            int op, cudaStream_t stream);
+
 // int8 -> fp16 staging copy of a strided matrix: dst[r*ld + c] = src[r*ld + c]
-// for r < outer, c < inner.
+// for r < outer, c < inner; relu != 0 stages max(src, 0) (the operand transform
+// of an int8 problem).
 cudaError_t launch_s8_to_f16(const int8_t* src, __half* dst, int64_t outer, int64_t inner, int64_t ld,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int relu = 0);
 
 }  // namespace gemmlib

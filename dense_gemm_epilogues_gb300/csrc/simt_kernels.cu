@@ -36,6 +36,8 @@ struct SliceLoader {
   int64_t ld;
   int64_t extent_mn;   // M (for A) or N (for B)
   int64_t K;
+  int xf_on, xf_relu;  // operand transform t(x) = act(scale * x) after the load
+  float xf_scale;
 
   __device__ __forceinline__ void load(int64_t mn0, int64_t k0, int tid, float (&v)[SG_NV][4]) const {
 #pragma unroll
@@ -62,6 +64,10 @@ struct SliceLoader {
 #pragma unroll
           for (int j = 0; j < 4; ++j) v[g][j] = (k < K && c + j < extent_mn) ? src[j] : 0.0f;
         }
+      }
+      if (xf_on) {   // zero fill stays zero: t(0) = 0
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[g][j] = xf_f32(v[g][j], xf_scale, xf_relu);
       }
     }
   }
@@ -116,8 +122,8 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
   const int64_t n0 = (int64_t)(blockIdx.x % tiles_n) * FFMA_BN;
   const int64_t bz = blockIdx.y;                      // problem of the batch
 
-  const SliceLoader<A_KMAJOR> la{p.A + bz * p.stride_a, p.lda, p.M, p.K};
-  const SliceLoader<B_KMAJOR> lb{p.B + bz * p.stride_b, p.ldb, p.N, p.K};
+  const SliceLoader<A_KMAJOR> la{p.A + bz * p.stride_a, p.lda, p.M, p.K, p.xf.a_on, p.xf.a_relu, p.xf.a_scale};
+  const SliceLoader<B_KMAJOR> lb{p.B + bz * p.stride_b, p.ldb, p.N, p.K, p.xf.b_on, p.xf.b_relu, p.xf.b_scale};
 
 #if GEMM_FFMA_PAIRED
   uint64_t acc2[8][4];   // acc2[i][q] holds columns 2q and 2q+1 of row i
@@ -259,6 +265,15 @@ __device__ __forceinline__ int64_t b_index(const SimtParams& p, int64_t k, int64
   return p.b_row_major ? k * p.ldb + j : k + j * p.ldb;
 }
 
+// The operand transform of one element of a floating problem: t(x) =
+// act(scale * x) in fp32, rounded back to the operand's type for 16-bit operands.
+__device__ __forceinline__ float xf_elem(float x, int dt, float scale, int relu) {
+  const float v = xf_f32(x, scale, relu);
+  if (dt == GEMM_F16) return __half2float(__float2half_rn(v));
+  if (dt == GEMM_BF16) return __bfloat162float(__float2bfloat16_rn(v));
+  return v;
+}
+
 template <bool IS_INT>
 __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
   using Acc = typename std::conditional<IS_INT, int32_t, float>::type;
@@ -278,15 +293,25 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
       const int64_t ai = bm * GT + ty, ak = k0 + tx;
       Acc v = 0;
       if (ai < p.M && ak < p.K) {
-        if constexpr (IS_INT) v = load_as_int(Ab, p.ab_dtype, a_index(p, ai, ak));
-        else v = load_as_float(Ab, p.ab_dtype, a_index(p, ai, ak));
+        if constexpr (IS_INT) {
+          v = load_as_int(Ab, p.ab_dtype, a_index(p, ai, ak));
+          if (p.xf.a_on && p.xf.a_relu && v < 0) v = 0;   // int8: the activation only
+        } else {
+          v = load_as_float(Ab, p.ab_dtype, a_index(p, ai, ak));
+          if (p.xf.a_on) v = xf_elem(v, p.ab_dtype, p.xf.a_scale, p.xf.a_relu);
+        }
       }
       As[ty][tx] = v;
       const int64_t bk = k0 + ty, bj = bn * GT + tx;
       Acc w = 0;
       if (bk < p.K && bj < p.N) {
-        if constexpr (IS_INT) w = load_as_int(Bb, p.ab_dtype, b_index(p, bk, bj));
-        else w = load_as_float(Bb, p.ab_dtype, b_index(p, bk, bj));
+        if constexpr (IS_INT) {
+          w = load_as_int(Bb, p.ab_dtype, b_index(p, bk, bj));
+          if (p.xf.b_on && p.xf.b_relu && w < 0) w = 0;
+        } else {
+          w = load_as_float(Bb, p.ab_dtype, b_index(p, bk, bj));
+          if (p.xf.b_on) w = xf_elem(w, p.ab_dtype, p.xf.b_scale, p.xf.b_relu);
+        }
       }
       Bs[ty][tx] = w;
     }
@@ -331,8 +356,11 @@ __global__ void __launch_bounds__(GT* GT) simt_gemm_kernel(const SimtParams p) {
 
 // One thread converts 16 consecutive elements of a row (vector path when the
 // row start and leading dimension keep 16-byte alignment), grid-stride.
+// RELU: the int8 operand transform (the activation) is applied as it is staged.
+template <bool RELU>
 __global__ void s8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restrict__ dst, int64_t outer,
                                  int64_t inner, int64_t ld, int vec) {
+  auto cv = [](int8_t x) { return __int2half_rn(RELU && x < 0 ? 0 : (int)x); };
   const int64_t groups_per_row = (inner + 15) / 16;
   const int64_t total = outer * groups_per_row;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -347,7 +375,7 @@ __global__ void s8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restr
       uint32_t out[8];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        __half2 v = __halves2half2(__int2half_rn(b[2 * h]), __int2half_rn(b[2 * h + 1]));
+        __half2 v = __halves2half2(cv(b[2 * h]), cv(b[2 * h + 1]));
         out[h] = *reinterpret_cast<uint32_t*>(&v);
       }
       // One 32-byte store (d is 32-byte aligned on this path): each lane writes a
@@ -357,12 +385,70 @@ __global__ void s8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restr
                    "r"(out[2]), "r"(out[3]), "r"(out[4]), "r"(out[5]), "r"(out[6]), "r"(out[7])
                    : "memory");
     } else {
-      for (int j = 0; j < 16 && c + j < inner; ++j) d[j] = __int2half_rn(s[j]);
+      for (int j = 0; j < 16 && c + j < inner; ++j) d[j] = cv(s[j]);
+    }
+  }
+}
+
+// ========================== operand transform staging ==========================
+
+// One thread transforms 8 consecutive 16-bit elements of a row (one 16-byte
+// vector when the row start and leading dimension keep 16-byte alignment),
+// grid-stride; consecutive threads cover consecutive vectors of a row, so every
+// warp store writes whole 32-byte sectors.
+template <int KIND>
+__global__ void xf_stage_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int64_t outer,
+                                int64_t inner, int64_t ld, int vec, float scale, uint32_t scale2, int relu) {
+  const int64_t groups_per_row = (inner + 7) / 8;
+  const int64_t total = outer * groups_per_row;
+  const bool mul = scale != 1.0f;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = g / groups_per_row;
+    const int64_t c = (g - r * groups_per_row) * 8;
+    const uint16_t* s = src + r * ld + c;
+    uint16_t* d = dst + r * ld + c;
+    if (vec && c + 8 <= inner) {
+      uint4 w = __ldcs(reinterpret_cast<const uint4*>(s));
+      w.x = xf_word<KIND>(w.x, scale, scale2, mul, relu != 0);
+      w.y = xf_word<KIND>(w.y, scale, scale2, mul, relu != 0);
+      w.z = xf_word<KIND>(w.z, scale, scale2, mul, relu != 0);
+      w.w = xf_word<KIND>(w.w, scale, scale2, mul, relu != 0);
+      *reinterpret_cast<uint4*>(d) = w;
+    } else {
+      // Ragged row end: one element at a time (the other half of the pair is a copy of it).
+      for (int j = 0; j < 8 && c + j < inner; ++j) {
+        const uint32_t w = (uint32_t)s[j] | ((uint32_t)s[j] << 16);
+        d[j] = (uint16_t)(xf_word<KIND>(w, scale, scale2, mul, relu != 0) & 0xffffu);
+      }
     }
   }
 }
 
 }  // namespace
+
+cudaError_t launch_xf_stage(const void* src, void* dst, int64_t outer, int64_t inner, int64_t ld, const LoadXf& x,
+                            int op, cudaStream_t stream) {
+  if (outer <= 0 || inner <= 0) return cudaSuccess;
+  const int vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0 &&
+                   (ld % 8) == 0) ? 1 : 0;
+  const int64_t total = outer * ((inner + 7) / 8);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  const int kind = op ? x.b_kind : x.a_kind;
+  const float scale = op ? x.b_scale : x.a_scale;
+  const uint32_t scale2 = op ? x.b_scale2 : x.a_scale2;
+  const int relu = op ? x.b_relu : x.a_relu;
+  const uint16_t* s = static_cast<const uint16_t*>(src);
+  uint16_t* d = static_cast<uint16_t*>(dst);
+  if (kind == XF_F16_PACKED)
+    xf_stage_kernel<XF_F16_PACKED><<<(unsigned)blocks, 256, 0, stream>>>(s, d, outer, inner, ld, vec, scale, scale2, relu);
+  else if (kind == XF_BF16)
+    xf_stage_kernel<XF_BF16><<<(unsigned)blocks, 256, 0, stream>>>(s, d, outer, inner, ld, vec, scale, scale2, relu);
+  else
+    xf_stage_kernel<XF_F16_F32><<<(unsigned)blocks, 256, 0, stream>>>(s, d, outer, inner, ld, vec, scale, scale2, relu);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, int batch, cudaStream_t stream) {
   const int64_t tiles = ((p.N + FFMA_BN - 1) / FFMA_BN) * ((p.M + FFMA_BM - 1) / FFMA_BM);
@@ -388,14 +474,15 @@ cudaError_t launch_simt(const SimtParams& p, int batch, cudaStream_t stream) {
 }
 
 cudaError_t launch_s8_to_f16(const int8_t* src, __half* dst, int64_t outer, int64_t inner, int64_t ld,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int relu) {
   if (outer <= 0 || inner <= 0) return cudaSuccess;
   const int vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0 &&
                    (ld % 16) == 0) ? 1 : 0;
   const int64_t total = outer * ((inner + 15) / 16);
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  s8_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, dst, outer, inner, ld, vec);
+  if (relu) s8_to_f16_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(src, dst, outer, inner, ld, vec);
+  else s8_to_f16_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(src, dst, outer, inner, ld, vec);
   return cudaGetLastError();
 }
 

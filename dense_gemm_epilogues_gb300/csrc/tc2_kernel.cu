@@ -23,6 +23,12 @@
 // epilogue warps per CTA -- two per tensor-memory lane quarter, one per half of
 // the 256 columns -- convert each finished chunk to int32 and add it into 128
 // registers per thread, then apply the integer epilogue after the last chunk.
+// Operand transforms (a separate instance, XF): four more warps per CTA apply
+// t(x) = act(scale * x) in place to the CTA's staged A and/or B tiles of each
+// stage.  Then each CTA's TMA loads complete on its own full barrier, the
+// transform warps of both CTAs wait there, transform, fence the async proxy and
+// arrive on the leader's stage-transformed barrier, which is what the MMA
+// thread waits for instead of the full barrier.
 // Every TMA load brings one CTA's own operand data into that CTA's shared
 // memory; no load is delivered to more than one CTA.
 // Every mbarrier wait is bounded, as in tc_kernel.cu.
@@ -50,16 +56,18 @@ constexpr int PAIR_ACC_BUFS = 2;                        // 2 x 256 fp32 columns 
 #define GEMM_PAIR_STAGES (6 / GEMM_PAIR_SLABS)
 #endif
 constexpr int PAIR_STAGES = GEMM_PAIR_STAGES;
-constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
+constexpr int PAIR_NUM_BARS = 3 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
 constexpr int PAIR_OUT_STAGE_BYTES = 4 * 4096;   // a 32 x 32 output turn-around buffer per floating epilogue warp
 constexpr size_t PAIR_SMEM =
     1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_OUT_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16;
 
-// Producer warp, MMA warp, then 4 epilogue warps (floating) or 8 (exact integer).
-template <bool INT_MODE>
+// Producer warp, MMA warp, then 4 epilogue warps (floating) or 8 (exact integer),
+// then (operand transforms) 4 transform warps.
+template <bool INT_MODE, bool XF>
 struct PairThreads {
   static constexpr int EPI_WARPS = INT_MODE ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int XF_WARPS = XF ? 4 : 0;
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + XF_WARPS);
 };
 constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int MN_BOX = 64;   // MN extent of one TMA box of an MN-major operand (128 bytes)
@@ -95,10 +103,12 @@ __device__ __forceinline__ bool warp_wait_pair(uint32_t bar, uint32_t parity, co
 
 // One CTA pair per cluster of two.  A_MN / B_MN: the operand is stored
 // MN-contiguous (A column-major, B row-major) rather than K-contiguous.
-template <bool INT_MODE, bool A_MN, bool B_MN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE>::THREADS, 1)
+template <bool INT_MODE, bool A_MN, bool B_MN, bool XF>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE, XF>::THREADS, 1)
     tc_pair_gemm_kernel(const __grid_constant__ TcParams p) {
-  constexpr int EPI_WARPS = PairThreads<INT_MODE>::EPI_WARPS;
+  static_assert(!(XF && INT_MODE), "int8 operands are transformed in their staging pass");
+  constexpr int EPI_WARPS = PairThreads<INT_MODE, XF>::EPI_WARPS;
+  constexpr int XF_WARPS = PairThreads<INT_MODE, XF>::XF_WARPS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;   // same offset in both CTAs
@@ -115,6 +125,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
   auto tempty_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + PAIR_ACC_BUFS + b); };
   const uint32_t teardown_bar = bar0 + 8u * (uint32_t)(2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
   const uint32_t sk_bar = teardown_bar + 8u;   // epilogue warps: stream-K partial written
+  // Operand transforms: stage transformed in both CTAs (the leader's barrier counts).
+  auto xf_bar = [&](int s) { return sk_bar + 8u * (uint32_t)(1 + s); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -135,6 +147,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
     }
     mbar_init(teardown_bar, 1);
     mbar_init(sk_bar, EPI_WARPS);
+    if constexpr (XF)
+      for (int s = 0; s < PAIR_STAGES; ++s) mbar_init(xf_bar(s), 2 * XF_WARPS);   // transform warps of both CTAs
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -186,8 +200,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           // whole stage (zero-filled past K); a K-major one in one box per K block.
           const uint32_t a_bytes = (uint32_t)(A_MN ? PAIR_SLABS : nsl) * (uint32_t)PAIR_A_BYTES;
           const uint32_t b_bytes = (uint32_t)(B_MN ? PAIR_SLABS : nsl) * b_slab_bytes;
-          if (leader) mbar_expect_tx(fb_local, 2u * (a_bytes + b_bytes));
-          const uint32_t fb = leader ? fb_local : mapa_shared(fb_local, pair_leader);
+          // With operand transforms each CTA's copies complete on its own full
+          // barrier (its transform warps wait there); otherwise both CTAs' copies
+          // complete on the leader's.
+          if (XF) mbar_expect_tx(fb_local, a_bytes + b_bytes);
+          else if (leader) mbar_expect_tx(fb_local, 2u * (a_bytes + b_bytes));
+          const uint32_t fb = (XF || leader) ? fb_local : mapa_shared(fb_local, pair_leader);
           const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
           const uint32_t sb = sa + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES);
           const int k0 = kb * TC_BK;
@@ -216,7 +234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       }
       // The leader's full barriers count both CTAs' bytes: once its drains pass,
       // every copy of the pair has landed (the peer waits at the final cluster barrier).
-      if (leader) {
+      // With operand transforms every CTA's barriers count its own copies.
+      if (leader || XF) {
         for (int s = 0; s < PAIR_STAGES; ++s)
           if (issued & (1u << s)) drain_wait_pair(full_bar(s), (last_parity >> s) & 1u, p.timeout_ns);
       } else if (!ok) {
@@ -248,7 +267,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           const int kb_end = INT_MODE ? min(kb1, kb_begin + kb_per_unit) : kb1;
           for (int kb = kb_begin; kb < kb_end; kb += PAIR_SLABS) {
             const int nsl = kb_end - kb < PAIR_SLABS ? kb_end - kb : PAIR_SLABS;
-            if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
+            const bool landed = XF ? mbar_wait_cluster(xf_bar(stage), phase, wc) : mbar_wait(full_bar(stage), phase, wc);
+            if (!landed) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
             const uint32_t sb = sa + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES);
@@ -277,6 +297,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
       }
       tc_commit_pair(teardown_bar);
       drain_wait_pair(teardown_bar, 0, p.timeout_ns);
+    }
+  } else if (XF && warp >= 2 + EPI_WARPS) {
+    // ------------------------ operand transforms (both CTAs) ------------------------
+    // Wait for this CTA's copies of a stage, transform the loaded bytes of A and/or
+    // B in place, make the writes visible to the tensor cores (async proxy) and
+    // count the warp in on the leader's stage-transformed barrier.
+    constexpr int NT = 32 * XF_WARPS;
+    const int xt = (int)threadIdx.x - 32 * (2 + EPI_WARPS);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    SegmentIter it(cluster_id, num_clusters, p.num_tiles, p.sk_first_tile, p.num_kb, p.half_first_tile);
+    int tile, kb0, kb1, half;
+    while (ok && it.next(tile, kb0, kb1, half)) {
+      for (int kb = kb0; kb < kb1; kb += PAIR_SLABS) {
+        const int nsl = kb1 - kb < PAIR_SLABS ? kb1 - kb : PAIR_SLABS;
+        if (!warp_wait_pair(full_bar(stage), phase, wc)) { ok = false; break; }
+        const uint32_t sa = base + (uint32_t)(stage * PAIR_STAGE_BYTES);
+        const uint32_t sb = sa + (uint32_t)(PAIR_SLABS * PAIR_A_BYTES);
+        if (p.xf.a_on)
+          xf_smem(sa, (uint32_t)(A_MN ? PAIR_SLABS : nsl) * (uint32_t)PAIR_A_BYTES, p.xf, 0, xt, NT);
+        if (p.xf.b_on) {
+          if (B_MN) {
+            xf_smem(sb, (half < 0 ? 2u : 1u) * MN_STAGE_BYTES, p.xf, 1, xt, NT);
+          } else if (half < 0) {
+            xf_smem(sb, (uint32_t)nsl * (uint32_t)PAIR_B_BYTES, p.xf, 1, xt, NT);
+          } else {
+            for (int sl = 0; sl < nsl; ++sl)
+              xf_smem(sb + (uint32_t)(sl * PAIR_B_BYTES), (uint32_t)(PAIR_B_BYTES / 2), p.xf, 1, xt, NT);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(xf_bar(stage));
+          else mbar_arrive_cluster(mapa_shared(xf_bar(stage), pair_leader));
+        }
+        if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+      }
     }
   } else {
     // ---------------------------- epilogue (both CTAs) ----------------------------
@@ -440,17 +499,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
   if (warp == 1) tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
 }
 
-template <bool INT_MODE, bool A_MN, bool B_MN>
+template <bool INT_MODE, bool A_MN, bool B_MN, bool XF>
 int max_clusters_for(int device) {
   static int cached[64] = {};
   if (device < 0 || device >= 64) return 0;
   if (cached[device] > 0) return cached[device];
-  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN, XF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)PAIR_SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 256, 1, 1);
-  cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
+  cfg.blockDim = dim3(PairThreads<INT_MODE, XF>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -460,7 +519,7 @@ int max_clusters_for(int device) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN, XF>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -468,7 +527,7 @@ int max_clusters_for(int device) {
   return n;
 }
 
-template <bool INT_MODE, bool A_MN, bool B_MN>
+template <bool INT_MODE, bool A_MN, bool B_MN, bool XF>
 cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   static_assert(PAIR_SMEM <= 232448, "shared memory budget");
   int dev = 0;
@@ -476,8 +535,8 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)PAIR_SMEM);
+    e = cudaFuncSetAttribute(tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN, XF>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PAIR_SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -487,7 +546,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   // other, so they must all start together on an otherwise free GPU.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(PairThreads<INT_MODE>::THREADS, 1, 1);
+  cfg.blockDim = dim3(PairThreads<INT_MODE, XF>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = PAIR_SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -495,7 +554,7 @@ cudaError_t launch_mode(const TcParams& p, int clusters, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = p.sk_first_tile == p.num_tiles ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN>, p);
+  return cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<INT_MODE, A_MN, B_MN, XF>, p);
 }
 
 }  // namespace
@@ -505,23 +564,29 @@ int tc_pair_k_per_stage() { return PAIR_SLABS * TC_BK; }
 size_t tc_pair_smem_bytes() { return PAIR_SMEM; }
 
 int tc_pair_max_clusters(int device) {
-  // Every instantiation has the same threads per mode and shared memory.
-  const int a = max_clusters_for<false, false, false>(device);
-  const int b = max_clusters_for<true, false, false>(device);
-  return a < b ? a : b;
+  // Every instantiation has the same shared memory; the thread counts differ by mode.
+  const int a = max_clusters_for<false, false, false, false>(device);
+  const int b = max_clusters_for<true, false, false, false>(device);
+  const int c = max_clusters_for<false, false, false, true>(device);
+  return std::min(a, std::min(b, c));
 }
 
-template <bool INT_MODE>
+template <bool INT_MODE, bool XF>
 cudaError_t launch_layouts(const TcParams& p, int clusters, cudaStream_t stream) {
   if (p.a_mn_major)
-    return p.b_mn_major ? launch_mode<INT_MODE, true, true>(p, clusters, stream)
-                        : launch_mode<INT_MODE, true, false>(p, clusters, stream);
-  return p.b_mn_major ? launch_mode<INT_MODE, false, true>(p, clusters, stream)
-                      : launch_mode<INT_MODE, false, false>(p, clusters, stream);
+    return p.b_mn_major ? launch_mode<INT_MODE, true, true, XF>(p, clusters, stream)
+                        : launch_mode<INT_MODE, true, false, XF>(p, clusters, stream);
+  return p.b_mn_major ? launch_mode<INT_MODE, false, true, XF>(p, clusters, stream)
+                      : launch_mode<INT_MODE, false, false, XF>(p, clusters, stream);
 }
 
 cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream) {
-  return p.chunk_kb > 0 ? launch_layouts<true>(p, clusters, stream) : launch_layouts<false>(p, clusters, stream);
+  if (p.chunk_kb > 0) return p.xf.a_on || p.xf.b_on ? cudaErrorInvalidValue : launch_layouts<true, false>(p, clusters, stream);
+  // Operand transforms run in their own instance (four more warps), and without
+  // the stream-K tail (the host turns it off for them).
+  if (p.xf.a_on || p.xf.b_on)
+    return p.sk_first_tile < p.num_tiles ? cudaErrorInvalidValue : launch_layouts<false, true>(p, clusters, stream);
+  return launch_layouts<false, false>(p, clusters, stream);
 }
 
 }  // namespace gemmlib

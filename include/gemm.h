@@ -83,7 +83,36 @@ typedef enum {
  * library's reading).  out_scale is read for that cast only.
  * c_act is the elementwise transform applied to C as it is read ("ReLU on C",
  * "Flexible Performant GEMM Kernels on GPUs", section 5.3, Table 2); it only
- * matters when beta != 0. */
+ * matters when beta != 0.
+ *
+ * Operand transforms (load_xf != 0): the elementwise transforms that section
+ * 4.2 of the same paper ("Transforms", Figure 10) applies to the A and B tiles
+ * right after they are loaded and before the multiply-accumulate, e.g. a
+ * scaling and an activation.  With bit GEMM_XF_A of load_xf set, every element
+ * a of op(A) enters the product as
+ *     t_A(a) = a_act(a_scale * a)
+ * (the same for B with bit GEMM_XF_B, b_act and b_scale): the product is taken
+ * in fp32 and rounded to nearest even, then the activation (GEMM_ACT_NONE, or
+ * GEMM_ACT_RELU with threshold 0); for F16/BF16 plans the result is rounded to
+ * nearest even back to the operand's own type, since the tensor cores multiply
+ * 16-bit operands; F32 plans keep the fp32 value.  S8 plans accept the
+ * activation only (scale exactly 1; anything else is GEMM_ERR_UNSUPPORTED).
+ * Scales must be finite (else GEMM_ERR_INVALID_ARG).  load_xf == 0 (a
+ * zero-initialised struct) applies no transform and ignores the four fields.
+ * Where they run: the CUDA-core kernels transform each element as they load it;
+ * S8 plans in the int8 -> fp16 staging pass.  The tensor-core kernels either
+ * transform the staged shared-memory tiles in place, in extra warps, or -- for
+ * an operand that several output tiles re-read and that is at least 4 MiB --
+ * run a transform pass over the operand into plan-owned device scratch first
+ * (one read and one write of the operand at memory bandwidth, cheaper than
+ * transforming it once per re-reading tile inside the kernel);
+ * gemm_config_t.xf_staged reports which.  Environment GEMM_XF_STAGE=0 keeps
+ * every transform inside the kernel, =1 stages every transformed 16-bit
+ * operand.  The operands in memory are never modified.
+ * gemm_run_diag and gemm_run_complex return GEMM_ERR_UNSUPPORTED when
+ * load_xf != 0. */
+#define GEMM_XF_A 1u
+#define GEMM_XF_B 2u
 typedef struct {
     const void* bias;             /* device pointer, or NULL when bias_mode == GEMM_BIAS_NONE */
     gemm_dtype_t bias_dtype;      /* F32/F16/BF16 for floating plans, S32 for int8 plans */
@@ -92,6 +121,11 @@ typedef struct {
     gemm_dtype_t out_dtype;       /* dtype of D */
     gemm_act_t c_act;             /* transform of C as it is read (GEMM_ACT_NONE / GEMM_ACT_RELU) */
     float out_scale;              /* S8 plans with out_dtype GEMM_S8: the requantisation scale (finite) */
+    uint32_t load_xf;             /* GEMM_XF_A | GEMM_XF_B: which operands are transformed after load */
+    gemm_act_t a_act;             /* t_A(a) = a_act(a_scale * a) */
+    float a_scale;
+    gemm_act_t b_act;             /* t_B(b) = b_act(b_scale * b) */
+    float b_scale;
 } gemm_epilogue_t;
 
 typedef struct gemm_plan* gemm_plan_t;
@@ -126,6 +160,10 @@ typedef struct {
     int32_t half_tiles;   /* CTA-pair kernel: the last half_tiles tiles (a partial last wave
                              of at most half the CTA pairs) each run as two units of 256 x 128,
                              on two CTA pairs, so that the last wave takes half a tile's time */
+    int32_t xf_staged;    /* operand transforms (gemm_epilogue_t.load_xf) applied by a staging
+                             pass into plan scratch before the GEMM rather than inside it:
+                             GEMM_XF_A and/or GEMM_XF_B; 0 = every requested transform runs
+                             inside the GEMM kernel (or none was requested) */
 } gemm_config_t;
 
 /* ---------------------------------------------------------------------------
@@ -350,10 +388,11 @@ gemm_status_t gemm_plan_set_timeout(gemm_plan_t plan, uint64_t timeout_ns);
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* gemm_status_string(gemm_status_t status);
 
-/* ABI version of this header (major * 100 + minor): 108 (gemm_epilogue_t.c_act,
+/* ABI version of this header (major * 100 + minor): 109 (gemm_epilogue_t.c_act,
  * gemm_run_strided_batched, gemm_run_diag, gemm_run_complex, gemm_config_t.cluster,
  * gemm_epilogue_t.out_scale and int8 D, gemm_config_t.half_tiles,
- * gemm_noalloc_device_status and gemm_noalloc_set_timeout). */
+ * gemm_noalloc_device_status and gemm_noalloc_set_timeout, the operand
+ * transforms gemm_epilogue_t.load_xf / a_act / a_scale / b_act / b_scale). */
 int gemm_abi_version(void);
 
 /* ---------------------------------------------------------------------------

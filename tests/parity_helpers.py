@@ -83,6 +83,20 @@ def check_close(D_gpu: torch.Tensor, D_ref_raw: np.ndarray, d_dtype: str, what: 
         assert fro <= FRO_TOL, f"{what}: relative Frobenius error {fro:.3e} > {FRO_TOL}"
 
 
+def _act(a: str) -> int:
+    return G.GEMM_ACT_RELU if a == "relu" else G.GEMM_ACT_NONE
+
+
+def epilogue_for(p: I.Problem, bias_ptr: int = 0, **overrides) -> G.gemm_epilogue_t:
+    """The library's epilogue struct for a problem: bias, activations, output
+    type, and the operand transforms of A and B after load."""
+    kw = dict(out_scale=p.out_scale, a_act=_act(p.a_act), a_scale=p.a_scale, b_act=_act(p.b_act),
+              b_scale=p.b_scale)
+    kw.update(overrides)
+    return G.make_epilogue(G.DTYPE_CODES[p.d], bias_ptr, G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
+                           G_BIAS[p.bias_mode], _act(p.act), _act(p.c_act), **kw)
+
+
 class DeviceProblem:
     """Device copies of a problem's inputs, plus a guarded output buffer."""
 
@@ -98,14 +112,7 @@ class DeviceProblem:
         self.D = self.Dbuf[GUARD_ROWS:GUARD_ROWS + p.M]
 
     def epilogue(self) -> G.gemm_epilogue_t:
-        p = self.p
-        return G.make_epilogue(G.DTYPE_CODES[p.d],
-                               self.bias.data_ptr() if self.bias is not None else 0,
-                               G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32,
-                               G_BIAS[p.bias_mode],
-                               G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE,
-                               G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE,
-                               out_scale=p.out_scale)
+        return epilogue_for(self.p, self.bias.data_ptr() if self.bias is not None else 0)
 
     def run(self, plan: G.Plan, stream=None):
         p = self.p

@@ -2,6 +2,7 @@
 every entry point include/gemm.h declares, validates arguments and selects
 kernels as documented.  No compute call is made."""
 import os
+import ctypes
 import re
 
 import pytest
@@ -37,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings():
-    assert G.gemm_abi_version() == 108
+    assert G.gemm_abi_version() == 109
     for s in range(6):
         assert G.gemm_status_string(s).startswith("GEMM_")
     assert "unknown" in G.gemm_status_string(99)
@@ -75,9 +76,43 @@ def test_validation_accepts_a_plain_problem():
      G.GEMM_ERR_INVALID_ARG),                                        # bias type
     (dict(M=1 << 31), G.GEMM_ERR_UNSUPPORTED),
     (dict(epi=G.make_epilogue(G.GEMM_F32, c_act=7)), G.GEMM_ERR_INVALID_ARG),
+    # operand transforms
+    (dict(epi=G.make_epilogue(G.GEMM_F32, load_xf=4)), G.GEMM_ERR_INVALID_ARG),      # unknown operand bit
+    (dict(epi=G.make_epilogue(G.GEMM_F32, a_act=5)), G.GEMM_ERR_INVALID_ARG),        # unknown activation
+    (dict(epi=G.make_epilogue(G.GEMM_F32, b_act=2)), G.GEMM_ERR_INVALID_ARG),
+    (dict(epi=G.make_epilogue(G.GEMM_F32, a_scale=float("nan"))), G.GEMM_ERR_INVALID_ARG),
+    (dict(epi=G.make_epilogue(G.GEMM_F32, b_scale=float("inf"))), G.GEMM_ERR_INVALID_ARG),
+    (dict(ab=G.GEMM_S8, c=G.GEMM_S32, epi=G.make_epilogue(G.GEMM_S32, a_scale=2.0)),
+     G.GEMM_ERR_UNSUPPORTED),                                        # int8 operands: activation only
 ])
 def test_validation_rejects(kw, status):
     assert _v(**kw) == status
+
+
+@pytest.mark.parametrize("kw", [
+    dict(epi=G.make_epilogue(G.GEMM_F32, a_act=G.GEMM_ACT_RELU, a_scale=-2.5, b_scale=0.5)),
+    dict(ab=G.GEMM_BF16, epi=G.make_epilogue(G.GEMM_BF16, b_act=G.GEMM_ACT_RELU)),
+    dict(ab=G.GEMM_F32, epi=G.make_epilogue(G.GEMM_F32, a_scale=3.0)),
+    dict(ab=G.GEMM_S8, c=G.GEMM_S32, epi=G.make_epilogue(G.GEMM_S32, a_act=G.GEMM_ACT_RELU,
+                                                          b_act=G.GEMM_ACT_RELU)),
+    # fields of an operand whose bit is clear are ignored
+    dict(epi=G.make_epilogue(G.GEMM_F32, a_act=9, a_scale=float("nan"), load_xf=G.GEMM_XF_B)),
+])
+def test_validation_accepts_operand_transforms(kw):
+    assert _v(**kw) == G.GEMM_OK
+
+
+def test_epilogue_struct_matches_the_header():
+    """The binding's struct has the header's fields in order (offsets of a C
+    struct of ints, floats and one pointer on an LP64 target)."""
+    E = G.gemm_epilogue_t
+    names = [n for n, _ in E._fields_]
+    assert names == ["bias", "bias_dtype", "bias_mode", "act", "out_dtype", "c_act", "out_scale", "load_xf",
+                     "a_act", "a_scale", "b_act", "b_scale"]
+    assert E.load_xf.offset == 32 and E.b_scale.offset == 48 and ctypes.sizeof(E) == 56
+    e = G.make_epilogue(G.GEMM_F32, b_act=G.GEMM_ACT_RELU)
+    assert e.load_xf == G.GEMM_XF_B and e.a_scale == 1.0
+    assert G.make_epilogue(G.GEMM_F32).load_xf == 0
 
 
 def test_validation_edge_cases_accepted():

@@ -49,10 +49,7 @@ def run_batched(p: I.Problem, batch: int, seed: int, share_b=False, gap=8, kerne
     s = H.SENTINEL[p.d]
     Dbuf = torch.full((batch * sd,), s, dtype=I.TORCH_DTYPES[p.d], device="cuda")
     plan = H.make_plan(p, kernel)
-    epi = G.make_epilogue(G.DTYPE_CODES[p.d], bias.data_ptr() if bias is not None else 0,
-                          G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32, H.G_BIAS[p.bias_mode],
-                          G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE,
-                          G.GEMM_ACT_RELU if p.c_act == "relu" else G.GEMM_ACT_NONE)
+    epi = H.epilogue_for(p, bias.data_ptr() if bias is not None else 0)
     G.gemm_run_strided_batched(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b],
                                p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, sa, B.data_ptr(), p.ldb,
                                sb, p.beta, C.data_ptr() if C is not None else None,
