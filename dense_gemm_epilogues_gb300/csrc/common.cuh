@@ -606,6 +606,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// 1-D tiled TMA load (a box of a vector; zero fill past its end).
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* tm, int32_t x, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled TMA load (x innermost, z = problem of a batch).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar) {

@@ -10,7 +10,16 @@
 // end on GB300 that is an HBM-bound elementwise pass over x, C and D: no zero is
 // stored or loaded and no tensor-core instruction is issued.
 //
-// Work decomposition: 64 x 64 tiles of D, CTAs persistent over the tiles; each
+// Two kernels share the arithmetic.  The TMA-staged kernel (16-bit x, and C
+// absent or fp32/fp16/bf16, every operand TMA-alignable) keeps the bytes in
+// flight in shared memory instead of registers: one producer thread per CTA
+// streams 64 x 64 boxes of x and C, and the tile's 64 entries of the diagonal
+// and of the bias, with TMA into a ring of stages, one CTA per
+// SM, and sixteen consumer warps finish each tile from shared memory (lane = row,
+// eight consecutive columns per lane, so every D store writes whole 32-byte
+// sectors).  The register kernel below serves every other type and alignment.
+//
+// Register kernel work decomposition: 64 x 64 tiles of D, CTAs persistent over the tiles; each
 // thread owns two 8-wide row segments of a tile.  x, C and D move as aligned
 // 8-element vectors where the host found the rows (columns) aligned, scalars
 // otherwise and at ragged edges.  A column-major x is read column-contiguous
@@ -181,6 +190,12 @@ __device__ __forceinline__ void store8_d(void* D, int dt, int64_t idx, bool vec,
 
 __device__ __forceinline__ int clamp8(int64_t v) { return v <= 0 ? 0 : (v >= 8 ? 8 : (int)v); }
 
+// All lanes of a warp wait; the warp gives up together if any lane gave up.
+__device__ __forceinline__ bool warp_all_wait(uint32_t bar, uint32_t parity, const WaitCtx& wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // ------------------------------- the kernel ---------------------------------
 
 template <typename XT, bool X_ROW_MAJOR>
@@ -306,6 +321,205 @@ __global__ void __launch_bounds__(DG_THREADS) diag_gemm_kernel(const DiagParams 
   }
 }
 
+// ------------------------- the TMA-staged kernel ----------------------------
+
+// Sixteen consumer warps, one 32-row x 8-column task each per tile: with eight
+// (two tasks each) the consumers could not keep up (4096^2, fp16 x, fp32 C and
+// D: 30.5 / 33.2 us for row- / column-major x against 27.8 / 28.5 us with 16).
+constexpr int DT_CONS_WARPS = 16;
+constexpr int DT_THREADS = 32 * (DT_CONS_WARPS + 1);        // + one producer warp
+constexpr int DT_X_BYTES = DIAG_TM * DIAG_TN * 2;           // 8 KiB: a 16-bit x box
+constexpr int DT_C_BYTES = DIAG_TM * DIAG_TN * 4;           // 16 KiB: fp32 C (16-bit C uses half)
+constexpr int DT_V_OFF = DT_X_BYTES + DT_C_BYTES;           // the tile's 64 diagonal entries (16-bit)
+constexpr int DT_BIAS_OFF = DT_V_OFF + 128;                 // the tile's 64 bias entries (up to fp32)
+constexpr int DT_STAGE_BYTES = DT_X_BYTES + DT_C_BYTES + 1024;   // whole KiBs keep the boxes 1024-aligned
+constexpr size_t DT_SMEM = 1024 + (size_t)DIAG_TMA_STAGES * DT_STAGE_BYTES + 2 * DIAG_TMA_STAGES * 8 + 16;
+static_assert(DIAG_TM == 64 && DIAG_TN == 64 && DT_CONS_WARPS == 16, "16 tasks of 32 rows x 8 columns per 64 x 64 box");
+
+// Byte offset of 16-byte chunk q of row R in a box stored with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128(uint32_t R, uint32_t q) { return R * 128u + ((q ^ (R & 7u)) << 4); }
+
+__device__ __forceinline__ float h16_to_float(uint16_t b, bool bf16) {
+  if (bf16) return __uint_as_float((uint32_t)b << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+template <bool X_ROW_MAJOR>
+__global__ void __launch_bounds__(DT_THREADS, 1) diag_tma_kernel(const __grid_constant__ DiagParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;        // swizzle atoms need 1024-byte alignment
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar0 = base + (uint32_t)(DIAG_TMA_STAGES * DT_STAGE_BYTES);
+  volatile int32_t* abort_flag =
+      reinterpret_cast<volatile int32_t*>(base_ptr + DIAG_TMA_STAGES * DT_STAGE_BYTES + 2 * DIAG_TMA_STAGES * 8);
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(DIAG_TMA_STAGES + s); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const EpiParams& e = p.epi;
+  const bool c_f32 = e.c_dtype == GEMM_F32;
+  const uint32_t c_bytes = e.read_c ? (c_f32 ? (uint32_t)DT_C_BYTES : (uint32_t)DT_C_BYTES / 2) : 0u;
+  const bool has_bias = e.bias_mode != GEMM_BIAS_NONE;
+  const uint32_t bias_bytes = has_bias ? 64u * (uint32_t)dtype_bytes(e.bias_dtype) : 0u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DIAG_TMA_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);               // the producer's expect_tx arrival + the copies' bytes
+      mbar_init(empty_bar(s), DT_CONS_WARPS);  // one arrival per consumer warp
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == DT_CONS_WARPS) {
+    // ------------------------------- producer -------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tmX);
+      if (e.read_c) tma_prefetch_desc(&p.tmC);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_parity = 0;
+      for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        const int32_t i0 = (int32_t)((t / p.tiles_n) * DIAG_TM);
+        const int32_t j0 = (int32_t)((t % p.tiles_n) * DIAG_TN);
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) break;
+        const uint32_t fb = full_bar(stage);
+        const uint32_t sx = base + (uint32_t)(stage * DT_STAGE_BYTES);
+        mbar_expect_tx(fb, (uint32_t)DT_X_BYTES + c_bytes + 128u + bias_bytes);
+        tma_load_1d(sx + DT_V_OFF, &p.tmDiag, p.left ? i0 : j0, fb);
+        if (has_bias) tma_load_1d(sx + DT_BIAS_OFF, &p.tmBias, e.bias_mode == GEMM_BIAS_ROW ? i0 : j0, fb);
+        if (X_ROW_MAJOR) tma_load_2d(sx, &p.tmX, j0, i0, fb);   // rows of x: (columns, rows)
+        else tma_load_2d(sx, &p.tmX, i0, j0, fb);               // columns of x: (rows, columns)
+        if (e.read_c) {
+          tma_load_2d(sx + DT_X_BYTES, &p.tmC, j0, i0, fb);
+          if (c_f32) tma_load_2d(sx + DT_X_BYTES + DT_C_BYTES / 2, &p.tmC, j0 + 32, i0, fb);
+        }
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == DIAG_TMA_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      // Every copy this thread started lands before the CTA may exit.
+      for (int s = 0; s < DIAG_TMA_STAGES; ++s)
+        if (issued & (1u << s)) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(full_bar(s), (last_parity >> s) & 1u))
+            if (globaltimer_ns() - t0 > 1000000000ull) break;
+        }
+    }
+  } else {
+    // ------------------------------- consumers ------------------------------
+    const bool bf16 = p.ab_dtype == GEMM_BF16;
+    const EpiPtrs ptr = epi_ptrs(e, 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      const int64_t i0 = (t / p.tiles_n) * DIAG_TM;
+      const int64_t j0 = (t % p.tiles_n) * DIAG_TN;
+      if (!warp_all_wait(full_bar(stage), phase, wc)) break;
+      const uint8_t* sx = base_ptr + stage * DT_STAGE_BYTES;
+      const uint8_t* sc = sx + DT_X_BYTES;
+      const uint16_t* sv = reinterpret_cast<const uint16_t*>(sx + DT_V_OFF);
+      const uint8_t* sbias = sx + DT_BIAS_OFF;
+      {
+        // Task: rows 32h .. 32h + 31 of the tile (one per lane), columns 8g .. 8g + 7.
+        const int task = warp;
+        const int h = task / 8, g = task % 8;
+        const int r = 32 * h + lane;
+        const int64_t i = i0 + r, j = j0 + 8 * g;
+        float x[8];
+        if constexpr (X_ROW_MAJOR) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sx + sw128((uint32_t)r, (uint32_t)g));
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            x[2 * u] = h16_to_float((uint16_t)(ww[u] & 0xffffu), bf16);
+            x[2 * u + 1] = h16_to_float((uint16_t)(ww[u] >> 16), bf16);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            x[u] = h16_to_float(*reinterpret_cast<const uint16_t*>(
+                                    sx + sw128((uint32_t)(8 * g + u), (uint32_t)(r >> 3)) + (uint32_t)(r & 7) * 2u),
+                                bf16);
+        }
+        float c[8];
+        if (e.read_c) {
+          if (c_f32) {
+            const uint8_t* box = sc + (g >> 2) * (DT_C_BYTES / 2);
+            const uint4 a = *reinterpret_cast<const uint4*>(box + sw128((uint32_t)r, (uint32_t)(2 * (g & 3))));
+            const uint4 b = *reinterpret_cast<const uint4*>(box + sw128((uint32_t)r, (uint32_t)(2 * (g & 3) + 1)));
+            c[0] = __uint_as_float(a.x); c[1] = __uint_as_float(a.y); c[2] = __uint_as_float(a.z);
+            c[3] = __uint_as_float(a.w); c[4] = __uint_as_float(b.x); c[5] = __uint_as_float(b.y);
+            c[6] = __uint_as_float(b.z); c[7] = __uint_as_float(b.w);
+          } else {
+            const uint4 w = *reinterpret_cast<const uint4*>(sc + sw128((uint32_t)r, (uint32_t)g));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            const bool cb = e.c_dtype == GEMM_BF16;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              c[2 * u] = h16_to_float((uint16_t)(ww[u] & 0xffffu), cb);
+              c[2 * u + 1] = h16_to_float((uint16_t)(ww[u] >> 16), cb);
+            }
+          }
+          if (e.c_relu) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c[u] = fmaxf(c[u], 0.0f);
+          }
+        }
+        if (i < p.M && j < p.N) {
+          const int n_out = clamp8(p.N - j);
+          float v[8];
+          const float drow = p.left ? h16_to_float(sv[r], bf16) : 0.0f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float d = p.left ? drow : h16_to_float(sv[8 * g + u], bf16);
+            v[u] = e.alpha * (d * x[u]);
+            if (e.read_c) v[u] = fmaf(e.beta, c[u], v[u]);
+          }
+          if (e.bias_mode == GEMM_BIAS_COL) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] += load_as_float(sbias, e.bias_dtype, 8 * g + u);
+          } else if (e.bias_mode == GEMM_BIAS_ROW) {
+            const float b = load_as_float(sbias, e.bias_dtype, r);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] += b;
+          }
+          if (e.relu) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = fmaxf(v[u], 0.0f);
+          }
+          store8_d(ptr.D, e.d_dtype, i * e.ldd + j, e.vec_d != 0, n_out, v);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(stage));
+      if (++stage == DIAG_TMA_STAGES) { stage = 0; phase ^= 1u; }
+    }
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_tma(const DiagParams& p, int x_row_major, int sm_count, int* grid_out, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  if (dev < 64 && !configured[dev]) {
+    ce = cudaFuncSetAttribute(diag_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM);
+    if (ce == cudaSuccess)
+      ce = cudaFuncSetAttribute(diag_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM);
+    if (ce != cudaSuccess) return ce;
+    configured[dev] = true;
+  }
+  const int grid = (int)std::min<int64_t>(p.num_tiles, std::max(1, sm_count));
+  if (x_row_major) diag_tma_kernel<true><<<grid, DT_THREADS, DT_SMEM, stream>>>(p);
+  else diag_tma_kernel<false><<<grid, DT_THREADS, DT_SMEM, stream>>>(p);
+  *grid_out = grid;
+  return cudaGetLastError();
+}
+
 template <typename XT, bool RM>
 cudaError_t launch_one(const DiagParams& p, int sm_count, int* grid_out, cudaStream_t stream) {
   // Resident CTAs per SM of this instantiation (looked up once per process).
@@ -327,6 +541,10 @@ cudaError_t launch_one(const DiagParams& p, int sm_count, int* grid_out, cudaStr
 
 cudaError_t launch_diag(const DiagParams& p, int x_row_major, int sm_count, int* grid_out, cudaStream_t stream) {
   if (p.num_tiles <= 0) return cudaErrorInvalidValue;
+  if (p.use_tma) {
+    if (p.ab_dtype != GEMM_F16 && p.ab_dtype != GEMM_BF16) return cudaErrorInvalidValue;
+    return launch_tma(p, x_row_major, sm_count, grid_out, stream);
+  }
   switch (p.ab_dtype) {
     case GEMM_F16:
       return x_row_major ? launch_one<__half, true>(p, sm_count, grid_out, stream)

@@ -610,6 +610,39 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
   return launch_tc(tp, bn, cfg.grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// A 2-D tensor map with elements of `es` bytes, 128-byte swizzle (the
+// diagonal kernel's boxes: 128-byte inner extent).
+bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, int es, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  if (!encode_fn()) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * (uint64_t)es};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A 1-D tensor map over a vector of n elements, boxes of `box` elements.
+bool encode_1d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t n, uint32_t box) {
+  if (!encode_fn()) return false;
+  cuuint64_t dims[1] = {n};
+  cuuint64_t strides[1] = {0};   // unused for rank 1
+  cuuint32_t boxd[1] = {box};
+  cuuint32_t estr[1] = {1};
+  CUresult r = g_encode(tm, dt, 1, const_cast<void*>(ptr), dims, strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+CUtensorMapDataType tma_dtype(gemm_dtype_t t) {
+  return t == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                       : t == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
 // The CTA-pair kernel: each CTA of a pair loads 128 rows of A and 128 columns
 // of B per K block, so both tensor maps use 128-row (K-major) or 64 x 64
 // (MN-major) boxes; the MMA instruction covers M = 256, N = 256.
@@ -1128,6 +1161,33 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx
   p.vec_x = (aligned16(X) && (ldx * es) % 16 == 0) ? 1 : 0;
   p.vec_diag = aligned16(diag) ? 1 : 0;
   p.epi = make_epi(plan, alpha, beta, C, ldc, D, ldd, epi);
+  // 16-bit x with TMA-alignable x and C: the TMA-staged kernel (x and C stream
+  // through a ring of shared-memory stages; GEMM_DIAG_TMA=0 keeps the register kernel).
+  const int cs = dtype_bytes(plan->c);
+  const bool has_bias = p.epi.bias_mode != GEMM_BIAS_NONE;
+  bool tma = is_f16ish(plan->ab) && tma_ok(X, ldx, 2) && aligned16(diag) &&
+             (!p.epi.read_c || (is_float_out(plan->c) && tma_ok(C, ldc, cs))) &&
+             (!has_bias || (is_float_out((gemm_dtype_t)p.epi.bias_dtype) && aligned16(p.epi.bias)));
+  if (const char* env = std::getenv("GEMM_DIAG_TMA"))
+    if (std::atoi(env) == 0) tma = false;
+  if (tma) {
+    const CUtensorMapDataType xdt =
+        plan->ab == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const bool x_rm = lx == GEMM_OP_T;
+    bool ok = encode_2d(&p.tmX, xdt, 2, X, x_rm ? (uint64_t)N : (uint64_t)M, x_rm ? (uint64_t)M : (uint64_t)N,
+                        (uint64_t)ldx, DIAG_TN, DIAG_TM);
+    if (ok && p.epi.read_c)
+      ok = encode_2d(&p.tmC, tma_dtype(plan->c), cs, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc,
+                     plan->c == GEMM_F32 ? 32 : 64, DIAG_TM);
+    if (ok) ok = encode_1d(&p.tmDiag, xdt, diag, (uint64_t)(left ? M : N), 64);
+    if (ok && has_bias)
+      ok = encode_1d(&p.tmBias, tma_dtype((gemm_dtype_t)p.epi.bias_dtype), p.epi.bias,
+                     (uint64_t)(p.epi.bias_mode == GEMM_BIAS_ROW ? M : N), 64);
+    if (!ok) return GEMM_ERR_CUDA;
+    p.use_tma = 1;
+    p.err = plan->d_err;
+    p.timeout_ns = plan->timeout_ns;
+  }
   int grid = 0;
   if (launch_diag(p, lx == GEMM_OP_T, plan->sm_count, &grid, reinterpret_cast<cudaStream_t>(stream_)) !=
       cudaSuccess)
@@ -1135,7 +1195,7 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx
   cfg.kernel = GEMM_KERNEL_DIAG;
   cfg.bm = DIAG_TM;
   cfg.bn = DIAG_TN;
-  cfg.stages = 1;
+  cfg.stages = p.use_tma ? DIAG_TMA_STAGES : 1;
   cfg.grid = grid;
   cfg.tiles = (int32_t)std::min<int64_t>(p.num_tiles, kMaxDim);
   plan->last = cfg;

@@ -100,6 +100,15 @@ inline cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) { retur
 // (left) or epilogue(alpha * x * diag(d) + beta * C) (right), x the dense
 // operand seen as an M x N matrix.  One product per output, no tensor cores.
 struct DiagParams {
+  // TMA-staged kernel (use_tma): 64 x 64 boxes of x (128-byte swizzle; 16-bit x)
+  // and of C (two 32-column boxes for fp32 C), loaded into a ring of stages.
+  CUtensorMap tmX;
+  CUtensorMap tmC;
+  CUtensorMap tmDiag;     // TMA-staged kernel: 64-entry boxes of the diagonal
+  CUtensorMap tmBias;     // TMA-staged kernel: 64-entry boxes of the bias vector (when there is one)
+  int32_t use_tma;
+  int32_t* err;           // TMA-staged kernel: error word (first expired wait)
+  uint64_t timeout_ns;    // TMA-staged kernel: bound of every wait
   const void* X;          // dense operand, ab_dtype, row-major (layout T) or column-major (N)
   const void* diag;       // the diagonal: M entries (left) or N entries (right), ab_dtype
   int64_t ldx;
@@ -112,6 +121,7 @@ struct DiagParams {
   EpiParams epi;
 };
 constexpr int DIAG_TM = 64, DIAG_TN = 64;
+constexpr int DIAG_TMA_STAGES = 6;   // ring depth of the TMA-staged kernel
 // Persistent launch: min(tiles, sm_count x resident CTAs per SM) CTAs; the grid used goes to *grid_out.
 cudaError_t launch_diag(const DiagParams& p, int x_row_major, int sm_count, int* grid_out, cudaStream_t stream);
 

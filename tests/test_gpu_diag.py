@@ -42,18 +42,49 @@ FLOAT_EPI = [
 ]
 
 
+@pytest.fixture(params=["tma", "registers"])
+def diag_kernel(request, monkeypatch):
+    """16-bit x with TMA-alignable operands takes the TMA-staged kernel by
+    default; GEMM_DIAG_TMA=0 keeps the register kernel, so both are checked."""
+    if request.param == "registers":
+        monkeypatch.setenv("GEMM_DIAG_TMA", "0")
+    else:
+        monkeypatch.delenv("GEMM_DIAG_TMA", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("side", ["left", "right"])
 @pytest.mark.parametrize("layout", ["N", "T"])
 @pytest.mark.parametrize("ab", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("epi", range(len(FLOAT_EPI)))
-def test_diag_float(side, layout, ab, epi):
+def test_diag_float(side, layout, ab, epi, diag_kernel):
     """200 x 136: 4 x 3 tiles of 64 x 64 with ragged last rows and columns."""
+    if ab == "f32" and diag_kernel == "registers":
+        pytest.skip("fp32 x always takes the register kernel (covered by the tma case)")
     kw = dict(FLOAT_EPI[epi])
     if ab == "f32" and kw.get("c"):
         kw["c"] = "f32"                    # fp32 plans take fp32 C only
     p = I.DiagProblem(f"diag_{ab}", ab, side, layout, 200, 136, **kw)
     cfg = run_full(p, 400 + epi)
     assert cfg["tiles"] == 4 * 3 and cfg["bm"] == 64 and cfg["bn"] == 64
+    staged = ab != "f32" and diag_kernel == "tma"
+    assert cfg["stages"] == (6 if staged else 1), cfg
+    assert cfg["grid"] == (min(12, torch.cuda.get_device_properties(0).multi_processor_count) if staged
+                           else cfg["grid"])
+
+
+@pytest.mark.parametrize("side", ["left", "right"])
+@pytest.mark.parametrize("layout", ["N", "T"])
+@pytest.mark.parametrize("cd", [("f32", "f32"), ("bf16", "f16"), (None, "bf16")], ids=["f32C", "bf16C", "noC"])
+def test_diag_tma_kernel_many_tiles(side, layout, cd):
+    """The TMA-staged kernel on more tiles than CTAs (every CTA cycles its ring
+    of stages several times), a ragged last tile row and column, every C type."""
+    c, d = cd
+    kw = dict(alpha=1.5, beta=0.5, c=c) if c else dict(alpha=1.5)
+    p = I.DiagProblem("diag_tma_many", "bf16", side, layout, 64 * 40 + 16, 64 * 33 + 40, d=d,
+                      bias="f32", bias_mode="col", act="relu", **kw)
+    cfg = run_full(p, 440)
+    assert cfg["stages"] == 6 and cfg["tiles"] == 41 * 34
 
 
 @pytest.mark.parametrize("side", ["left", "right"])
