@@ -382,6 +382,17 @@ gemm_status_t select_config(gemm_dtype_t ab, gemm_dtype_t c, gemm_layout_t la, g
       cfg.tiles = (int32_t)std::min<int64_t>(tiles, kMaxDim);
       cfg.grid = cfg.tiles;
       cfg.raster = 1;
+      // A last wave of CTAs at most half full (single problems): its tiles are
+      // split over K, and a reduction pass finishes them (GEMM_FFMA_TAIL=0: off).
+      int split = 0;
+      int64_t tail = batch == 1 ? ffma_tail_split(tiles, K, sm_count, &split) : 0;
+      if (const char* env = std::getenv("GEMM_FFMA_TAIL"))
+        if (std::atoi(env) == 0) tail = 0;
+      if (tail > 0) {
+        cfg.sk_tiles = (int32_t)tail;
+        cfg.split_k = split;
+        cfg.grid = (int32_t)(tiles - tail + tail * split);
+      }
       break;
     }
     default: {  // SIMT
@@ -1021,6 +1032,18 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       fp.K = (int32_t)K;
       fp.stride_a = bt.sa;
       fp.stride_b = bt.sb;
+      fp.full_tiles = cfg.tiles;
+      fp.split = 1;
+      if (cfg.sk_tiles > 0) {
+        // Split tail wave: raw fp32 sums of each part of each tail tile in plan scratch.
+        fp.full_tiles = cfg.tiles - cfg.sk_tiles;
+        fp.split = cfg.split_k;
+        const int64_t nkt = (K + FFMA_BK - 1) / FFMA_BK;
+        fp.kb_per_part = (int32_t)((nkt + cfg.split_k - 1) / cfg.split_k);
+        s = ensure_ws(plan, (size_t)cfg.sk_tiles * cfg.split_k * FFMA_BM * FFMA_BN * sizeof(float), stream);
+        if (s != GEMM_OK) break;
+        fp.ws = static_cast<float*>(plan->ws);
+      }
       fp.xf = xf;
       fp.epi = e;
       s = launch_ffma(fp, la == GEMM_OP_T, lb == GEMM_OP_T, (int)bt.count, stream) == cudaSuccess ? GEMM_OK

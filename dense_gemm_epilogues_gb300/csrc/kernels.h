@@ -63,22 +63,30 @@ size_t tc_pair_smem_bytes();
 int tc_pair_max_clusters(int device);   // co-resident clusters of two (0 if unknown)
 cudaError_t launch_tc_pair(const TcParams& p, int clusters, cudaStream_t stream);
 
-// FFMA SGEMM (fp32, CUDA cores).
+// FFMA SGEMM (fp32, CUDA cores): 128 x 128 tiles, one per CTA of 128 threads.
 struct FfmaParams {
   const float* A;
   const float* B;
   int64_t lda, ldb;
   int64_t stride_a, stride_b;   // batched problems (elements); one problem per grid row
   int32_t M, N, K;
+  // Split tail wave (single problems): tiles [full_tiles, tiles) run as `split`
+  // CTAs each over kb_per_part K slices, writing raw fp32 sums to ws (128 x 128
+  // row-major per tile and part); ffma tail reduction then finishes them.
+  // full_tiles == tiles (split 1): no tail split.
+  int32_t full_tiles;
+  int32_t split;
+  int32_t kb_per_part;
+  float* ws;
   LoadXf xf;                    // transforms of A / B elements as they are loaded
   EpiParams epi;
 };
-// K slice per shared-memory buffer: 8 (measured 5 % faster than 16 at 4096^3 and
-// 8192^3: half the staging registers, the same one barrier per slice).
-#ifndef GEMM_FFMA_BK
-#define GEMM_FFMA_BK 8
-#endif
-constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = GEMM_FFMA_BK;
+constexpr int FFMA_BM = 128, FFMA_BN = 128, FFMA_BK = 16;
+constexpr int FFMA_CTAS_PER_SM = 2;   // 128 threads x <= 256 registers, 33 KiB shared memory each
+// Tail split for a single problem of `tiles` tiles and K of `K` on `sm_count` SMs:
+// when the last wave of CTAs is at most half full, its tiles are split over K
+// into *split parts (0: no split).  Returns the number of tail tiles.
+int64_t ffma_tail_split(int64_t tiles, int64_t K, int sm_count, int* split);
 cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, int batch, cudaStream_t stream);
 
 // Generic CUDA-core kernel: any dtype, layout, alignment; K may be 0.

@@ -19,14 +19,15 @@ namespace {
 
 // ================================ FFMA SGEMM =================================
 
-constexpr int SG_THREADS = 256;
+constexpr int SG_THREADS = 128;
 constexpr int SG_PAD = 4;                       // row padding: conflict-free transposed stores
 constexpr int SG_LDS = FFMA_BM + SG_PAD;        // 132 floats per K row (BM == BN)
 
 // Loads one BK x 128 slice of op(A) (as A^T: [k][m]) or of op(B) ([k][n]) into
-// registers: NV = BK/8 groups of four values per thread (one at BK = 8).  `KMAJOR`: the operand
-// is K-contiguous in global memory (A row-major / B column-major), so a thread
-// loads 4 consecutive K values of one row/column per group; otherwise 4
+// registers as 2 x SG_NV groups of four values per thread (each thread stands
+// for two of the 256 "loader lanes" v = tid and tid + 128).  `KMAJOR`: the
+// operand is K-contiguous in global memory (A row-major / B column-major), so a
+// lane loads 4 consecutive K values of one row/column per group; otherwise 4
 // consecutive M/N values of one K row.
 constexpr int SG_NV = FFMA_BK / 8;
 
@@ -39,66 +40,59 @@ struct SliceLoader {
   int xf_on, xf_relu;  // operand transform t(x) = act(scale * x) after the load
   float xf_scale;
 
-  __device__ __forceinline__ void load(int64_t mn0, int64_t k0, int tid, float (&v)[SG_NV][4]) const {
+  __device__ __forceinline__ void load(int64_t mn0, int64_t k0, int v, float (&out)[SG_NV][4]) const {
 #pragma unroll
     for (int g = 0; g < SG_NV; ++g) {
       if constexpr (KMAJOR) {
-        const int64_t r = mn0 + (tid >> 1);
-        const int64_t k = k0 + (tid & 1) * 4 + g * 8;
+        const int64_t r = mn0 + (v >> 1);
+        const int64_t k = k0 + (v & 1) * 4 + g * 8;
         const float* src = ptr + r * ld + k;
         if (r < extent_mn && k + 4 <= K) {
           const float4 f = *reinterpret_cast<const float4*>(src);
-          v[g][0] = f.x; v[g][1] = f.y; v[g][2] = f.z; v[g][3] = f.w;
+          out[g][0] = f.x; out[g][1] = f.y; out[g][2] = f.z; out[g][3] = f.w;
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[g][j] = (r < extent_mn && k + j < K) ? src[j] : 0.0f;
+          for (int j = 0; j < 4; ++j) out[g][j] = (r < extent_mn && k + j < K) ? src[j] : 0.0f;
         }
       } else {
-        const int64_t k = k0 + (tid >> 5) + g * 8;
-        const int64_t c = mn0 + (tid & 31) * 4;
+        const int64_t k = k0 + (v >> 5) + g * 8;
+        const int64_t c = mn0 + (v & 31) * 4;
         const float* src = ptr + k * ld + c;
         if (k < K && c + 4 <= extent_mn) {
           const float4 f = *reinterpret_cast<const float4*>(src);
-          v[g][0] = f.x; v[g][1] = f.y; v[g][2] = f.z; v[g][3] = f.w;
+          out[g][0] = f.x; out[g][1] = f.y; out[g][2] = f.z; out[g][3] = f.w;
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[g][j] = (k < K && c + j < extent_mn) ? src[j] : 0.0f;
+          for (int j = 0; j < 4; ++j) out[g][j] = (k < K && c + j < extent_mn) ? src[j] : 0.0f;
         }
       }
       if (xf_on) {   // zero fill stays zero: t(0) = 0
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[g][j] = xf_f32(v[g][j], xf_scale, xf_relu);
+        for (int j = 0; j < 4; ++j) out[g][j] = xf_f32(out[g][j], xf_scale, xf_relu);
       }
     }
   }
 
   // Store the values into the [BK][SG_LDS] shared buffer.
-  __device__ __forceinline__ void store(float* s, int tid, const float (&v)[SG_NV][4]) const {
+  __device__ __forceinline__ void store(float* s, int v, const float (&in)[SG_NV][4]) const {
 #pragma unroll
     for (int g = 0; g < SG_NV; ++g) {
       if constexpr (KMAJOR) {
-        const int r = tid >> 1, k = (tid & 1) * 4 + g * 8;
+        const int r = v >> 1, k = (v & 1) * 4 + g * 8;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[(k + j) * SG_LDS + r] = v[g][j];
+        for (int j = 0; j < 4; ++j) s[(k + j) * SG_LDS + r] = in[g][j];
       } else {
-        const int k = (tid >> 5) + g * 8, c = (tid & 31) * 4;
-        *reinterpret_cast<float4*>(&s[k * SG_LDS + c]) = make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
+        const int k = (v >> 5) + g * 8, c = (v & 31) * 4;
+        *reinterpret_cast<float4*>(&s[k * SG_LDS + c]) = make_float4(in[g][0], in[g][1], in[g][2], in[g][3]);
       }
     }
   }
 };
 
-#ifndef GEMM_FFMA_MINB
-#define GEMM_FFMA_MINB 2
-#endif
 // Paired FP32 FMA (fma.rn.f32x2): two independent fp32 FMAs, each rounded as
 // fmaf would, in one instruction -- half the issue slots of scalar FFMA for the
 // same FMA-pipe work.  Adjacent columns of a thread's tile share one packed
 // B operand; the A value is duplicated into both halves.
-#ifndef GEMM_FFMA_PAIRED
-#define GEMM_FFMA_PAIRED 1
-#endif
-
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -110,51 +104,124 @@ __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
+
+// The fused epilogue of four consecutive outputs (row m, columns nb .. nb+3) from
+// their fp32 sums x: alpha, beta * c_act(C), bias, ReLU, cast, store.
+__device__ __forceinline__ void ffma_finish4(const EpiParams& e, const EpiPtrs& ptr, int64_t m, int64_t nb,
+                                             int64_t N, float (&x)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] *= e.alpha;
+  const bool full = nb + 4 <= N;
+  if (e.read_c) {
+    const int64_t off = m * e.ldc + nb;
+    if (full && e.vec_c && e.c_dtype == GEMM_F32) {
+      float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(ptr.C) + off);
+      if (e.c_relu) {
+        c.x = fmaxf(c.x, 0.0f); c.y = fmaxf(c.y, 0.0f); c.z = fmaxf(c.z, 0.0f); c.w = fmaxf(c.w, 0.0f);
+      }
+      x[0] = fmaf(e.beta, c.x, x[0]); x[1] = fmaf(e.beta, c.y, x[1]);
+      x[2] = fmaf(e.beta, c.z, x[2]); x[3] = fmaf(e.beta, c.w, x[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (nb + j < N) {
+          float c = load_as_float(ptr.C, e.c_dtype, off + j);
+          if (e.c_relu) c = fmaxf(c, 0.0f);
+          x[j] = fmaf(e.beta, c, x[j]);
+        }
+    }
+  }
+  if (e.bias_mode == GEMM_BIAS_COL) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (nb + j < N) x[j] += load_as_float(ptr.bias, e.bias_dtype, nb + j);
+  } else if (e.bias_mode == GEMM_BIAS_ROW) {
+    const float b = load_as_float(ptr.bias, e.bias_dtype, m);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] += b;
+  }
+  if (e.relu) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = fmaxf(x[j], 0.0f);
+  }
+  const int64_t doff = m * e.ldd + nb;
+  if (full && e.vec_d && e.d_dtype == GEMM_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(ptr.D) + doff) = make_float4(x[0], x[1], x[2], x[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (nb + j < N) store_float_as(ptr.D, e.d_dtype, doff + j, x[j]);
+  }
+}
+
+// The CUTLASS page's hierarchy ("Thread Block Tile", "Warp Tile", "Thread
+// Tile", "Software Pipelining"): a 128 x 128 block tile over 128 threads, each
+// accumulating an 8 x 16 register tile from 8 x 1 and 1 x 16 fragments of A and B
+// in shared memory (outer products, 64 paired FMAs per K step), with global
+// loads for the next K slice in flight while the current one is multiplied and
+// two shared-memory buffers, one __syncthreads() per slice of 16.  Thread (tx,
+// ty) owns rows 4ty .. 4ty+3 and 64+4ty .. 64+4ty+3, columns 4tx + 32j .. +3
+// (j = 0..3): eight lanes of a quarter warp read 128 contiguous bytes of B, and
+// a quarter warp shares one A address (broadcast).  8 x 16 per thread needs 6
+// shared loads per 64 paired FMAs where 8 x 8 needed 4 per 32: shared-memory
+// throughput bound the 8 x 8 kernel (measured 51.7 against 55.5 TFLOP/s at
+// 4096^3 TN, 54.9 against 60.2 at 8192^3).
 template <bool A_KMAJOR, bool B_KMAJOR>
-__global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(const FfmaParams p) {
+__global__ void __launch_bounds__(SG_THREADS, FFMA_CTAS_PER_SM) ffma_sgemm_kernel(const FfmaParams p) {
   __shared__ __align__(16) float As[2][FFMA_BK * SG_LDS];
   __shared__ __align__(16) float Bs[2][FFMA_BK * SG_LDS];
 
   const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
+  const int tx = tid & 7, ty = tid >> 3;
   const int64_t tiles_n = (p.N + FFMA_BN - 1) / FFMA_BN;
-  const int64_t m0 = (int64_t)(blockIdx.x / tiles_n) * FFMA_BM;
-  const int64_t n0 = (int64_t)(blockIdx.x % tiles_n) * FFMA_BN;
+  // A tail tile is shared by `split` CTAs, each over its own range of K slices.
+  int64_t tile = blockIdx.x;
+  int part = -1;
+  if ((int)blockIdx.x >= p.full_tiles) {
+    const int idx = (int)blockIdx.x - p.full_tiles;
+    tile = p.full_tiles + idx / p.split;
+    part = idx % p.split;
+  }
+  const int64_t m0 = (tile / tiles_n) * FFMA_BM;
+  const int64_t n0 = (tile % tiles_n) * FFMA_BN;
   const int64_t bz = blockIdx.y;                      // problem of the batch
 
   const SliceLoader<A_KMAJOR> la{p.A + bz * p.stride_a, p.lda, p.M, p.K, p.xf.a_on, p.xf.a_relu, p.xf.a_scale};
   const SliceLoader<B_KMAJOR> lb{p.B + bz * p.stride_b, p.ldb, p.N, p.K, p.xf.b_on, p.xf.b_relu, p.xf.b_scale};
 
-#if GEMM_FFMA_PAIRED
-  uint64_t acc2[8][4];   // acc2[i][q] holds columns 2q and 2q+1 of row i
+  uint64_t acc2[8][8];   // acc2[i][q]: row i of the thread, columns 2q and 2q+1 of its 16
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;
-#else
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-#endif
+    for (int q = 0; q < 8; ++q) acc2[i][q] = 0ull;
 
-  const int nkt = (p.K + FFMA_BK - 1) / FFMA_BK;
-  float ra[SG_NV][4], rb[SG_NV][4];
-  if (nkt > 0) {
-    la.load(m0, 0, tid, ra);
-    lb.load(n0, 0, tid, rb);
-    la.store(As[0], tid, ra);
-    lb.store(Bs[0], tid, rb);
+  const int nkt_all = (p.K + FFMA_BK - 1) / FFMA_BK;
+  const int kt0 = part < 0 ? 0 : min(nkt_all, part * p.kb_per_part);
+  const int kt1 = part < 0 ? nkt_all : min(nkt_all, kt0 + p.kb_per_part);
+  float ra[2][SG_NV][4], rb[2][SG_NV][4];
+  if (kt0 < kt1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      la.load(m0, (int64_t)kt0 * FFMA_BK, tid + SG_THREADS * h, ra[h]);
+      lb.load(n0, (int64_t)kt0 * FFMA_BK, tid + SG_THREADS * h, rb[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      la.store(As[0], tid + SG_THREADS * h, ra[h]);
+      lb.store(Bs[0], tid + SG_THREADS * h, rb[h]);
+    }
   }
   __syncthreads();
 
   int buf = 0;
-  for (int kt = 0; kt < nkt; ++kt) {
-    const bool more = kt + 1 < nkt;
+  for (int kt = kt0; kt < kt1; ++kt) {
+    const bool more = kt + 1 < kt1;
     if (more) {
-      la.load(m0, (int64_t)(kt + 1) * FFMA_BK, tid, ra);
-      lb.load(n0, (int64_t)(kt + 1) * FFMA_BK, tid, rb);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        la.load(m0, (int64_t)(kt + 1) * FFMA_BK, tid + SG_THREADS * h, ra[h]);
+        lb.load(n0, (int64_t)(kt + 1) * FFMA_BK, tid + SG_THREADS * h, rb[h]);
+      }
     }
     const float* as = As[buf];
     const float* bs = Bs[buf];
@@ -162,96 +229,88 @@ __global__ void __launch_bounds__(SG_THREADS, GEMM_FFMA_MINB) ffma_sgemm_kernel(
     for (int kk = 0; kk < FFMA_BK; ++kk) {
       const float4 a0 = *reinterpret_cast<const float4*>(&as[kk * SG_LDS + ty * 4]);
       const float4 a1 = *reinterpret_cast<const float4*>(&as[kk * SG_LDS + 64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + 64 + tx * 4]);
+      float4 b[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4*>(&bs[kk * SG_LDS + tx * 4 + 32 * j]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#if GEMM_FFMA_PAIRED
-      const uint64_t b2[4] = {pack2(b0.x, b0.y), pack2(b0.z, b0.w), pack2(b1.x, b1.y), pack2(b1.z, b1.w)};
+      uint64_t b2[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        b2[2 * j] = pack2(b[j].x, b[j].y);
+        b2[2 * j + 1] = pack2(b[j].z, b[j].w);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint64_t ai = pack2(a[i], a[i]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ffma2(acc2[i][q], ai, b2[q]);
+        for (int q = 0; q < 8; ++q) ffma2(acc2[i][q], ai, b2[q]);
       }
-#else
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-#endif
     }
     if (more) {
-      la.store(As[buf ^ 1], tid, ra);
-      lb.store(Bs[buf ^ 1], tid, rb);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        la.store(As[buf ^ 1], tid + SG_THREADS * h, ra[h]);
+        lb.store(Bs[buf ^ 1], tid + SG_THREADS * h, rb[h]);
+      }
     }
     __syncthreads();
     buf ^= 1;
   }
 
-#if GEMM_FFMA_PAIRED
-  float acc[8][8];
+  if (part >= 0) {
+    // A part of a tail tile: its raw fp32 sums, 128 x 128 row-major per (tile, part).
+    float* w = p.ws + ((size_t)(tile - p.full_tiles) * p.split + part) * (FFMA_BM * FFMA_BN);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i) {
+      const int r = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) unpack2(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
-#endif
-  // Fused epilogue.  Thread rows: ty*4+i and 64+ty*4+i; columns tx*4+j and 64+tx*4+j.
-  const EpiParams& e = p.epi;
-  const EpiPtrs ptr = epi_ptrs(e, bz);
+      for (int j = 0; j < 4; ++j) {
+        float x[4];
+        unpack2(acc2[i][2 * j], x[0], x[1]);
+        unpack2(acc2[i][2 * j + 1], x[2], x[3]);
+        __stcg(reinterpret_cast<float4*>(w + r * FFMA_BN + 32 * j + tx * 4), make_float4(x[0], x[1], x[2], x[3]));
+      }
+    }
+    return;
+  }
+  // Fused epilogue.
+  const EpiPtrs ptr = epi_ptrs(p.epi, bz);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
     if (m >= p.M) continue;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t nb = n0 + h * 64 + tx * 4;
+    for (int j = 0; j < 4; ++j) {
+      const int64_t nb = n0 + 32 * j + tx * 4;
+      if (nb >= p.N) continue;
       float x[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) x[j] = acc[i][h * 4 + j] * e.alpha;
-      const bool full = nb + 4 <= p.N;
-      if (e.read_c) {
-        const int64_t off = m * e.ldc + nb;
-        if (full && e.vec_c && e.c_dtype == GEMM_F32) {
-          float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(ptr.C) + off);
-          if (e.c_relu) {
-            c.x = fmaxf(c.x, 0.0f); c.y = fmaxf(c.y, 0.0f); c.z = fmaxf(c.z, 0.0f); c.w = fmaxf(c.w, 0.0f);
-          }
-          x[0] = fmaf(e.beta, c.x, x[0]); x[1] = fmaf(e.beta, c.y, x[1]);
-          x[2] = fmaf(e.beta, c.z, x[2]); x[3] = fmaf(e.beta, c.w, x[3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (nb + j < p.N) {
-              float c = load_as_float(ptr.C, e.c_dtype, off + j);
-              if (e.c_relu) c = fmaxf(c, 0.0f);
-              x[j] = fmaf(e.beta, c, x[j]);
-            }
-        }
-      }
-      if (e.bias_mode == GEMM_BIAS_COL) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (nb + j < p.N) x[j] += load_as_float(ptr.bias, e.bias_dtype, nb + j);
-      } else if (e.bias_mode == GEMM_BIAS_ROW) {
-        const float b = load_as_float(ptr.bias, e.bias_dtype, m);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] += b;
-      }
-      if (e.relu) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = fmaxf(x[j], 0.0f);
-      }
-      const int64_t doff = m * e.ldd + nb;
-      if (full && e.vec_d && e.d_dtype == GEMM_F32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(ptr.D) + doff) = make_float4(x[0], x[1], x[2], x[3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (nb + j < p.N) store_float_as(ptr.D, e.d_dtype, doff + j, x[j]);
-      }
+      unpack2(acc2[i][2 * j], x[0], x[1]);
+      unpack2(acc2[i][2 * j + 1], x[2], x[3]);
+      ffma_finish4(p.epi, ptr, m, nb, p.N, x);
     }
   }
+}
+
+// The tail tiles' parts summed in part order (K order), then the fused epilogue;
+// one thread per four consecutive outputs of a tail tile.
+__global__ void __launch_bounds__(256) ffma_tail_reduce_kernel(const FfmaParams p) {
+  const int64_t tiles_n = (p.N + FFMA_BN - 1) / FFMA_BN;
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // float4 index over the tail tiles
+  constexpr int Q_PER_TILE = FFMA_BM * FFMA_BN / 4;
+  const int64_t t = q / Q_PER_TILE;
+  const int rem = (int)(q - t * Q_PER_TILE);
+  const int r = rem / (FFMA_BN / 4), c4 = (rem % (FFMA_BN / 4)) * 4;
+  const int64_t tile = p.full_tiles + t;
+  const int64_t m = (tile / tiles_n) * FFMA_BM + r;
+  const int64_t nb = (tile % tiles_n) * FFMA_BN + c4;
+  if (m >= p.M || nb >= p.N) return;
+  float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int part = 0; part < p.split; ++part) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+        p.ws + ((size_t)t * p.split + part) * (FFMA_BM * FFMA_BN) + r * FFMA_BN + c4));
+    x[0] += v.x; x[1] += v.y; x[2] += v.z; x[3] += v.w;
+  }
+  ffma_finish4(p.epi, epi_ptrs(p.epi, 0), m, nb, p.N, x);
 }
 
 // ============================ generic SIMT kernel ============================
@@ -450,16 +509,38 @@ cudaError_t launch_xf_stage(const void* src, void* dst, int64_t outer, int64_t i
   return cudaGetLastError();
 }
 
+int64_t ffma_tail_split(int64_t tiles, int64_t K, int sm_count, int* split) {
+  *split = 0;
+  const int64_t slots = (int64_t)std::max(1, sm_count) * FFMA_CTAS_PER_SM;
+  const int64_t nkt = (K + FFMA_BK - 1) / FFMA_BK;
+  if (tiles <= slots) return 0;
+  const int64_t rem = tiles % slots;
+  if (rem == 0 || 2 * rem > slots) return 0;
+  // Parts of at least 8 K slices each, at most 4 parts.
+  const int64_t s = std::min<int64_t>(std::min<int64_t>(slots / rem, 4), nkt / 8);
+  if (s < 2) return 0;
+  *split = (int)s;
+  return rem;
+}
+
 cudaError_t launch_ffma(const FfmaParams& p, int a_row_major, int b_row_major, int batch, cudaStream_t stream) {
   const int64_t tiles = ((p.N + FFMA_BN - 1) / FFMA_BN) * ((p.M + FFMA_BM - 1) / FFMA_BM);
   if (tiles > 0x7fffffffLL || batch < 1 || batch > 65535) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)tiles, (unsigned)batch);
+  const bool tail = p.full_tiles < tiles;
+  if (tail && (batch != 1 || p.split < 2 || p.ws == nullptr || p.kb_per_part < 1)) return cudaErrorInvalidValue;
+  const int64_t ctas = tail ? p.full_tiles + (tiles - p.full_tiles) * p.split : tiles;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)ctas, (unsigned)batch);
   // A row-major (T) is K-contiguous; B column-major (N) is K-contiguous.
   const bool ak = a_row_major != 0, bk = b_row_major == 0;
   if (ak && bk) ffma_sgemm_kernel<true, true><<<grid, SG_THREADS, 0, stream>>>(p);
   else if (ak) ffma_sgemm_kernel<true, false><<<grid, SG_THREADS, 0, stream>>>(p);
   else if (bk) ffma_sgemm_kernel<false, true><<<grid, SG_THREADS, 0, stream>>>(p);
   else ffma_sgemm_kernel<false, false><<<grid, SG_THREADS, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !tail) return e;
+  const int64_t quads = (tiles - p.full_tiles) * (FFMA_BM * FFMA_BN / 4);
+  ffma_tail_reduce_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

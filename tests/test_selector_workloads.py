@@ -47,7 +47,11 @@ def test_headline_8192_on_cta_pairs(layout):
 def test_workload_kernels(make, kernel, tile):
     cfg = select(make())
     assert cfg["kernel"] == kernel and (cfg["bm"], cfg["bn"]) == tile, cfg
-    assert cfg["sk_tiles"] == 0
+    if kernel == G.GEMM_KERNEL_FFMA:
+        # 1024 tiles on 2 x 152 CTA slots: a last wave of 112 tiles, split over K in two.
+        assert cfg["sk_tiles"] == 112 and cfg["split_k"] == 2 and cfg["grid"] == 912 + 224, cfg
+    else:
+        assert cfg["sk_tiles"] == 0
 
 
 @pytest.mark.parametrize("n,kernel,bn", [(512, G.GEMM_KERNEL_TC, 64), (1024, G.GEMM_KERNEL_TC, 64),
