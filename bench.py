@@ -353,6 +353,7 @@ def bench_ours(args, rank, world, local_rank):
         run_batched_suite(G, device)
         run_diag_suite(G, device)
         run_pair_suite(G, device)
+        run_transform_suite(G, device)
     plan.close()
     if dist:
         dist.destroy_process_group()
@@ -572,6 +573,78 @@ def run_suite(G, device, warmup=3, iters=20):
         print(json.dumps(rec), flush=True)
         plan.close()
         del A, B, C, D, bias, flush
+        torch.cuda.empty_cache()
+
+
+def run_transform_suite(G, device, iters=10):
+    """Operand transforms after load (t(x) = act(scale * x) on A and/or B): each
+    workload graph-timed without transforms, with them on the selector's path,
+    and forced inside the kernel / staged (GEMM_XF_STAGE=0 / 1).  One JSON line
+    per workload."""
+    import torch
+    from dense_gemm_epilogues_gb300 import inputs as I
+    cases = [("fc_relu_x", I.fc_bf16_8192x4096x11008(), dict(a_act=G.GEMM_ACT_RELU)),
+             ("gemm8192_tn_relu_a_scale_b", I.square_fp16_8192("TN").with_(beta=0.0, c=None),
+              dict(a_act=G.GEMM_ACT_RELU, b_scale=0.5)),
+             ("gemm2048_relu_a", I.square_fp16(2048), dict(a_act=G.GEMM_ACT_RELU)),
+             ("skinny_relu_a", I.skinny_fp16_16384x64x16384(), dict(a_act=G.GEMM_ACT_RELU))]
+    for name, p, xf in cases:
+        inp = I.generate(p, I.BASE_SEED + 30)
+        A, B = inp.A.to(device), inp.B.to(device)
+        C = inp.C.to(device) if inp.C is not None else None
+        bias = inp.bias.to(device) if inp.bias is not None else None
+        D = torch.empty((p.M, p.ldd), dtype=I.TORCH_DTYPES[p.d], device=device)
+        plan = G.Plan(G.DTYPE_CODES[p.ab], G.DTYPE_CODES[p.c or "f32"], device.index or 0)
+        bm = {"none": G.GEMM_BIAS_NONE, "col": G.GEMM_BIAS_COL, "row": G.GEMM_BIAS_ROW}[p.bias_mode]
+
+        def graph_us(epi):
+            side = torch.cuda.Stream(device)
+
+            def call():
+                G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M, p.N, p.K,
+                           p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                           C.data_ptr() if C is not None else None, p.ldc if C is not None else 0,
+                           D.data_ptr(), p.ldd, epi, side.cuda_stream)
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    call()
+                side.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                gr.capture_begin()
+                for _ in range(iters):
+                    call()
+                gr.capture_end()
+                gr.replay()
+                side.synchronize()
+                g0 = torch.cuda.Event(enable_timing=True)
+                g1 = torch.cuda.Event(enable_timing=True)
+                g0.record(side)
+                gr.replay()
+                g1.record(side)
+            side.synchronize()
+            return round(g0.elapsed_time(g1) * 1e3 / iters, 2), plan.last_config()
+
+        def epi_of(**kw):
+            return G.make_epilogue(G.DTYPE_CODES[p.d], bias.data_ptr() if bias is not None else 0,
+                                   G.DTYPE_CODES[p.bias] if p.bias else G.GEMM_F32, bm,
+                                   G.GEMM_ACT_RELU if p.act == "relu" else G.GEMM_ACT_NONE, **kw)
+        rec = {"transform_suite": name, "M": p.M, "N": p.N, "K": p.K, "transform": {
+            k: v for k, v in xf.items()}}
+        rec["plain_us"], _ = graph_us(epi_of())
+        old_env = os.environ.pop("GEMM_XF_STAGE", None)
+        rec["default_us"], cfg = graph_us(epi_of(**xf))
+        rec["default_path"] = "staged" if cfg["xf_staged"] else "in_kernel"
+        for v, key in (("0", "in_kernel_us"), ("1", "staged_us")):
+            os.environ["GEMM_XF_STAGE"] = v
+            rec[key], _ = graph_us(epi_of(**xf))
+        os.environ.pop("GEMM_XF_STAGE", None)
+        if old_env is not None:
+            os.environ["GEMM_XF_STAGE"] = old_env
+        rec["kernel"] = cfg["kernel_name"]
+        rec["status"] = plan.device_status()
+        print(json.dumps(rec), flush=True)
+        plan.close()
+        del A, B, C, D, bias
         torch.cuda.empty_cache()
 
 
