@@ -618,6 +618,10 @@ gemm_status_t launch_tc_problem(gemm_plan* plan, const gemm_config_t& cfg, gemm_
     tp.sk_partials = static_cast<float*>(plan->sk1_ws);
     tp.sk_flags = reinterpret_cast<int32_t*>(static_cast<char*>(plan->sk1_ws) + part_bytes);
   }
+  // K rotation for a single tile column (whole floating tiles only; GEMM_TC_KROT=0 off).
+  tp.k_rotate = (tp.tiles_n == 1 && tp.tiles_m > 1 && chunk_kb == 0 && tp.sk_first_tile == tp.num_tiles) ? 1 : 0;
+  if (const char* env = std::getenv("GEMM_TC_KROT"))
+    if (std::atoi(env) == 0) tp.k_rotate = 0;
   return launch_tc(tp, bn, cfg.grid, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

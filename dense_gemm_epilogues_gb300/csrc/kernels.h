@@ -29,6 +29,7 @@ struct TcParams {
   uint32_t idesc_half;    // CTA-pair kernel: the same for half-tile units (N = 128)
   int32_t half_first_tile;  // CTA-pair kernel: tiles from here on run as two column halves (num_tiles: none)
   int32_t chunk_kb;       // > 0: exact integer mode, K blocks per fp32 chunk
+  int32_t k_rotate;       // single-CTA kernel, one tile column: rotate each tile's K start (see tc_kernel.cu)
   LoadXf xf;              // transforms of the staged A / B tiles (launched as a separate kernel instance)
   EpiParams epi;
   int32_t* err;

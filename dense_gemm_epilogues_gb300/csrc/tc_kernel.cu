@@ -212,6 +212,12 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
         tile_coords(t, p, bz, tm, tn);
         const int m0 = tm * TC_BM, n0 = tn * BN;
         const int za = p.a_batched ? bz : 0, zb = p.b_batched ? bz : 0;
+        // One tile column (every tile streams its own rows of A once, all share B):
+        // tile t loads its K blocks starting at one of 8 evenly spaced blocks and
+        // wraps around, so the CTAs' concurrent reads of A spread over DRAM instead
+        // of all reading the same K columns at once.  The MMAs consume the stages in
+        // order; only the summation order of K changes.
+        const int rot = p.k_rotate ? (int)(((int64_t)(t & 7) * p.num_kb) >> 3) : 0;
         for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += Cfg::SLABS) {
           // A unit of the exact integer mode spans an even number of K blocks, so
           // stages never straddle two units.
@@ -223,7 +229,9 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
           for (int sl = 0; sl < nsl; ++sl) {
           const uint32_t sa = st + (uint32_t)(sl * Cfg::A_BYTES);
           const uint32_t sb = st + (uint32_t)(Cfg::SLABS * Cfg::A_BYTES + sl * Cfg::B_BYTES);
-          const int k0 = (kb0 + sl) * TC_BK;
+          int kp = kb0 + sl + rot;
+          if (kp >= p.num_kb) kp -= p.num_kb;
+          const int k0 = kp * TC_BK;
           if (p.a_mn_major) {
 #pragma unroll
             for (int h = 0; h < TC_BM / MN_BOX; ++h)

@@ -32,3 +32,26 @@ def test_single_tile_column_all_layouts(layout):
     p = H.tma_aligned(I.Problem("skinny_lay", "bf16", layout[0], layout[1], 2000, 64, 2000, beta=-1.0,
                                 c="bf16", d="bf16"))
     H.run_and_check_full(p, 171, expect_kernel=G.GEMM_KERNEL_TC)
+
+
+@pytest.mark.parametrize("krot", ["on", "off"])
+@pytest.mark.parametrize("layout", ["TN", "NT"])
+def test_k_rotation_small_integers_bit_exact(krot, layout, monkeypatch):
+    """With one tile column each tile starts its K loop at one of 8 evenly spaced
+    K blocks and wraps around (a permutation of the K blocks: 19 blocks, the
+    ragged last one landing mid-loop for most tiles).  Small integers keep every
+    sum exact, so rotated and unrotated runs both equal the oracle bit for bit."""
+    import numpy as np
+    import torch
+    monkeypatch.setenv("GEMM_TC_KROT", "1" if krot == "on" else "0")
+    p = H.tma_aligned(I.Problem("skinny_rot", "f16", layout[0], layout[1], 128 * 12, 64, 64 * 18 + 40, alpha=2.0,
+                                beta=1.0, c="f32", dist_a=I.Dist("small", -3, 3), dist_b=I.Dist("small", -3, 3),
+                                dist_c=I.Dist("small", -50, 50)))
+    inp = I.generate(p, 172)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0 and plan.last_config()["kernel"] == G.GEMM_KERNEL_TC
+    np.testing.assert_array_equal(dp.result().cpu().numpy(), H.oracle_full(inp))
+    plan.close()
