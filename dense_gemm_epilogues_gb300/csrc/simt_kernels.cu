@@ -1,17 +1,11 @@
 // simt_kernels.cu -- CUDA-core kernels of the library (sm_103a):
-//   * ffma_sgemm_kernel: fp32 SGEMM, register-blocked FFMA, double-buffered
-//     shared memory, fused epilogue;
+//   * ffma_sgemm_kernel: fp32 SGEMM, register-blocked paired FFMA, double-
+//     buffered shared memory, fused epilogue (see the kernel for its tiling),
+//     and ffma_tail_reduce_kernel, which finishes a last wave split over K;
 //   * simt_gemm_kernel: the generic path for every type, layout and alignment
 //     (and K == 0), used where TMA cannot describe the operands;
+//   * xf_stage_kernel: the operand-transform staging pass of 16-bit operands;
 //   * s8_to_f16_kernel: the int8 -> fp16 staging copy of the exact int8 path.
-//
-// The SGEMM follows the hierarchy of the CUTLASS page ("Thread Block Tile",
-// "Warp Tile", "Thread Tile", "Software Pipelining"): a 128x128 block tile
-// over 256 threads, each thread accumulating an 8x8 register tile from 8x1 and
-// 1x8 fragments of A and B in shared memory (outer products, K innermost per
-// tile), with global loads for the next K slice in flight while the current
-// slice is multiplied, and two shared-memory buffers so that one
-// __syncthreads() per K slice suffices.
 #include "kernels.h"
 
 namespace gemmlib {
