@@ -192,3 +192,26 @@ def test_diag_argument_errors():
                         G.make_epilogue(G.GEMM_S32))
     assert e.value.status == G.GEMM_ERR_UNSUPPORTED
     p8.close()
+
+
+def test_diag_tma_kernel_bounded_wait_reports_timeout():
+    """A wait bound far below the kernel's run time makes the TMA-staged kernel's
+    waits expire: it records GEMM_ERR_TIMEOUT, its producer drains the copies in
+    flight, and the same context then runs the problem correctly."""
+    p = I.DiagProblem("diag_tmo", "f16", "left", "T", 4096, 4096, beta=0.5, c="f32")
+    dinp = I.generate_diag(p, 450)
+    dd = H.DeviceDiag(dinp)
+    plan = H.make_diag_plan(p)
+    G.gemm_plan_set_timeout(plan.handle, 200)       # 200 ns
+    dd.run(plan)
+    torch.cuda.synchronize()
+    assert plan.last_config()["stages"] == 6
+    assert plan.device_status() == G.GEMM_ERR_TIMEOUT
+    G.gemm_plan_set_timeout(plan.handle, 4_000_000_000)
+    dd.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    rows, cols = H.sample_entries(p.M, p.N, 2000, 451, 64, 64)
+    got = dd.result()[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    H.check_close(got, H.oracle_entries(H.dense_inputs_of(dinp), rows, cols), p.d, "after timeout")
+    plan.close()

@@ -262,3 +262,25 @@ def test_paths_without_transforms_refuse_them(clean_env):
                            dev.data_ptr(), 16, dev.data_ptr(), 16, 0.0, None, 0, out.data_ptr(), 16, epi, stream)
     assert e.value.status == G.GEMM_ERR_UNSUPPORTED
     plan.close()
+
+
+@pytest.mark.parametrize("kernel", [G.GEMM_KERNEL_TC, G.GEMM_KERNEL_TC_PAIR], ids=["cta1", "pair"])
+def test_transform_warps_bounded_wait_reports_timeout(kernel, clean_env):
+    """With the transforms inside the kernel and a 200 ns wait bound, the waits
+    of the transform warps and of the MMA thread expire: the kernel records
+    GEMM_ERR_TIMEOUT and winds down; the context then runs correctly."""
+    clean_env.setenv("GEMM_XF_STAGE", "0")
+    p = I.Problem("xf_tmo", "f16", "T", "N", 512, 512, 4096, a_act="relu", b_scale=0.5)
+    inp = I.generate(p, 313)
+    dp = H.DeviceProblem(inp)
+    plan = H.make_plan(p, kernel)
+    G.gemm_plan_set_timeout(plan.handle, 200)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == G.GEMM_ERR_TIMEOUT
+    G.gemm_plan_set_timeout(plan.handle, 4_000_000_000)
+    dp.run(plan)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0 and plan.last_config()["xf_staged"] == 0
+    H.check_close(dp.result(), H.oracle_full(inp), "f32", "after timeout")
+    plan.close()
