@@ -114,3 +114,17 @@ def test_noalloc_expired_wait_is_reported_and_context_survives():
     assert G.gemm_noalloc_device_status() == 0
     dp.check_guards()
     H.check_close(dp.result(), H.oracle_full(inp), "s32", "no-alloc after an expired wait")
+
+
+def test_noalloc_operand_transforms():
+    """The operand transform of int8 problems (ReLU on A and/or B) applies here as
+    for gemm_run: in the staging pass, exact."""
+    p = PROBLEMS[0].with_(name="noalloc_relu", a_act="relu", b_act="relu")
+    inp = I.generate(p, 320)
+    dp = H.DeviceProblem(inp)
+    assert G.gemm_noalloc_device_status() == 0
+    _noalloc_run(dp)
+    torch.cuda.synchronize()
+    assert G.gemm_noalloc_device_status() == 0
+    dp.check_guards()
+    H.check_close(dp.result(), H.oracle_full(inp), "s32", "no-alloc with ReLU on A and B")
