@@ -148,14 +148,17 @@ typedef struct {
     int32_t bm, bn, bk;   /* CTA tile (rows of D, columns of D, K per pipeline stage) */
     int32_t stages;       /* shared-memory pipeline depth */
     int32_t cta_group;    /* CTAs cooperating on one MMA tile (1 or 2) */
-    int32_t split_k;      /* most K segments any tile is split into (1 = no split) */
+    int32_t split_k;      /* most K segments any tile is split into (1 = no split); FFMA kernel:
+                             the parts of each split tail tile (see sk_tiles) */
     int32_t raster;       /* tile rows per raster group (L2 reuse) */
     int32_t grid;         /* CTAs launched */
     int32_t k_chunk;      /* int8 path: K elements per exact fp32 chunk; 0 otherwise */
     int32_t tiles;        /* output tiles */
     int32_t sk_tiles;     /* stream-K tiles: their K blocks are shared out over all CTAs
-                             (single-CTA kernel) or CTA pairs of the launch; 0 = every tile
-                             runs whole on one CTA or CTA pair */
+                             (single-CTA kernel) or CTA pairs of the launch; FFMA kernel: the
+                             tiles of a last wave at most half full, each split over K into
+                             split_k parts that a reduction pass adds in K order; 0 = every
+                             tile runs whole on one CTA or CTA pair */
     int32_t cluster;      /* CTAs per thread-block cluster: 1, or 2 (one CTA pair) */
     int32_t half_tiles;   /* CTA-pair kernel: the last half_tiles tiles (a partial last wave
                              of at most half the CTA pairs) each run as two units of 256 x 128,
