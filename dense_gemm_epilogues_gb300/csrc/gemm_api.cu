@@ -10,8 +10,11 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <cstdio>
 #include <mutex>
 #include <new>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "kernels.h"
 
@@ -50,6 +53,47 @@ namespace {
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;   // tile indices and TMA coordinates are 32-bit
 constexpr int kHostMaxPanels = 16;           // gemm_run_host: most row panels of its copy pipeline
+
+// NVTX range around a public entry point (a profiler's timeline shows each call;
+// without a tool attached a push or pop costs a predictable branch).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// GEMM_LOG=1: every launch prints the configuration it runs to stderr.
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GEMM_LOG");
+    return v != nullptr && std::atoi(v) != 0;
+  }();
+  return on;
+}
+
+const char* kernel_label(int k) {
+  switch (k) {
+    case GEMM_KERNEL_NONE: return "none";
+    case GEMM_KERNEL_TC: return "tc";
+    case GEMM_KERNEL_TC_INT8: return "tc_int8";
+    case GEMM_KERNEL_FFMA: return "ffma";
+    case GEMM_KERNEL_SIMT: return "simt";
+    case GEMM_KERNEL_TC_PAIR: return "tc_pair";
+    case GEMM_KERNEL_DIAG: return "diag";
+    default: return "?";
+  }
+}
+
+void log_config(const char* entry, int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_config_t& c) {
+  if (!log_enabled()) return;
+  std::fprintf(stderr,
+               "gemm: %s M=%lld N=%lld K=%lld batch=%lld kernel=%s tile=%dx%dx%d stages=%d cta_group=%d grid=%d "
+               "tiles=%d split_k=%d sk_tiles=%d half_tiles=%d k_chunk=%d xf_staged=%d\n",
+               entry, (long long)M, (long long)N, (long long)K, (long long)batch, kernel_label(c.kernel), c.bm, c.bn,
+               c.bk, c.stages, c.cta_group, c.grid, c.tiles, c.split_k, c.sk_tiles, c.half_tiles, c.k_chunk,
+               c.xf_staged);
+}
 
 bool is_f16ish(int t) { return t == GEMM_F16 || t == GEMM_BF16; }
 bool is_float_out(int t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
@@ -1074,7 +1118,10 @@ gemm_status_t run_impl(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
       break;
     }
   }
-  if (s == GEMM_OK) plan->last = cfg;
+  if (s == GEMM_OK) {
+    plan->last = cfg;
+    log_config("run", M, N, K, bt.count, cfg);
+  }
   return s;
 }
 
@@ -1100,6 +1147,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb, int
                        const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
                        gemm_stream_t stream) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
+  NvtxRange range("gemm_run");
   gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
   return run_impl(plan, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi, stream, Batch());
@@ -1112,6 +1160,7 @@ gemm_status_t gemm_run_strided_batched(gemm_plan_t plan, gemm_layout_t la, gemm_
                                        int64_t ldd, int64_t stride_d, int64_t batch,
                                        const gemm_epilogue_t* epi, int64_t stride_bias, gemm_stream_t stream) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
+  NvtxRange range("gemm_run_strided_batched");
   gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
   if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0 || stride_d < 0 || stride_bias < 0)
@@ -1154,6 +1203,7 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx
                             const void* C, int64_t ldc, void* D, int64_t ldd, const gemm_epilogue_t* epi,
                             gemm_stream_t stream_) {
   if (!plan || (side != GEMM_SIDE_LEFT && side != GEMM_SIDE_RIGHT)) return GEMM_ERR_INVALID_ARG;
+  NvtxRange range("gemm_run_diag");
   const bool left = side == GEMM_SIDE_LEFT;
   // The checks of the equivalent dense call (the diagonal as a square operand).
   gemm_status_t s =
@@ -1226,6 +1276,7 @@ gemm_status_t gemm_run_diag(gemm_plan_t plan, gemm_side_t side, gemm_layout_t lx
   cfg.grid = grid;
   cfg.tiles = (int32_t)std::min<int64_t>(p.num_tiles, kMaxDim);
   plan->last = cfg;
+  log_config("diag", M, N, left ? M : N, 1, cfg);
   return GEMM_OK;
 }
 
@@ -1234,6 +1285,7 @@ gemm_status_t gemm_run_complex(gemm_plan_t plan, gemm_unit_t unit, gemm_layout_t
                                const void* B, int64_t ldb, double beta, const void* C, int64_t ldc, void* D,
                                int64_t ldd, const gemm_epilogue_t* epi, gemm_stream_t stream_) {
   if (!plan || (unit != GEMM_UNIT_IMAGINARY && unit != GEMM_UNIT_DUAL)) return GEMM_ERR_INVALID_ARG;
+  NvtxRange range("gemm_run_complex");
   // The argument checks of gemm_run, in pairs.
   gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
@@ -1289,6 +1341,7 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, gemm_layout_t la, gemm_layout_t lb
                             double beta, const void* C, int64_t ldc, void* D, int64_t ldd,
                             const gemm_epilogue_t* epi, gemm_stream_t stream_) {
   if (!plan) return GEMM_ERR_INVALID_ARG;
+  NvtxRange range("gemm_run_host");
   gemm_status_t s = validate(plan->ab, plan->c, la, lb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, epi);
   if (s != GEMM_OK) return s;
   if (M == 0 || N == 0) return GEMM_OK;

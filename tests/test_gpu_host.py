@@ -67,3 +67,21 @@ def test_host_panels_int8_exact():
     inp = I.generate(p, 720)
     D = _host_run(p, inp)
     H.check_close(D[:, :p.N], H.oracle_full(inp), "s32", p.name)
+
+
+def test_gemm_log_prints_the_configuration():
+    """GEMM_LOG=1 (read once per process): every launch prints the configuration
+    it runs to stderr -- checked in a child process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import torch, dense_gemm_epilogues_gb300 as G\n"
+            "a = torch.randn(1024, 512, device='cuda', dtype=torch.float16)\n"
+            "b = torch.randn(512, 768, device='cuda', dtype=torch.float16)\n"
+            "G.matmul(a, b); torch.cuda.synchronize()\n")
+    env = dict(os.environ, GEMM_LOG="1", PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = [l for l in r.stderr.splitlines() if l.startswith("gemm: run ")]
+    assert len(line) == 1 and "M=1024 N=768 K=512" in line[0] and "kernel=tc" in line[0], r.stderr
