@@ -59,9 +59,9 @@ def _check_whole(p: I.Problem, seed: int, expect_kernel):
     return cfg
 
 
-def _check_boundaries(p: I.Problem, seed: int, expect_kernel, kernel=None):
+def _check_boundaries(p: I.Problem, seed: int, expect_kernel, kernel=None, row_block=128, col_block=64):
     inp, dp, cfg = _run(p, seed, expect_kernel, kernel)
-    rows, cols = H.boundary_entries(p.M, p.N, 128, 64)
+    rows, cols = H.boundary_entries(p.M, p.N, row_block, col_block)
     r2, c2 = H.sample_entries(p.M, p.N, N_SAMPLES, seed, cfg["bm"] or 128, cfg["bn"] or 128)
     rows, cols = np.concatenate([rows, r2]), np.concatenate([cols, c2])
     ref = H.oracle_entries(inp, rows, cols)
@@ -119,3 +119,21 @@ def test_skinny_fp16_whole():
     p = I.skinny_fp16_16384x64x16384()
     cfg = H.run_and_check_full(p, I.BASE_SEED + 6)
     assert cfg["kernel"] in TC_ANY
+
+
+def test_fc_relu_on_x_staged_at_full_size():
+    """The FC layer with ReLU applied to X after load: X is re-read by 43 tile
+    columns, so the selector stages the transform; whole rows and columns at
+    both edges of every 256 x 256 pair tile against the oracle (its transformed
+    path is slower, so the blocks are the pair tiles rather than 128 x 64)."""
+    p = I.fc_bf16_8192x4096x11008().with_(name="fc_relu_x", a_act="relu")
+    cfg = _check_boundaries(p, I.BASE_SEED + 2, G.GEMM_KERNEL_TC_PAIR, row_block=256, col_block=256)
+    assert cfg["xf_staged"] == G.GEMM_XF_A
+
+
+def test_skinny_relu_on_a_in_kernel():
+    """The skinny GEMM with ReLU on A (A read by one tile column): the transform
+    runs inside the kernel; block-edge rows and columns against the oracle."""
+    p = I.skinny_fp16_16384x64x16384().with_(name="skinny_relu_a", a_act="relu", b_scale=0.5)
+    cfg = _check_boundaries(p, I.BASE_SEED + 6, TC_ANY)
+    assert cfg["xf_staged"] == 0
