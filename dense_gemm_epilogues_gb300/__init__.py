@@ -322,11 +322,15 @@ class Plan:
 
 def matmul(a, b, *, c=None, alpha: float = 1.0, beta: float = 0.0, bias=None,
            bias_mode: int = GEMM_BIAS_COL, relu: bool = False, out=None, out_dtype=None,
-           plan: Optional[Plan] = None, stream=None):
-    """D = epilogue(alpha * a @ b + beta * c) on the GPU for CUDA tensors.
+           plan: Optional[Plan] = None, stream=None, c_relu: bool = False,
+           a_relu: bool = False, a_scale: float = 1.0, b_relu: bool = False, b_scale: float = 1.0):
+    """D = epilogue(alpha * t_A(a) @ t_B(b) + beta * c_act(c)) on the GPU for CUDA tensors.
 
     a: M x K view, b: K x N view (each with unit stride along one dimension;
-    the stride decides N/T).  c, out: row-major M x N.  Returns `out`."""
+    the stride decides N/T).  c, out: row-major M x N.  relu / c_relu: ReLU on
+    the result / on c as it is read.  a_relu, a_scale (b_relu, b_scale): the
+    operand transform t(x) = relu?(scale * x) applied to a (b) after load.
+    Returns `out`."""
     import torch
     M, K = a.shape
     K2, N = b.shape
@@ -348,7 +352,10 @@ def matmul(a, b, *, c=None, alpha: float = 1.0, beta: float = 0.0, bias=None,
     epi = make_epilogue(_torch_code(out), bias.data_ptr() if bias is not None else 0,
                         _torch_code(bias) if bias is not None else GEMM_F32,
                         bias_mode if bias is not None else GEMM_BIAS_NONE,
-                        GEMM_ACT_RELU if relu else GEMM_ACT_NONE)
+                        GEMM_ACT_RELU if relu else GEMM_ACT_NONE,
+                        GEMM_ACT_RELU if c_relu else GEMM_ACT_NONE,
+                        a_act=GEMM_ACT_RELU if a_relu else GEMM_ACT_NONE, a_scale=a_scale,
+                        b_act=GEMM_ACT_RELU if b_relu else GEMM_ACT_NONE, b_scale=b_scale)
     cp, ldc = (c.data_ptr(), c.stride(0)) if (c is not None and beta != 0.0) else (None, 0)
     gemm_run(plan.handle, la, lb, M, N, K, alpha, a.data_ptr(), lda, b.data_ptr(), ldb, beta, cp,
              ldc, out.data_ptr(), out.stride(0), epi, stream)

@@ -284,3 +284,17 @@ def test_transform_warps_bounded_wait_reports_timeout(kernel, clean_env):
     assert plan.device_status() == 0 and plan.last_config()["xf_staged"] == 0
     H.check_close(dp.result(), H.oracle_full(inp), "f32", "after timeout")
     plan.close()
+
+
+def test_matmul_helper_transforms_equal_pretransformed_operands(clean_env):
+    """The Python helper's operand transforms: relu(0.5 * a) and relu(b) given as
+    transforms give the same bits as the product of the operands transformed
+    beforehand in fp16 (one rounding of the exact fp16 product either way)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(314)
+    a = torch.randn(1024, 512, device="cuda", generator=g).half()
+    b = torch.randn(512, 768, device="cuda", generator=g).half()
+    got = G.matmul(a, b, a_relu=True, a_scale=0.5, b_relu=True)
+    want = G.matmul(torch.relu(a * 0.5), torch.relu(b))
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
