@@ -27,7 +27,8 @@
  *   - All sizes and leading dimensions are in elements, not bytes.
  *   - Device pointers (gemm_run) and the stream are owned by the caller; the
  *     library never frees them.  A plan owns only its own device scratch
- *     (an error word, and the int8 operand staging described at gemm_run).
+ *     (an error word, and the staging and partial-sum buffers described at
+ *     gemm_run).
  *   - gemm_run is asynchronous on `stream`: its return value reports argument
  *     and launch errors only.  Device-side failures surface at the caller's
  *     stream synchronisation or through gemm_plan_device_status.
@@ -206,11 +207,14 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
  * Kernel choice: 16-byte aligned A/B with 16-byte multiple strides use the
  * tcgen05 tensor-core kernel (S8: an int8->fp16 staging pass into plan-owned
  * device scratch, grown on demand with stream-ordered allocation, then the
- * tensor-core kernel in exact K-chunks); F32 uses the FFMA kernel; anything
- * else uses the generic CUDA-core kernel.  All paths run on the GPU.
+ * tensor-core kernel in exact K-chunks); F32 uses the FFMA kernel (a last
+ * wave at most half full is split over K, its partial sums in plan scratch);
+ * anything else uses the generic CUDA-core kernel.  Staged operand transforms
+ * (see gemm_epilogue_t) also write plan scratch.  All paths run on the GPU.
  * Errors: GEMM_ERR_INVALID_ARG / GEMM_ERR_UNSUPPORTED before any launch;
  * GEMM_ERR_CUDA when a launch or scratch allocation fails.
- * A plan's device scratch (int8 staging, stream-K partials, host staging) is
+ * A plan's device scratch (int8 and operand-transform staging, stream-K and
+ * split-tail partials, host staging) is
  * reused by every call: calls that use one plan from several streams or host
  * threads at once race on it; use one plan per concurrent stream.
  * Stream-K (environment GEMM_STREAM_K=1, off by default) lets CTA pairs of one
