@@ -208,9 +208,29 @@ def measured_counters() -> dict:
         out = {"traffic": float(kv["dram_bytes_per_launch"])}
         if "tensor_pipe_active_pct" in kv:
             out["tensor_pipe_active_pct"] = float(kv["tensor_pipe_active_pct"])
+        for k in ("sm_cycles_active", "sm_clock_hz_under_ncu", "launch_us_under_ncu"):
+            if k in kv:
+                out[k] = float(kv[k])
         return out
     except (OSError, KeyError, ValueError):
         return {}
+
+
+def theoretical_at_clock(counters: dict, flops_per_launch: float, sms: int) -> dict:
+    """The second denominator: SMs x per-SM dense rate x the clock ncu saw.  The
+    per-SM rate is measured from the committed counters (flops per tensor-active
+    cycle per SM), the SM count read from the device.  None when the counters
+    are stale or absent."""
+    need = ("sm_cycles_active", "sm_clock_hz_under_ncu", "launch_us_under_ncu", "tensor_pipe_active_pct")
+    if not all(k in counters for k in need):
+        return None
+    busy = counters["sm_cycles_active"] * counters["tensor_pipe_active_pct"] / 100.0
+    per_sm_rate = flops_per_launch / sms / busy
+    peak = sms * per_sm_rate * counters["sm_clock_hz_under_ncu"] / 1e12
+    achieved = flops_per_launch / (counters["launch_us_under_ncu"] * 1e-6) / 1e12
+    return {"sms": sms, "flops_per_tensor_cycle_per_sm": round(per_sm_rate, 1),
+            "clock_ghz": round(counters["sm_clock_hz_under_ncu"] / 1e9, 4), "peak": round(peak, 1),
+            "achieved_under_ncu": round(achieved, 1), "frac": round(achieved / peak, 4), "unit": "TFLOP/s"}
 
 
 def measured_traffic():
@@ -319,10 +339,13 @@ def bench_ours(args, rank, world, local_rank):
                      for li, l in enumerate(LAYOUTS)}
     achieved = flops_per_gemm / avg_launch_s / 1e12
     peak, peak_source = choose_tensor_peak(peaks, clocks, total_ms / 1e3)
+    counters = measured_counters()
     roofline = {"bound": "tensor", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": measured_traffic(),
-                "tensor_pipe_active_pct": measured_counters().get("tensor_pipe_active_pct"),
+                "frac": round(achieved / peak, 4), "traffic": counters.get("traffic"),
+                "tensor_pipe_active_pct": counters.get("tensor_pipe_active_pct"),
+                "theoretical_at_ncu_clock": theoretical_at_clock(
+                    counters, flops_per_gemm, torch.cuda.get_device_properties(device).multi_processor_count),
                 "counters_source": "profiles/tc_pair_gemm_f16_8192_traffic.txt (ncu, TN launch; null once "
                                    "the kernel sources change)",
                 "peak_source": peak_source,

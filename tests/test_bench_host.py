@@ -59,3 +59,18 @@ def test_default_run_measures_every_other_workload():
     assert bounds["cfg5a_sgemm_f32_tn_4096_bias_relu"] == "alu"
     sweep = sorted(w[1].M for w in bench.config_workloads() if w[0].startswith("cfg5b"))
     assert sweep == [512, 1024, 2048, 4096, 16384]
+
+
+def test_theoretical_peak_at_the_ncu_clock():
+    """The second denominator from the committed counters: flops per
+    tensor-active cycle per SM (8192 for fp16 tcgen05 on GB300) times the SMs
+    and the clock ncu saw; the launch under ncu as a fraction of it matches the
+    tensor-pipe share."""
+    c = bench.measured_counters()
+    if "sm_cycles_active" not in c:
+        pytest.skip("counters stale for the current kernel sources")
+    t = bench.theoretical_at_clock(c, 2.0 * 8192 ** 3, 152)
+    assert abs(t["flops_per_tensor_cycle_per_sm"] - 8192) < 0.01 * 8192, t
+    assert 1900 < t["peak"] < 2100 and 0.8 < t["frac"] < 0.95, t
+    assert abs(t["frac"] - c["tensor_pipe_active_pct"] / 100.0) < 0.02, t
+    assert bench.theoretical_at_clock({}, 1.0, 152) is None
