@@ -417,6 +417,90 @@ __device__ __forceinline__ void st_row_32b(void* p, const uint32_t* w) {
   }
 }
 
+// epi_store_chunk32_sectors with D's type fixed at compile time.
+template <int DT>
+__device__ __forceinline__ void epi_store_chunk32_t(void* D, int64_t ldd, int64_t m0, int64_t M, int64_t n_base,
+                                                    const float (&x)[32], uint32_t stage) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();   // the previous chunk's reads of the buffer are done
+  if constexpr (DT == GEMM_F32) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)(lane * 128 + ((q ^ (lane & 7)) << 4))),
+                   "r"(__float_as_uint(x[4 * q])), "r"(__float_as_uint(x[4 * q + 1])),
+                   "r"(__float_as_uint(x[4 * q + 2])), "r"(__float_as_uint(x[4 * q + 3]))
+                   : "memory");
+    __syncwarp();
+    const int pl = lane & 7;
+    float* dst = static_cast<float*>(D) + (m0 + (lane >> 3)) * ldd + n_base + pl * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + (lane >> 3);
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(stage + (uint32_t)(r * 128 + ((pl ^ (r & 7)) << 4))) : "memory");
+      if (m0 + r < M) *reinterpret_cast<uint4*>(dst + (int64_t)(4 * i) * ldd) = v;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        if constexpr (DT == GEMM_F16) {
+          __half2 v = __floats2half2_rn(x[8 * q + 2 * h], x[8 * q + 2 * h + 1]);
+          w[h] = *reinterpret_cast<uint32_t*>(&v);
+        } else {
+          __nv_bfloat162 v = __floats2bfloat162_rn(x[8 * q + 2 * h], x[8 * q + 2 * h + 1]);
+          w[h] = *reinterpret_cast<uint32_t*>(&v);
+        }
+      }
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4))),
+                   "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                   : "memory");
+    }
+    __syncwarp();
+    const int pl = lane & 3;
+    uint16_t* dst = static_cast<uint16_t*>(D) + (m0 + (lane >> 2)) * ldd + n_base + pl * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 8 * i + (lane >> 2);
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(stage + (uint32_t)(r * 64 + ((pl ^ ((r >> 1) & 3)) << 4))) : "memory");
+      if (m0 + r < M) *reinterpret_cast<uint4*>(dst + (int64_t)(8 * i) * ldd) = v;
+    }
+  }
+}
+
+// The plain floating epilogue of one warp -- no beta*C, bias or ReLU, every
+// chunk inside D, D taking vector stores -- over chunks [c_begin, c_end) of its
+// rows (columns n0 + 32c ... n0 + 32c + 31; m0 = the warp's first row), with
+// D's type fixed at compile time, so that no chunk tests the epilogue's
+// parameters.  acc(c, x) fills x with alpha times chunk c's accumulator.
+template <int DT, typename Acc>
+__device__ __forceinline__ void epi_chunks_plain(void* D, int64_t ldd, int64_t m0, int64_t n0, int64_t M,
+                                                 uint32_t stage, int c_begin, int c_end, Acc& acc) {
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; ++c) {
+    float x[32];
+    acc(c, x);
+    epi_store_chunk32_t<DT>(D, ldd, m0, M, n0 + c * 32, x, stage);
+  }
+}
+
+// The plain epilogue applies: returns false (nothing done) otherwise.
+template <typename Acc>
+__device__ __forceinline__ bool epi_chunks_plain_any(const EpiParams& e, void* D, int64_t m0, int64_t n0, int64_t N,
+                                                     int64_t M, uint32_t stage, int c_begin, int c_end, Acc&& acc) {
+  if (e.read_c || e.bias_mode != GEMM_BIAS_NONE || e.relu || !e.vec_d || n0 + 32 * (int64_t)c_end > N) return false;
+  if (e.d_dtype == GEMM_F32) epi_chunks_plain<GEMM_F32>(D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
+  else if (e.d_dtype == GEMM_F16) epi_chunks_plain<GEMM_F16>(D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
+  else if (e.d_dtype == GEMM_BF16) epi_chunks_plain<GEMM_BF16>(D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
+  else return false;
+  return true;
+}
+
 // x[j] holds the exact int32 product sums of columns n_base..n_base+31 of row m;
 // it is finished in place (alpha, beta*C, bias, ReLU) and stored.  Called by all
 // 32 lanes of a warp together, as the floating version.

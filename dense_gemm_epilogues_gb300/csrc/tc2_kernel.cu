@@ -455,30 +455,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
             __syncwarp();
             if (!good) cp_last = cp_first - 1;   // results are void; the error word says why
           }
-#pragma unroll 1
-          for (int c = 0; c < chunks; ++c) {
+          const uint32_t stage_buf = out_stage0 + (uint32_t)((warp - 2) * 4096);
+          // A whole tile with the plain epilogue: the loop specialised on D's type.
+          auto acc = [&](int c, float (&x)[32]) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
             tmem_wait_ld();
-            float x[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-            for (int cp = cp_first; cp <= cp_last; ++cp) {
-              const float4* slot = reinterpret_cast<const float4*>(
-                  p.sk_partials + (size_t)(cp * 2 + (int)rank) * SLOT_FLOATS);
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
+          };
+          if (cp_last >= cp_first ||
+              !epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc)) {
+#pragma unroll 1
+            for (int c = 0; c < chunks; ++c) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+              tmem_wait_ld();
+              float x[32];
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 y = __ldcg(&slot[(c * 8 + v) * TC_BM + row_in_cta]);
-                x[4 * v] += y.x;
-                x[4 * v + 1] += y.y;
-                x[4 * v + 2] += y.z;
-                x[4 * v + 3] += y.w;
+              for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+              for (int cp = cp_first; cp <= cp_last; ++cp) {
+                const float4* slot = reinterpret_cast<const float4*>(
+                    p.sk_partials + (size_t)(cp * 2 + (int)rank) * SLOT_FLOATS);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  const float4 y = __ldcg(&slot[(c * 8 + v) * TC_BM + row_in_cta]);
+                  x[4 * v] += y.x;
+                  x[4 * v + 1] += y.y;
+                  x[4 * v + 2] += y.z;
+                  x[4 * v + 3] += y.w;
+                }
               }
-            }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] *= p.epi.alpha;
-            epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x,
-                                   out_stage0 + (uint32_t)((warp - 2) * 4096), p.M);
+              for (int j = 0; j < 32; ++j) x[j] *= p.epi.alpha;
+              epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x, stage_buf, p.M);
+            }
           }
           tc_fence_before();
           __syncwarp();

@@ -483,16 +483,26 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
         if (!warp_wait(tfull_bar(buf), apar, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
-#pragma unroll 1
-        for (int c = c0; c < c0 + CHUNKS; ++c) {
+        const uint32_t stage_buf = out_stage0 + (uint32_t)((warp - 2) * 4096);
+        // The plain epilogue: the loop specialised on D's type.
+        auto acc = [&](int c, float (&x)[32]) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
           tmem_wait_ld();
-          float x[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
-          epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x,
-                                 out_stage0 + (uint32_t)((warp - 2) * 4096), p.M);
+        };
+        if (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
+#pragma unroll 1
+          for (int c = c0; c < c0 + CHUNKS; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
+            epi_finish_row32_float(p.epi, ptr, m, row_ok, n0 + c * 32, p.N, x, stage_buf, p.M);
+          }
         }
         tc_fence_before();
         __syncwarp();
