@@ -289,17 +289,104 @@ __device__ __forceinline__ void epi_store_chunk32_sectors(const EpiParams& e, vo
   }
 }
 
+// beta * C added into a warp's 32 x 32 chunk (lane r: row m0 + r, x = its 32
+// values), with C read through the warp's shared buffer `stage`: each load
+// instruction reads whole rows of the chunk (4 rows x 128 bytes of fp32 C, 8 rows
+// x 64 bytes of 16-bit C) and the rows are turned around in the buffer (the
+// same XOR swizzle as the D stores), where a load of 16 bytes from each of 32
+// rows would touch 32 sectors per instruction.  ReLU on C if asked.  Rows at or
+// past M are not read.  Requires the 32 columns inside C and 16-byte aligned rows.
+__device__ __forceinline__ void epi_add_c_chunk32_turned(const EpiParams& e, const void* C, int64_t m0, int64_t M,
+                                                         int64_t n_base, float (&x)[32], uint32_t stage) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();   // the previous chunk's use of the buffer is done
+  if (e.c_dtype == GEMM_F32) {
+    const int pl = lane & 7;
+    const float* src = static_cast<const float*>(C) + (m0 + (lane >> 3)) * e.ldc + n_base + pl * 4;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (m0 + 4 * i + (lane >> 3) < M) v[i] = *reinterpret_cast<const uint4*>(src + (int64_t)(4 * i) * e.ldc);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + (lane >> 3);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)(r * 128 + ((pl ^ (r & 7)) << 4))),
+                   "r"(v[i].x), "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
+                   : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 c;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(c.x), "=f"(c.y), "=f"(c.z), "=f"(c.w)
+                   : "r"(stage + (uint32_t)(lane * 128 + ((q ^ (lane & 7)) << 4))) : "memory");
+      if (e.c_relu) {
+        c.x = fmaxf(c.x, 0.0f); c.y = fmaxf(c.y, 0.0f); c.z = fmaxf(c.z, 0.0f); c.w = fmaxf(c.w, 0.0f);
+      }
+      x[4 * q + 0] = fmaf(e.beta, c.x, x[4 * q + 0]);
+      x[4 * q + 1] = fmaf(e.beta, c.y, x[4 * q + 1]);
+      x[4 * q + 2] = fmaf(e.beta, c.z, x[4 * q + 2]);
+      x[4 * q + 3] = fmaf(e.beta, c.w, x[4 * q + 3]);
+    }
+  } else {
+    const int pl = lane & 3;
+    const uint16_t* src = static_cast<const uint16_t*>(C) + (m0 + (lane >> 2)) * e.ldc + n_base + pl * 8;
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (m0 + 8 * i + (lane >> 2) < M) v[i] = *reinterpret_cast<const uint4*>(src + (int64_t)(8 * i) * e.ldc);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 8 * i + (lane >> 2);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)(r * 64 + ((pl ^ ((r >> 1) & 3)) << 4))),
+                   "r"(v[i].x), "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
+                   : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(stage + (uint32_t)(lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4))) : "memory");
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float lo, hi;
+        if (e.c_dtype == GEMM_F16) {
+          __half2 hv = *reinterpret_cast<__half2*>(&w[h]);
+          lo = __low2float(hv); hi = __high2float(hv);
+        } else {
+          __nv_bfloat162 bv = *reinterpret_cast<__nv_bfloat162*>(&w[h]);
+          lo = __low2float(bv); hi = __high2float(bv);
+        }
+        if (e.c_relu) {
+          lo = fmaxf(lo, 0.0f);
+          hi = fmaxf(hi, 0.0f);
+        }
+        x[8 * q + 2 * h + 0] = fmaf(e.beta, lo, x[8 * q + 2 * h + 0]);
+        x[8 * q + 2 * h + 1] = fmaf(e.beta, hi, x[8 * q + 2 * h + 1]);
+      }
+    }
+  }
+}
+
 // x[j] holds alpha*acc for columns n_base..n_base+31 of row m.  Called by all
 // 32 lanes of a warp together (the bias is shared by shuffles); lanes whose row
 // is outside D (row_ok false) take part but neither read C nor store.
-// stage != 0: the warp's 4 KiB shared buffer for row-contiguous stores (used
-// when the 32 columns are inside D and its rows are 16-byte aligned); M is then
-// D's row count.
+// stage != 0: the warp's 4 KiB shared buffer for row-contiguous stores of D and
+// loads of C (each used when the 32 columns are inside the matrix and its rows
+// are 16-byte aligned); M is then D's (and C's) row count.
 __device__ __forceinline__ void epi_finish_row32_float(const EpiParams& e, const EpiPtrs& ptr, int64_t m,
                                                        bool row_ok, int64_t n_base, int64_t N, float (&x)[32],
                                                        uint32_t stage = 0, int64_t M = 0) {
   const bool full = n_base + 32 <= N;
-  if (e.read_c && row_ok) {
+  if (e.read_c && stage != 0 && full && e.vec_c) {
+    // All 32 lanes take part; rows outside C are not read.
+    epi_add_c_chunk32_turned(e, ptr.C, m - (threadIdx.x & 31), M, n_base, x, stage);
+  } else if (e.read_c && row_ok) {
     const int64_t off = m * e.ldc + n_base;
     if (full && e.vec_c) {
       if (e.c_dtype == GEMM_F32) {
