@@ -576,6 +576,20 @@ __device__ __forceinline__ void epi_chunks_plain(void* D, int64_t ldd, int64_t m
   }
 }
 
+// D = alpha * acc + beta * C with fp32 C and D and no bias or ReLU (the same
+// conditions on the chunks as the plain loop, and C read as whole rows).
+template <typename Acc>
+__device__ __forceinline__ void epi_chunks_c32(const EpiParams& e, const EpiPtrs& ptr, int64_t m0, int64_t n0,
+                                               int64_t M, uint32_t stage, int c_begin, int c_end, Acc& acc) {
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; ++c) {
+    float x[32];
+    acc(c, x);
+    epi_add_c_chunk32_turned(e, ptr.C, m0, M, n0 + c * 32, x, stage);
+    epi_store_chunk32_t<GEMM_F32>(ptr.D, e.ldd, m0, M, n0 + c * 32, x, stage);
+  }
+}
+
 // The plain epilogue applies: returns false (nothing done) otherwise.
 template <typename Acc>
 __device__ __forceinline__ bool epi_chunks_plain_any(const EpiParams& e, void* D, int64_t m0, int64_t n0, int64_t N,

@@ -492,7 +492,12 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
         };
-        if (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
+        const bool c32 = p.epi.read_c && p.epi.vec_c && p.epi.vec_d && p.epi.c_dtype == GEMM_F32 &&
+                         p.epi.d_dtype == GEMM_F32 && !p.epi.c_relu && p.epi.bias_mode == GEMM_BIAS_NONE &&
+                         !p.epi.relu && n0 + 32 * (c0 + CHUNKS) <= p.N;
+        if (c32) {
+          epi_chunks_c32(p.epi, ptr, m - lane, n0, p.M, stage_buf, c0, c0 + CHUNKS, acc);
+        } else if (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
 #pragma unroll 1
           for (int c = c0; c < c0 + CHUNKS; ++c) {
             uint32_t r[32];
