@@ -590,6 +590,50 @@ __device__ __forceinline__ void epi_chunks_c32(const EpiParams& e, const EpiPtrs
   }
 }
 
+// D = act(alpha * acc + bias[column]) with an fp32 column bias, no C, ReLU or
+// not (the fully connected layer's epilogue), D's type fixed at compile time.
+template <int DT, bool RELU, typename Acc>
+__device__ __forceinline__ void epi_chunks_bias(const EpiParams& e, const EpiPtrs& ptr, int64_t m0, int64_t n0,
+                                                int64_t M, uint32_t stage, int c_begin, int c_end, Acc& acc) {
+  const int lane = threadIdx.x & 31;
+  const float* bias = static_cast<const float*>(ptr.bias) + n0 + lane;
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; ++c) {
+    const float bl = bias[c * 32];   // lane j holds bias[n0 + 32c + j]; shared by shuffles
+    float x[32];
+    acc(c, x);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      x[j] += __shfl_sync(0xffffffffu, bl, j);
+      if constexpr (RELU) x[j] = fmaxf(x[j], 0.0f);
+    }
+    epi_store_chunk32_t<DT>(ptr.D, e.ldd, m0, M, n0 + c * 32, x, stage);
+  }
+}
+
+// The fully connected epilogue applies (see epi_chunks_bias): returns false otherwise.
+template <typename Acc>
+__device__ __forceinline__ bool epi_chunks_bias_any(const EpiParams& e, const EpiPtrs& ptr, int64_t m0, int64_t n0,
+                                                    int64_t N, int64_t M, uint32_t stage, int c_begin, int c_end,
+                                                    Acc&& acc) {
+  if (e.read_c || e.bias_mode != GEMM_BIAS_COL || e.bias_dtype != GEMM_F32 || !e.vec_d ||
+      n0 + 32 * (int64_t)c_end > N)
+    return false;
+  if (e.d_dtype == GEMM_BF16) {
+    if (e.relu) epi_chunks_bias<GEMM_BF16, true>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+    else epi_chunks_bias<GEMM_BF16, false>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+  } else if (e.d_dtype == GEMM_F16) {
+    if (e.relu) epi_chunks_bias<GEMM_F16, true>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+    else epi_chunks_bias<GEMM_F16, false>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+  } else if (e.d_dtype == GEMM_F32) {
+    if (e.relu) epi_chunks_bias<GEMM_F32, true>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+    else epi_chunks_bias<GEMM_F32, false>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+  } else {
+    return false;
+  }
+  return true;
+}
+
 // The plain epilogue applies: returns false (nothing done) otherwise.
 template <typename Acc>
 __device__ __forceinline__ bool epi_chunks_plain_any(const EpiParams& e, void* D, int64_t m0, int64_t n0, int64_t N,

@@ -470,7 +470,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
           if (c32) {
             epi_chunks_c32(p.epi, ptr, m - lane, n0, p.M, stage_buf, 0, chunks, acc);
           } else if (cp_last >= cp_first ||
-                     !epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc)) {
+                     (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc) &&
+                      !epi_chunks_bias_any(p.epi, ptr, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc))) {
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
               uint32_t r[32];

@@ -497,7 +497,8 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
                          !p.epi.relu && n0 + 32 * (c0 + CHUNKS) <= p.N;
         if (c32) {
           epi_chunks_c32(p.epi, ptr, m - lane, n0, p.M, stage_buf, c0, c0 + CHUNKS, acc);
-        } else if (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
+        } else if (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc) &&
+                   !epi_chunks_bias_any(p.epi, ptr, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
 #pragma unroll 1
           for (int c = c0; c < c0 + CHUNKS; ++c) {
             uint32_t r[32];
