@@ -611,14 +611,35 @@ __device__ __forceinline__ void epi_chunks_bias(const EpiParams& e, const EpiPtr
   }
 }
 
-// The fully connected epilogue applies (see epi_chunks_bias): returns false otherwise.
+// The common epilogues of a warp's chunks [c_begin, c_end) (columns n0 + 32c ...,
+// m0 = the warp's first row) in loops specialised on D's type:
+//   - fp32 C and D, no bias or ReLU;
+//   - plain: no C, bias or ReLU;
+//   - an fp32 column bias with or without ReLU, no C.
+// Each applies only when every chunk lies inside D (and C) and D's (and C's) rows
+// take 16-byte vector accesses.  Returns false, having done nothing, for every
+// other epilogue, which then takes the general per-chunk path.
 template <typename Acc>
-__device__ __forceinline__ bool epi_chunks_bias_any(const EpiParams& e, const EpiPtrs& ptr, int64_t m0, int64_t n0,
-                                                    int64_t N, int64_t M, uint32_t stage, int c_begin, int c_end,
-                                                    Acc&& acc) {
-  if (e.read_c || e.bias_mode != GEMM_BIAS_COL || e.bias_dtype != GEMM_F32 || !e.vec_d ||
-      n0 + 32 * (int64_t)c_end > N)
+__device__ __forceinline__ bool epi_chunks_typed(const EpiParams& e, const EpiPtrs& ptr, int64_t m0, int64_t n0,
+                                                 int64_t N, int64_t M, uint32_t stage, int c_begin, int c_end,
+                                                 Acc&& acc) {
+  if (!e.vec_d || n0 + 32 * (int64_t)c_end > N) return false;
+  if (e.read_c) {
+    if (e.vec_c && !e.c_relu && e.c_dtype == GEMM_F32 && e.d_dtype == GEMM_F32 && e.bias_mode == GEMM_BIAS_NONE &&
+        !e.relu) {
+      epi_chunks_c32(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
+      return true;
+    }
     return false;
+  }
+  if (e.bias_mode == GEMM_BIAS_NONE && !e.relu) {
+    if (e.d_dtype == GEMM_F32) epi_chunks_plain<GEMM_F32>(ptr.D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
+    else if (e.d_dtype == GEMM_F16) epi_chunks_plain<GEMM_F16>(ptr.D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
+    else if (e.d_dtype == GEMM_BF16) epi_chunks_plain<GEMM_BF16>(ptr.D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
+    else return false;
+    return true;
+  }
+  if (e.bias_mode != GEMM_BIAS_COL || e.bias_dtype != GEMM_F32) return false;
   if (e.d_dtype == GEMM_BF16) {
     if (e.relu) epi_chunks_bias<GEMM_BF16, true>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
     else epi_chunks_bias<GEMM_BF16, false>(e, ptr, m0, n0, M, stage, c_begin, c_end, acc);
@@ -631,18 +652,6 @@ __device__ __forceinline__ bool epi_chunks_bias_any(const EpiParams& e, const Ep
   } else {
     return false;
   }
-  return true;
-}
-
-// The plain epilogue applies: returns false (nothing done) otherwise.
-template <typename Acc>
-__device__ __forceinline__ bool epi_chunks_plain_any(const EpiParams& e, void* D, int64_t m0, int64_t n0, int64_t N,
-                                                     int64_t M, uint32_t stage, int c_begin, int c_end, Acc&& acc) {
-  if (e.read_c || e.bias_mode != GEMM_BIAS_NONE || e.relu || !e.vec_d || n0 + 32 * (int64_t)c_end > N) return false;
-  if (e.d_dtype == GEMM_F32) epi_chunks_plain<GEMM_F32>(D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
-  else if (e.d_dtype == GEMM_F16) epi_chunks_plain<GEMM_F16>(D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
-  else if (e.d_dtype == GEMM_BF16) epi_chunks_plain<GEMM_BF16>(D, e.ldd, m0, n0, M, stage, c_begin, c_end, acc);
-  else return false;
   return true;
 }
 

@@ -456,7 +456,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
             if (!good) cp_last = cp_first - 1;   // results are void; the error word says why
           }
           const uint32_t stage_buf = out_stage0 + (uint32_t)((warp - 2) * 4096);
-          // A whole tile with the plain epilogue: the loop specialised on D's type.
+          // A whole tile (no later parts to add): the common epilogues run in loops
+          // specialised on D's type, the others on the general per-chunk path.
           auto acc = [&](int c, float (&x)[32]) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
@@ -464,14 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairThreads<INT_MODE
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
           };
-          const bool c32 = cp_last < cp_first && p.epi.read_c && p.epi.vec_c && p.epi.vec_d &&
-                           p.epi.c_dtype == GEMM_F32 && p.epi.d_dtype == GEMM_F32 && !p.epi.c_relu &&
-                           p.epi.bias_mode == GEMM_BIAS_NONE && !p.epi.relu && n0 + 32 * chunks <= p.N;
-          if (c32) {
-            epi_chunks_c32(p.epi, ptr, m - lane, n0, p.M, stage_buf, 0, chunks, acc);
-          } else if (cp_last >= cp_first ||
-                     (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc) &&
-                      !epi_chunks_bias_any(p.epi, ptr, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc))) {
+          if (cp_last >= cp_first ||
+              !epi_chunks_typed(p.epi, ptr, m - lane, n0, p.N, p.M, stage_buf, 0, chunks, acc)) {
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
               uint32_t r[32];

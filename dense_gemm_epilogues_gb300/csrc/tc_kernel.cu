@@ -484,7 +484,8 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + (uint32_t)(buf * BN);
         const uint32_t stage_buf = out_stage0 + (uint32_t)((warp - 2) * 4096);
-        // The plain epilogue: the loop specialised on D's type.
+        // The common epilogues in loops specialised on D's type, the others on the
+        // general per-chunk path.
         auto acc = [&](int c, float (&x)[32]) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tb + (uint32_t)(c * 32), r);
@@ -492,13 +493,7 @@ __global__ void __launch_bounds__(TcThreads<INT_MODE, XF>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * p.epi.alpha;
         };
-        const bool c32 = p.epi.read_c && p.epi.vec_c && p.epi.vec_d && p.epi.c_dtype == GEMM_F32 &&
-                         p.epi.d_dtype == GEMM_F32 && !p.epi.c_relu && p.epi.bias_mode == GEMM_BIAS_NONE &&
-                         !p.epi.relu && n0 + 32 * (c0 + CHUNKS) <= p.N;
-        if (c32) {
-          epi_chunks_c32(p.epi, ptr, m - lane, n0, p.M, stage_buf, c0, c0 + CHUNKS, acc);
-        } else if (!epi_chunks_plain_any(p.epi, ptr.D, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc) &&
-                   !epi_chunks_bias_any(p.epi, ptr, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
+        if (!epi_chunks_typed(p.epi, ptr, m - lane, n0, p.N, p.M, stage_buf, c0, c0 + CHUNKS, acc)) {
 #pragma unroll 1
           for (int c = c0; c < c0 + CHUNKS; ++c) {
             uint32_t r[32];
