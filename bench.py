@@ -1030,6 +1030,7 @@ def _cases():
         "int8_4096": I.int8_8192().with_(name="gemm_s8_tn_4096", M=4096, N=4096, K=4096),
         "int8_8192": I.int8_8192(),
         "square2048": I.square_fp16(2048),
+        "square4096_k1024": I.square_fp16(4096).with_(name="gemm_f16_tn_4096x4096x1024", K=1024, d="f16"),
         "sgemm4096": I.sgemm_4096_bias_relu(),
         "skinny": I.skinny_fp16_16384x64x16384(),
     }
