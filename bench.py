@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
-                    help="skip the per-workload measurements of the other BASELINE configs")
+                    help="skip the per-workload measurements of the other benchmark workloads")
     ap.add_argument("--case", default=None,
                     help="run one named workload --iters times (profiling driver); see CASES")
     ap.add_argument("--iters", type=int, default=3)
@@ -671,7 +671,8 @@ def run_transform_suite(G, device, iters=10):
         torch.cuda.empty_cache()
 
 
-# Every workload BASELINE names beside the contract's, measured in the default
+# Every benchmark workload beside the contract's (the FC layer, int8, SGEMM, the
+# square sweep and the skinny GEMM), measured in the default
 # run: (problem constructor, seed offset, bound of its roofline).
 def config_workloads():
     from dense_gemm_epilogues_gb300 import inputs as I
@@ -700,7 +701,7 @@ def ffma_peak_tflops(sm_count: int, sm_mhz: float) -> float:
 
 
 def measure_configs(G, device, gpu_id, min_region_s=0.4, max_iters=3000):
-    """One record per BASELINE workload: mean device time per call from CUDA
+    """One record per benchmark workload: mean device time per call from CUDA
     events on the launching stream around `iters` back-to-back calls, with its
     own clock record and roofline.  A workload whose inputs and output fit in L2 rotates over enough
     copies of them (different addresses, same values) that the copies together
