@@ -676,12 +676,12 @@ def run_transform_suite(G, device, iters=10):
 # run: (problem constructor, seed offset, bound of its roofline).
 def config_workloads():
     from dense_gemm_epilogues_gb300 import inputs as I
-    out = [("cfg1_gemm_f16_tn_256", I.square_fp16_256(), 0, "tensor"),
-           ("cfg3_fc_bf16_8192x4096x11008_bias_relu", I.fc_bf16_8192x4096x11008(), 2, "tensor"),
-           ("cfg4_gemm_s8_tn_8192", I.int8_8192(), 3, "tensor"),
-           ("cfg5a_sgemm_f32_tn_4096_bias_relu", I.sgemm_4096_bias_relu(), 4, "alu")]
-    out += [(f"cfg5b_gemm_f16_tn_{n}", I.square_fp16(n), 5, "tensor") for n in (512, 1024, 2048, 4096, 16384)]
-    out += [("cfg5c_gemm_f16_tn_skinny_16384x64x16384", I.skinny_fp16_16384x64x16384(), 6, "hbm")]
+    out = [("gemm_f16_tn_256", I.square_fp16_256(), 0, "tensor"),
+           ("fc_bf16_8192x4096x11008_bias_relu", I.fc_bf16_8192x4096x11008(), 2, "tensor"),
+           ("gemm_s8_tn_8192", I.int8_8192(), 3, "tensor"),
+           ("sgemm_f32_tn_4096_bias_relu", I.sgemm_4096_bias_relu(), 4, "alu")]
+    out += [(f"sweep_gemm_f16_tn_{n}", I.square_fp16(n), 5, "tensor") for n in (512, 1024, 2048, 4096, 16384)]
+    out += [("skinny_gemm_f16_tn_16384x64x16384", I.skinny_fp16_16384x64x16384(), 6, "hbm")]
     return out
 
 

@@ -55,9 +55,9 @@ def test_default_run_measures_every_other_workload():
     # config 1, the FC layer, int8, SGEMM, the five squares of the sweep, the skinny shape
     assert len(names) == 10 and len(set(names)) == 10
     bounds = {w[0]: w[3] for w in bench.config_workloads()}
-    assert bounds["cfg5c_gemm_f16_tn_skinny_16384x64x16384"] == "hbm"
-    assert bounds["cfg5a_sgemm_f32_tn_4096_bias_relu"] == "alu"
-    sweep = sorted(w[1].M for w in bench.config_workloads() if w[0].startswith("cfg5b"))
+    assert bounds["skinny_gemm_f16_tn_16384x64x16384"] == "hbm"
+    assert bounds["sgemm_f32_tn_4096_bias_relu"] == "alu"
+    sweep = sorted(w[1].M for w in bench.config_workloads() if w[0].startswith("sweep_"))
     assert sweep == [512, 1024, 2048, 4096, 16384]
 
 
