@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--case", default=None,
                     help="run one named workload --iters times (profiling driver); see CASES")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--vs-cublas", action="store_true",
+                    help="time the library against torch.matmul / F.linear (cuBLAS) on the square "
+                         "sweep, a short-K shape and the FC layer; a comparison, not a contract line")
     return ap.parse_args()
 
 
@@ -558,6 +561,7 @@ def run_suite(G, device, warmup=3, iters=20):
         t_graph = None
         try:
             side = torch.cuda.Stream(device)
+            side.wait_stream(torch.cuda.current_stream(device))
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.stream(side):
                 gr.capture_begin()
@@ -622,6 +626,7 @@ def run_transform_suite(G, device, iters=10):
 
         def graph_us(epi):
             side = torch.cuda.Stream(device)
+            side.wait_stream(torch.cuda.current_stream(device))   # the inputs were copied on the current stream
 
             def call():
                 G.gemm_run(plan.handle, G.LAYOUT_CODES[p.layout_a], G.LAYOUT_CODES[p.layout_b], p.M, p.N, p.K,
@@ -844,6 +849,7 @@ def run_batched_suite(G, device, warmup=3, iters=20):
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / iters
         side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
             gr.capture_begin()
@@ -922,6 +928,7 @@ def run_diag_suite(G, device, warmup=3, iters=20, sets=4):
             torch.cuda.synchronize()
             t = e0.elapsed_time(e1) / 1e3 / iters
             side = torch.cuda.Stream(device)
+            side.wait_stream(torch.cuda.current_stream(device))
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.stream(side):
                 gr.capture_begin()
@@ -989,6 +996,7 @@ def run_pair_suite(G, device, warmup=3, iters=20):
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / iters
         side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
             gr.capture_begin()
@@ -1105,11 +1113,110 @@ def run_case(name: str, iters: int):
     plan.close()
 
 
+def _graph_us(device, call, iters=20, replays=5):
+    """GPU time per call: `iters` calls captured in one CUDA graph on a side
+    stream, the best of `replays` replays timed with CUDA events."""
+    import torch
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))   # the inputs were written on the current stream
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call(side)
+    side.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        gr.capture_begin()
+        for _ in range(iters):
+            call(side)
+        gr.capture_end()
+    side.synchronize()
+    best = float("inf")
+    for _ in range(replays):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            e0.record(side)
+            gr.replay()
+            e1.record(side)
+        side.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1000.0 / iters)
+    del gr
+    return best
+
+
+def run_vs_cublas():
+    """The library against cuBLAS (torch.matmul; F.linear + relu_ for the FC
+    layer) on the same inputs, both graph-timed, one JSON line per shape, in
+    increasing size with the short-K shape before the long ones (a long shape
+    changes the clock state the next one starts in).  fp16 in and out, TN;
+    every library result is checked against the fp32 product."""
+    import torch
+    import torch.nn.functional as F
+    import dense_gemm_epilogues_gb300 as G
+    G.load_library()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    for (M, N, K) in [(256,) * 3, (512,) * 3, (1024,) * 3, (2048,) * 3, (4096, 4096, 1024), (3072,) * 3,
+                      (4096,) * 3, (8192,) * 3]:
+        A = (torch.rand(M, K, device=dev, generator=g) * 2 - 1).half()
+        B = (torch.rand(N, K, device=dev, generator=g) * 2 - 1).half()
+        D = torch.empty(M, N, device=dev, dtype=torch.float16)
+        plan = G.Plan(G.GEMM_F16, G.GEMM_F32, 0)
+        epi = G.make_epilogue(G.GEMM_F16)
+
+        def lib(st):
+            G.gemm_run(plan.handle, G.GEMM_OP_T, G.GEMM_OP_N, M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), K,
+                       0.0, None, 0, D.data_ptr(), N, epi, st.cuda_stream)
+        Bt = B.t()
+
+        def cub(st):
+            torch.matmul(A, Bt)
+        t_lib = _graph_us(dev, lib)
+        torch.cuda.synchronize()
+        nonfinite = int((~torch.isfinite(D)).sum())
+        ref = torch.matmul(A.float(), B.float().t())
+        err = ((D.float() - ref).abs() / (ref.abs() + 1)).max().item()
+        del ref
+        t_cub = _graph_us(dev, cub)
+        print(json.dumps({"vs_cublas": f"{M}x{N}x{K}", "lib_us": round(t_lib, 2), "cublas_us": round(t_cub, 2),
+                          "lib_tflops": round(2 * M * N * K / t_lib / 1e6, 1),
+                          "cublas_tflops": round(2 * M * N * K / t_cub / 1e6, 1),
+                          "kernel": plan.last_config()["kernel_name"], "max_rel_err": err,
+                          "nonfinite": nonfinite, "status": plan.device_status()}), flush=True)
+        plan.close()
+    M, K, N = 8192, 4096, 11008
+    X = torch.randn(M, K, device=dev, generator=g).bfloat16()
+    W = (torch.randn(K, N, device=dev, generator=g) * 0.02).bfloat16()
+    bias = torch.randn(N, device=dev, generator=g) * 0.1
+    bias16 = bias.bfloat16()
+    D = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+    plan = G.Plan(G.GEMM_BF16, G.GEMM_F32, 0)
+    epi = G.make_epilogue(G.GEMM_BF16, bias.data_ptr(), G.GEMM_F32, G.GEMM_BIAS_COL, G.GEMM_ACT_RELU)
+
+    def lib_fc(st):
+        G.gemm_run(plan.handle, G.GEMM_OP_T, G.GEMM_OP_T, M, N, K, 1.0, X.data_ptr(), K, W.data_ptr(), N, 0.0,
+                   None, 0, D.data_ptr(), N, epi, st.cuda_stream)
+    Wt = W.t().contiguous()
+
+    def cub_fc(st):
+        torch.relu_(F.linear(X, Wt, bias16))
+    t_lib, t_cub = _graph_us(dev, lib_fc), _graph_us(dev, cub_fc)
+    print(json.dumps({"vs_cublas": "fc_8192x11008x4096_bias_relu", "lib_us": round(t_lib, 2),
+                      "cublas_us": round(t_cub, 2), "lib_tflops": round(2 * M * N * K / t_lib / 1e6, 1),
+                      "cublas_tflops": round(2 * M * N * K / t_cub / 1e6, 1),
+                      "kernel": plan.last_config()["kernel_name"], "status": plan.device_status()}), flush=True)
+    plan.close()
+
+
 def main():
     args = parse_args()
     rank, world, local_rank = dist_info()
     if args.case:
         run_case(args.case, args.iters)
+        return
+    if args.vs_cublas:
+        run_vs_cublas()
         return
     if args.impl == "reference":
         bench_reference(args, rank, world)
