@@ -74,3 +74,15 @@ def test_theoretical_peak_at_the_ncu_clock():
     assert 1900 < t["peak"] < 2100 and 0.8 < t["frac"] < 0.95, t
     assert abs(t["frac"] - c["tensor_pipe_active_pct"] / 100.0) < 0.02, t
     assert bench.theoretical_at_clock({}, 1.0, 152) is None
+
+
+def test_vs_cublas_mode_is_a_separate_entry(monkeypatch):
+    """--vs-cublas selects the comparison routine, which prints no contract line, and
+    its graph helper orders its side stream after the stream that wrote the inputs."""
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--vs-cublas"])
+    args = bench.parse_args()
+    assert args.vs_cublas and args.case is None
+    import inspect
+    src = inspect.getsource(bench._graph_us)
+    assert "wait_stream" in src
+    assert "run_vs_cublas" in inspect.getsource(bench.main)
